@@ -1,0 +1,234 @@
+/*
+ * mbk_oracle.c -- plain CPU reference of batch-1 Llama-shaped decode.
+ * TEST INFRASTRUCTURE ONLY (see mbk_oracle.h): the product path never links or calls it.
+ *
+ * Written for readability, not speed: one output element per loop iteration, double
+ * accumulation, no blocking or fusion beyond what each op's definition states.  OpenMP
+ * (when compiled in) only splits independent output rows or heads across threads, so the
+ * result does not depend on the thread count.
+ */
+#include "mbk_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int orc_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+static int threads_for(int nthreads) { return nthreads > 0 ? nthreads : orc_max_threads(); }
+
+/* bf16 is the upper half of an IEEE binary32. */
+float orc_bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+uint16_t orc_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0) /* NaN: keep it a quiet NaN */
+    return (uint16_t)((u >> 16) | 0x0040u);
+  /* round to nearest, ties to even: add 0x7fff plus the lowest kept bit, then truncate */
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+/* RMSNorm (article, "How a model gets in": the rms_norm region; Hugging Face Llama
+ * definition): x / sqrt(mean(x^2) + eps) * gain. */
+void orc_rmsnorm(const float *x, const uint16_t *g, int n, double eps, float *out) {
+  double ss = 0.0;
+  for (int i = 0; i < n; ++i) ss += (double)x[i] * (double)x[i];
+  double inv = 1.0 / sqrt(ss / (double)n + eps);
+  for (int i = 0; i < n; ++i) {
+    double gi = g ? (double)orc_bf16_to_f32(g[i]) : 1.0;
+    out[i] = (float)((double)x[i] * inv * gi);
+  }
+}
+
+/* A projection at batch 1 is a matrix-vector product over the [out, in] weight; the
+ * q/k/v bias (README, "Current status": addmm biases) is added to the exact sum. */
+void orc_gemv(const uint16_t *W, const float *x, const uint16_t *b, int rows, int cols, float *y, int nthreads) {
+  int nt = threads_for(nthreads);
+  (void)nt;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nt) schedule(static)
+#endif
+  for (int r = 0; r < rows; ++r) {
+    const uint16_t *w = W + (size_t)r * cols;
+    double acc = 0.0;
+    for (int k = 0; k < cols; ++k) acc += (double)orc_bf16_to_f32(w[k]) * (double)x[k];
+    if (b) acc += (double)orc_bf16_to_f32(b[r]);
+    y[r] = (float)acc;
+  }
+}
+
+/* RoPE (article, "How a model gets in": the rope region).  Rotate-half pairing as in
+ * Hugging Face Llama: element i pairs with element i + d/2, frequency theta^(-2i/d). */
+void orc_rope(float *v, int n_heads, int d, int pos, double theta) {
+  int half = d / 2;
+  for (int h = 0; h < n_heads; ++h) {
+    float *x = v + (size_t)h * d;
+    for (int i = 0; i < half; ++i) {
+      double inv_freq = pow(theta, -(2.0 * (double)i) / (double)d);
+      double ang = (double)pos * inv_freq;
+      double c = cos(ang), s = sin(ang);
+      double a = x[i], b = x[i + half];
+      x[i] = (float)(a * c - b * s);
+      x[i + half] = (float)(b * c + a * s);
+    }
+  }
+}
+
+/* Decode attention over the static cache (README, "Current status": decode attention with
+ * the query heads that share a KV head reading the same cached keys and values).
+ * Plain softmax(q K^T / sqrt(d)) V per query head, with the maximum subtracted. */
+void orc_attention(const float *q, const uint16_t *K, const uint16_t *V, int nq, int nkv, int d, int cap, int ctx,
+                   float *o, int nthreads) {
+  int group = nq / nkv;
+  int nt = threads_for(nthreads);
+  (void)nt;
+  double scale = 1.0 / sqrt((double)d);
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nt) schedule(static)
+#endif
+  for (int h = 0; h < nq; ++h) {
+    int kv = h / group;
+    const float *qh = q + (size_t)h * d;
+    const uint16_t *Kh = K + (size_t)kv * cap * d;
+    const uint16_t *Vh = V + (size_t)kv * cap * d;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1));
+    double m = -INFINITY;
+    for (int j = 0; j < ctx; ++j) {
+      double acc = 0.0;
+      for (int t = 0; t < d; ++t) acc += (double)qh[t] * (double)orc_bf16_to_f32(Kh[(size_t)j * d + t]);
+      s[j] = acc * scale;
+      if (s[j] > m) m = s[j];
+    }
+    double z = 0.0;
+    for (int j = 0; j < ctx; ++j) {
+      s[j] = exp(s[j] - m);
+      z += s[j];
+    }
+    for (int t = 0; t < d; ++t) {
+      double acc = 0.0;
+      for (int j = 0; j < ctx; ++j) acc += s[j] * (double)orc_bf16_to_f32(Vh[(size_t)j * d + t]);
+      o[(size_t)h * d + t] = ctx > 0 ? (float)(acc / z) : 0.0f;
+    }
+    free(s);
+  }
+}
+
+/* Gated activation (article, "How a model gets in": the fused SiLU-mul region). */
+void orc_silu_mul(const float *g, const float *u, int n, float *h) {
+  for (int i = 0; i < n; ++i) {
+    double z = g[i];
+    double silu = z / (1.0 + exp(-z));
+    h[i] = (float)(silu * (double)u[i]);
+  }
+}
+
+void orc_kv_fill(const orc_config *cfg, uint16_t *kv_layer, const float *k_raw, const float *v_raw, int p0, int n) {
+  int nkv = cfg->n_kv_heads, d = cfg->head_dim, cap = cfg->kv_capacity;
+  uint16_t *Kc = kv_layer;
+  uint16_t *Vc = kv_layer + (size_t)nkv * cap * d;
+  float *tmp = (float *)malloc(sizeof(float) * (size_t)d);
+  for (int h = 0; h < nkv; ++h) {
+    for (int i = 0; i < n; ++i) {
+      int p = p0 + i;
+      const float *kr = k_raw + ((size_t)h * n + i) * d;
+      const float *vr = v_raw + ((size_t)h * n + i) * d;
+      memcpy(tmp, kr, sizeof(float) * (size_t)d);
+      orc_rope(tmp, 1, d, p, cfg->rope_theta);
+      for (int t = 0; t < d; ++t) {
+        Kc[((size_t)h * cap + p) * d + t] = orc_f32_to_bf16(tmp[t]);
+        Vc[((size_t)h * cap + p) * d + t] = orc_f32_to_bf16(vr[t]);
+      }
+    }
+  }
+  free(tmp);
+}
+
+static int config_ok(const orc_config *c) {
+  if (c->n_layers <= 0 || c->hidden <= 0 || c->intermediate <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0) return 0;
+  if (c->head_dim <= 0 || (c->head_dim % 2) != 0 || c->vocab <= 0 || c->kv_capacity <= 0) return 0;
+  if (c->n_heads % c->n_kv_heads != 0) return 0;
+  return 1;
+}
+
+/* One decode step, in the order the article's section "What a megakernel is, and why small
+ * models want one" lists the ops, with the embedding at the start and the final norm and
+ * tied vocabulary projection at the end (README, "Current status"). */
+int orc_decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                    uint16_t *kv_cache, int token, int pos, float *logits, float *taps, int nthreads) {
+  if (!cfg || !embed || !layers || !kv_cache || !logits || !config_ok(cfg)) return -1;
+  if (token < 0 || token >= cfg->vocab || pos < 0 || pos >= cfg->kv_capacity) return -1;
+  const int L = cfg->n_layers, H = cfg->hidden, I = cfg->intermediate;
+  const int nq = cfg->n_heads, nkv = cfg->n_kv_heads, d = cfg->head_dim, cap = cfg->kv_capacity;
+  const size_t qdim = (size_t)nq * d, kvdim = (size_t)nkv * d;
+
+  float *x = (float *)malloc(sizeof(float) * H);
+  float *xn = (float *)malloc(sizeof(float) * H);
+  float *y = (float *)malloc(sizeof(float) * H);
+  float *q = (float *)malloc(sizeof(float) * qdim);
+  float *k = (float *)malloc(sizeof(float) * kvdim);
+  float *v = (float *)malloc(sizeof(float) * kvdim);
+  float *o = (float *)malloc(sizeof(float) * qdim);
+  float *g = (float *)malloc(sizeof(float) * I);
+  float *u = (float *)malloc(sizeof(float) * I);
+  float *hbuf = (float *)malloc(sizeof(float) * I);
+
+  /* embedding: the token's row of E, widened to fp32 */
+  for (int i = 0; i < H; ++i) x[i] = orc_bf16_to_f32(embed[(size_t)token * H + i]);
+  if (taps) memcpy(taps, x, sizeof(float) * H);
+
+  for (int l = 0; l < L; ++l) {
+    const orc_layer *w = &layers[l];
+    uint16_t *Kc = kv_cache + (size_t)l * 2 * nkv * cap * d;
+    uint16_t *Vc = Kc + (size_t)nkv * cap * d;
+
+    /* attention sublayer */
+    orc_rmsnorm(x, w->attn_norm, H, cfg->rms_eps, xn);
+    orc_gemv(w->wq, xn, cfg->qkv_bias ? w->bq : NULL, nq * d, H, q, nthreads);
+    orc_gemv(w->wk, xn, cfg->qkv_bias ? w->bk : NULL, nkv * d, H, k, nthreads);
+    orc_gemv(w->wv, xn, cfg->qkv_bias ? w->bv : NULL, nkv * d, H, v, nthreads);
+    orc_rope(q, nq, d, pos, cfg->rope_theta);
+    orc_rope(k, nkv, d, pos, cfg->rope_theta);
+    for (int h = 0; h < nkv; ++h)
+      for (int t = 0; t < d; ++t) {
+        Kc[((size_t)h * cap + pos) * d + t] = orc_f32_to_bf16(k[(size_t)h * d + t]);
+        Vc[((size_t)h * cap + pos) * d + t] = orc_f32_to_bf16(v[(size_t)h * d + t]);
+      }
+    orc_attention(q, Kc, Vc, nq, nkv, d, cap, pos + 1, o, nthreads);
+    orc_gemv(w->wo, o, NULL, H, nq * d, y, nthreads);
+    for (int i = 0; i < H; ++i) x[i] = (float)((double)x[i] + (double)y[i]);
+    if (taps) memcpy(taps + (size_t)(2 * l + 1) * H, x, sizeof(float) * H);
+
+    /* MLP sublayer */
+    orc_rmsnorm(x, w->mlp_norm, H, cfg->rms_eps, xn);
+    orc_gemv(w->w_gate, xn, NULL, I, H, g, nthreads);
+    orc_gemv(w->w_up, xn, NULL, I, H, u, nthreads);
+    orc_silu_mul(g, u, I, hbuf);
+    orc_gemv(w->w_down, hbuf, NULL, H, I, y, nthreads);
+    for (int i = 0; i < H; ++i) x[i] = (float)((double)x[i] + (double)y[i]);
+    if (taps) memcpy(taps + (size_t)(2 * l + 2) * H, x, sizeof(float) * H);
+  }
+
+  /* final norm, then the tied vocabulary projection (the embedding matrix) */
+  orc_rmsnorm(x, final_norm, H, cfg->rms_eps, xn);
+  orc_gemv(embed, xn, NULL, cfg->vocab, H, logits, nthreads);
+
+  free(x); free(xn); free(y); free(q); free(k); free(v); free(o); free(g); free(u); free(hbuf);
+  return 0;
+}

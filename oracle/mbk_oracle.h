@@ -1,0 +1,96 @@
+/*
+ * mbk_oracle.h -- plain, slow, CPU reference of batch-1 Llama-shaped decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library or its
+ * Python binding) may include, link, load or call this code; only the tests, the
+ * package's smoke check and the benchmark's CPU-baseline leg use it.  It shares no
+ * code, header, table or constant with the CUDA path.
+ *
+ * What it computes is the decoder the MegaBake pages describe, op by op:
+ *   "MegaBake: a PyTorch model compiled into one CUDA kernel, and what its 5.5x is
+ *    measured against" (the "article"), section "What a megakernel is, and why small
+ *    models want one": per layer an RMSNorm, the Q/K/V projections, RoPE, attention,
+ *    the output projection, a residual add, a second norm, gate and up projections,
+ *    SiLU, the down projection and a second residual add; and the megabake/megabake
+ *    README ("Current status"): embedding, every layer, final norm, vocabulary
+ *    projection and the KV-cache update, with a static contiguous decode KV cache.
+ * The pages give the op list but no formulas; the formulas below are the textbook
+ * (Hugging Face Llama) definitions of those ops.
+ *
+ * Precision (the pages are silent; this is the reading taken): weights and the KV
+ * cache are bf16; every activation is stored as fp32; every reduction (dot product,
+ * sum of squares, softmax sum) is accumulated in double and each op's result is
+ * rounded once to fp32.  Only K and V are rounded to bf16 (round to nearest even)
+ * when they are written into the cache; attention reads the rounded cache, including
+ * the row just written.
+ *
+ * Parity pins for each function are listed beside it.  Whole-decoder parity with the
+ * pages' own numbers is unpinned: the pages publish no weights or outputs.
+ */
+#ifndef MBK_ORACLE_H
+#define MBK_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int n_layers, hidden, intermediate, n_heads, n_kv_heads, head_dim, vocab, kv_capacity;
+  double rms_eps, rope_theta;
+  int qkv_bias;
+} orc_config;
+
+/* bf16 tensors are passed as their raw 16-bit patterns; matrices are [out, in] row-major. */
+typedef struct {
+  const uint16_t *attn_norm, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
+} orc_layer;
+
+/* ---- building blocks (exported so that the tests can pin each one) ---- */
+
+/* bf16 <-> fp32.  orc_f32_to_bf16 rounds to nearest, ties to even (NaN kept quiet). */
+float orc_bf16_to_f32(uint16_t b);
+uint16_t orc_f32_to_bf16(float f);
+
+/* out[i] = x[i] / sqrt(mean(x^2) + eps) * g[i]   (g == NULL means a gain of 1). */
+void orc_rmsnorm(const float *x, const uint16_t *g, int n, double eps, float *out);
+
+/* y[r] = sum_k W[r,k] x[k] (+ b[r])  for r < rows.  W bf16 [rows, cols], b bf16 or NULL. */
+void orc_gemv(const uint16_t *W, const float *x, const uint16_t *b, int rows, int cols, float *y, int nthreads);
+
+/* Rotary embedding, rotate-half convention: for each of n_heads vectors of length d and
+ * each i < d/2, (v[i], v[i+d/2]) is rotated by the angle pos * theta^(-2i/d). */
+void orc_rope(float *v, int n_heads, int d, int pos, double theta);
+
+/* Decode attention for one layer.  q: [nq][d] fp32 (post-RoPE).  K, V: bf16 caches of
+ * one layer laid out [nkv][cap][d].  Query head h reads kv head h / (nq/nkv), keys
+ * j = 0..ctx-1; scores q.K_j / sqrt(d), softmax over j, o_h = sum_j a_j V_j.  o: [nq][d]. */
+void orc_attention(const float *q, const uint16_t *K, const uint16_t *V, int nq, int nkv, int d, int cap, int ctx,
+                   float *o, int nthreads);
+
+/* h[i] = silu(g[i]) * u[i],  silu(z) = z / (1 + exp(-z)). */
+void orc_silu_mul(const float *g, const float *u, int n, float *h);
+
+/* Write cache rows p0..p0+n-1 of one layer from pre-RoPE K and V (fp32, [nkv][n][d]):
+ * K is rotated by its position, both are rounded to bf16.  kv_layer points at the
+ * layer's [2][nkv][cap][d] block. */
+void orc_kv_fill(const orc_config *cfg, uint16_t *kv_layer, const float *k_raw, const float *v_raw, int p0, int n);
+
+/* ---- the whole decode step ----
+ * Embeds `token`, runs every layer at position `pos` (writing cache row `pos` of every
+ * layer, attending over rows 0..pos), applies the final norm and the tied vocabulary
+ * projection.  kv_cache: bf16 [L][2][nkv][cap][d] (K then V per layer).  logits: fp32 [V].
+ * taps (optional, may be NULL): fp32 [(2L+1)][H], the residual stream after the embedding
+ * and after each attention and MLP sublayer.  nthreads <= 0 uses every core OpenMP offers.
+ * Returns 0, or -1 for an invalid argument (nothing is written then). */
+int orc_decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                    uint16_t *kv_cache, int token, int pos, float *logits, float *taps, int nthreads);
+
+/* Number of OpenMP threads the oracle would use for nthreads <= 0 (1 without OpenMP). */
+int orc_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

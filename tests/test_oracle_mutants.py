@@ -1,0 +1,106 @@
+"""Planted mistakes in the oracle (on the CPU only): each mutant is a copy of mbk_oracle.c with one
+plausible bug -- a dropped term, a wrong sign or index, a transposed operand -- and the pins of
+oracle_pins.py must reject every one of them.  This shows the pins constrain each part of the
+oracle, not just its overall shape."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle_pins as pins
+from oracle import OracleDecoder
+from oracle.oracle import GCC_FLAGS, bind
+from persistent_decode_megakernel_gb300 import workloads
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "mbk_oracle.c")
+
+# (name, text to find, replacement, occurrence index or None for "exactly one occurrence")
+MUTANTS = [
+    ("rope_sign", "x[i] = (float)(a * c - b * s);", "x[i] = (float)(a * c + b * s);", None),
+    ("rope_frequency", "-(2.0 * (double)i) / (double)d", "-(1.0 * (double)i) / (double)d", None),
+    ("rope_pairing", "double a = x[i], b = x[i + half];", "double a = x[i], b = x[half - 1 - i];", None),
+    ("attn_scale_dropped", "s[j] = acc * scale;", "s[j] = acc;", None),
+    ("gqa_mapping", "int kv = h / group;", "int kv = h % nkv;", None),
+    ("attn_reads_k_as_v", "acc += s[j] * (double)orc_bf16_to_f32(Vh[(size_t)j * d + t]);",
+     "acc += s[j] * (double)orc_bf16_to_f32(Kh[(size_t)j * d + t]);", None),
+    ("attn_excludes_current_row", "orc_attention(q, Kc, Vc, nq, nkv, d, cap, pos + 1, o, nthreads);",
+     "orc_attention(q, Kc, Vc, nq, nkv, d, cap, pos > 0 ? pos : 1, o, nthreads);", None),
+    ("rms_eps_dropped", "sqrt(ss / (double)n + eps)", "sqrt(ss / (double)n + 100.0 * eps)", None),
+    ("rms_sum_not_mean", "sqrt(ss / (double)n + eps)", "sqrt(ss + eps)", None),
+    ("rms_gain_dropped", "double gi = g ? (double)orc_bf16_to_f32(g[i]) : 1.0;", "double gi = 1.0;", None),
+    ("gemv_transposed", "acc += (double)orc_bf16_to_f32(w[k]) * (double)x[k];",
+     "acc += (double)orc_bf16_to_f32(W[(size_t)k * rows + r]) * (double)x[k];", None),
+    ("bias_dropped", "if (b) acc += (double)orc_bf16_to_f32(b[r]);", "(void)b;", None),
+    ("attn_residual_dropped", "for (int i = 0; i < H; ++i) x[i] = (float)((double)x[i] + (double)y[i]);",
+     "for (int i = 0; i < H; ++i) x[i] = y[i];", 0),
+    ("mlp_residual_dropped", "for (int i = 0; i < H; ++i) x[i] = (float)((double)x[i] + (double)y[i]);",
+     "for (int i = 0; i < H; ++i) x[i] = y[i];", 1),
+    ("silu_is_sigmoid", "double silu = z / (1.0 + exp(-z));", "double silu = 1.0 / (1.0 + exp(-z));", None),
+    ("gate_up_swapped", "orc_silu_mul(g, u, I, hbuf);", "orc_silu_mul(u, g, I, hbuf);", None),
+    ("bf16_truncates", "u += 0x7fffu + lsb;", "u += 0u * lsb;", None),
+    ("k_cached_unrotated", "orc_rope(k, nkv, d, pos, cfg->rope_theta);", "(void)0;", None),
+    ("final_norm_gain_dropped", "orc_rmsnorm(x, final_norm, H, cfg->rms_eps, xn);", "orc_rmsnorm(x, NULL, H, cfg->rms_eps, xn);", None),
+    ("v_row_from_k", "Vc[((size_t)h * cap + pos) * d + t] = orc_f32_to_bf16(v[(size_t)h * d + t]);",
+     "Vc[((size_t)h * cap + pos) * d + t] = orc_f32_to_bf16(k[(size_t)h * d + t]);", None),
+]
+
+
+def _mutate(src: str, find: str, repl: str, occ):
+    n = src.count(find)
+    if occ is None:
+        assert n == 1, f"mutation site must be unique, found {n}"
+        return src.replace(find, repl)
+    assert n > occ
+    idx = -1
+    for _ in range(occ + 1):
+        idx = src.index(find, idx + 1)
+    return src[:idx] + repl + src[idx + len(find):]
+
+
+def _build(tmp_path, name, text):
+    c = tmp_path / f"{name}.c"
+    c.write_text(text)
+    hdr_dir = os.path.dirname(SRC)
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc"] + GCC_FLAGS + ["-I", hdr_dir, "-o", str(so), str(c), "-lm"], check=True)
+    return bind(ctypes.CDLL(str(so)))
+
+
+@pytest.fixture(scope="module")
+def decoders():
+    tiny = workloads.generate("tiny", seed=0)
+    gains = workloads.generate("tiny", seed=1, random_gains=True)
+    bias = workloads.generate(workloads.scaled_down(workloads.SHAPES["qwen2-0.5b"], n_layers=2, hidden=128,
+                                                    intermediate=320, n_heads=6, n_kv_heads=2, vocab=512,
+                                                    kv_capacity=32, steps=4), seed=3)
+    return tiny, gains, bias
+
+
+def _all_pins(lib, decoders):
+    tiny, gains, bias = decoders
+    checks = [
+        lambda: pins.pin_bf16_rounding(lib), lambda: pins.pin_rmsnorm(lib), lambda: pins.pin_gemv(lib),
+        lambda: pins.pin_rope(lib), lambda: pins.pin_attention(lib), lambda: pins.pin_silu_mul(lib),
+        lambda: pins.pin_decoder_vs_torch(lib, tiny, 4, lambda wl: OracleDecoder(wl, lib=lib)),
+        lambda: pins.pin_decoder_vs_torch(lib, gains, 3, lambda wl: OracleDecoder(wl, lib=lib)),
+        lambda: pins.pin_decoder_vs_torch(lib, bias, 3, lambda wl: OracleDecoder(wl, lib=lib)),
+    ]
+    failed = []
+    for i, chk in enumerate(checks):
+        try:
+            chk()
+        except AssertionError:
+            failed.append(i)
+    return failed
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path, decoders):
+    lib = _build(tmp_path, "clean", open(SRC).read())
+    assert _all_pins(lib, decoders) == []
+
+
+@pytest.mark.parametrize("name,find,repl,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, decoders, name, find, repl, occ):
+    lib = _build(tmp_path, name, _mutate(open(SRC).read(), find, repl, occ))
+    assert _all_pins(lib, decoders), f"mutant {name} passed every pin"
