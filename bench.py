@@ -1,0 +1,313 @@
+"""Benchmark: batch-1 decode tokens/s and achieved HBM GB/s as a fraction of the GB300 roofline.
+
+One bench step is one decode step (one token: embedding, every layer, final norm, LM head) of the
+SmolLM-135M-shaped decoder (30 layers, hidden 576, 9/3 heads, vocab 49152, static 128-entry KV
+cache), teacher-forced over seeded uniform token ids at positions 0..127 (cycling), random-init
+bf16 weights ~N(0, 0.02).  `--config` picks another decoder shape.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Our arm times K back-to-back steps with CUDA events on the launching stream (inputs resident in
+HBM; the 270 MB of weights read per step exceed the 129 MB L2, and weights stream with an
+evict-first L2 policy).  `e2e` repeats the measurement through the C ABI with host buffers: each
+step passes the token id from the host and copies the logits back into pinned host memory.  The
+reference arm (`--impl reference`) is the CPU oracle timed on this machine's cores.
+With N > 1 (torchrun), every rank runs an independent replica: the decode does not shard.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+PAGES_TOKS = {"smollm-135m": 912.0, "qwen2-0.5b": 759.0, "smollm-1.7b": 419.0}  # H200 MIG 60-SM slice, context only
+METRIC = "batch-1 decode tokens/s and achieved HBM GB/s as fraction of GB300 roofline"
+
+
+def algorithmic_bytes(shape, positions) -> float:
+    """Bytes a decode step must move, averaged over `positions`: every weight once (tied E as the LM
+    head), the norm gains, the token's embedding row, K/V rows 0..p read once, one K/V row written."""
+    s = shape
+    H, I, d = s.hidden, s.intermediate, s.head_dim
+    qd, kvd = s.n_heads * d, s.n_kv_heads * d
+    per_layer = (qd * H + 2 * kvd * H + H * qd + 3 * H * I + 2 * H) * 2
+    if s.qkv_bias:
+        per_layer += (qd + 2 * kvd) * 2
+    fixed = s.n_layers * per_layer + s.vocab * H * 2 + H * 2 + H * 2
+    kv_row = s.n_layers * 2 * kvd * 2
+    kv = statistics.fmean([(p + 1) * kv_row + kv_row for p in positions])
+    return fixed + kv
+
+
+def load_peaks():
+    p = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="mbk_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, bus_id: str | None):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(bus_id.lower()[-12:])]
+            rows = mine or rows
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if os.environ.get("MBK_BENCH_BACKEND", "nccl") == "nccl" else "gloo")
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_oracle(wl, budget_s: float, max_steps: int):
+    """Oracle decode steps of `wl` for about budget_s seconds; returns (tokens/s, steps, threads)."""
+    from oracle import OracleDecoder
+    orc = OracleDecoder(wl)
+    s = wl.shape
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps:
+        orc.step(int(wl.tokens[n % s.steps]), s.pos0 + (n % s.steps))
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, n, orc.lib.orc_max_threads()
+
+
+def run_reference(args, shape_name):
+    from persistent_decode_megakernel_gb300 import workloads
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    wl = workloads.generate(shape_name, seed=0)
+    s = wl.shape
+    budget = float(os.environ.get("MBK_REF_BUDGET_S", "60"))
+    # warm-up steps (untimed), then the timed sample
+    from oracle import OracleDecoder
+    warm = OracleDecoder(wl)
+    for i in range(min(args.warmup, 3)):
+        warm.step(int(wl.tokens[i]), s.pos0 + i)
+    tps, n, cores = time_oracle(wl, budget, args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(tps, 3), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / tps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{shape_name} batch-1 teacher-forced decode", "positions": f"{s.pos0}..{s.pos0 + s.steps - 1}",
+                   "kv_capacity": s.kv_capacity},
+        "cpu_baseline": {"value": round(tps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {args.steps} decode steps (time-bounded to {budget:.0f} s)"},
+        "e2e": {"value": round(tps, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, shape_name):
+    import torch
+
+    from persistent_decode_megakernel_gb300 import build, mbk, workloads
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    build.build()
+    wl = workloads.generate(shape_name, seed=0)
+    s = wl.shape
+    dec = mbk.Decoder(wl, device=local)
+    stream = torch.cuda.current_stream()
+    steps, warm = args.steps, args.warmup
+    toks = [int(wl.tokens[i % s.steps]) for i in range(steps + warm)]
+    poss = [s.pos0 + (i % s.steps) for i in range(steps + warm)]
+    out = dec.logits
+    for i in range(warm):
+        dec.step(toks[i], poss[i], out)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler()
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        dec.step(toks[warm + i], poss[warm + i], out)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(local).pci_bus_id
+    except Exception:
+        pass
+    clocks = sampler.stop(bus)
+    assert dec.status() == 0, "device-side wait timed out during the benchmark"
+    total_ms = max_over_ranks(start.elapsed_time(end), world, torch.device("cuda", local))
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_avg_ms = statistics.fmean(kern_ms)
+
+    # end to end through the C ABI with host buffers (token from the host, logits to pinned memory)
+    host = torch.empty(s.vocab, dtype=torch.float32, pin_memory=True)
+    e2e_steps = min(steps, 2000)
+    for i in range(min(warm, 8)):
+        mbk.mbk_decode_step_host(dec.handle, toks[i], poss[i], host.data_ptr(), stream.cuda_stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        rc = mbk.mbk_decode_step_host(dec.handle, toks[warm + i], poss[warm + i], host.data_ptr(), stream.cuda_stream)
+        assert rc == 0, mbk.mbk_error_string(rc)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, torch.device("cuda", local))
+
+    positions = [poss[warm + i] for i in range(steps)]
+    algo = algorithmic_bytes(s, positions)
+    peak, peak_kind = load_peaks()
+    achieved = algo / (kernel_avg_ms * 1e-3) / 1e9
+    tps = steps * world / (total_ms * 1e-3)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        budget = float(os.environ.get("MBK_CPU_BUDGET_S", "15"))
+        ctps, cn, cores = time_oracle(wl, budget, s.steps)
+        cpu = {"value": round(ctps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{cn} teacher-forced decode steps of the same workload (time-bounded to {budget:.0f} s)"}
+    traffic = None
+    tp = os.path.join(_ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            tr = json.load(f)
+        ent = tr.get(shape_name)
+        if ent and ent.get("kernel_source_hash") == _kernel_hash():
+            traffic = ent["dram_bytes_per_launch"]
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": round(tps / PAGES_TOKS[shape_name], 3) if shape_name in PAGES_TOKS else None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{shape_name} batch-1 teacher-forced decode, random-init weights",
+                       "positions": f"{s.pos0}..{s.pos0 + s.steps - 1} cycling", "kv_capacity": s.kv_capacity,
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "inputs larger than L2 (weights stream evict-first)",
+                       "vs_baseline_note": "pages' H200 MIG 60-SM number, context only"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": round(algo), "kernel_avg_us": round(kernel_avg_ms * 1e3, 3),
+                         "kernel": "mbk::decode_kernel"},
+            "e2e": {"value": round(e2e_steps * world / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                    "d2h_bytes_per_step": s.vocab * 4},
+            "gpu_launches": steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("mbk_kernel.cu", "mbk_plan.h", "mbk_device.h", "mbk_sched.cpp"):
+        with open(os.path.join(_ROOT, "persistent_decode_megakernel_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8192)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="smollm-135m")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, args.config)
+    else:
+        run_ours(args, args.config)
+
+
+if __name__ == "__main__":
+    main()

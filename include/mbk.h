@@ -1,0 +1,181 @@
+/*
+ * mbk.h -- C ABI of the persistent batch-1 decode megakernel for GB300 (sm_103a).
+ *
+ * One call to mbk_decode_step runs a whole decode step of a Llama-shaped bf16 decoder as ONE
+ * persistent cooperative kernel (one CTA per SM): token embedding, for every layer RMSNorm,
+ * Q/K/V projection (+ bias), RoPE, KV-cache append, GQA decode attention, output projection,
+ * residual add, RMSNorm, gate/up projection, SiLU*up, down projection, residual add, then the
+ * final norm and the tied vocabulary projection, with no return to the host in between.
+ *
+ * Where the operation is defined (the MegaBake pages; they give the op list, not formulas):
+ *  - "MegaBake: a PyTorch model compiled into one CUDA kernel, and what its 5.5x is measured
+ *    against", section "What a megakernel is, and why small models want one": the per-layer op
+ *    sequence of a Llama-style decode step and the one-CTA-per-SM persistent execution model.
+ *  - megabake/megabake README, section "Current status": embedding, every layer, final norm,
+ *    vocabulary projection and KV-cache updates inside one cooperative kernel; q/k/v biases in
+ *    the projection epilogue; flash-decoding attention that splits long contexts across CTAs and
+ *    packs the query heads sharing a KV head so each cached key/value is read once.
+ *  - MegaBake project website, "Integration & evaluation": bf16, static contiguous decode KV state.
+ * The formulas are the Hugging Face Llama definitions: RMSNorm x/sqrt(mean(x^2)+eps)*g; RoPE in
+ * the rotate-half convention (element i pairs with i+d/2, angle pos*theta^(-2i/d)), applied to q
+ * and k after the bias, with K cached after rotation; softmax(q.K/sqrt(d)) V with query head h
+ * reading KV head h/(n_heads/n_kv_heads); silu(z) = z/(1+exp(-z)); tied LM head (logits = E.xn).
+ *
+ * Numerics: weights and KV cache bf16; all activations fp32 (accumulation in fp32); K and V are
+ * rounded to bf16 (round to nearest even) when appended, and attention reads the rounded values.
+ *
+ * Memory layouts (all row-major, C order):
+ *  - weight matrices: bf16 [out][in] (Hugging Face nn.Linear layout), read in place;
+ *  - embedding / LM head: bf16 [vocab][hidden];
+ *  - KV cache: bf16 [n_layers][2][n_kv_heads][kv_capacity][head_dim] (index 0 = K, 1 = V);
+ *  - logits: fp32 [vocab].
+ *
+ * Ownership: the caller owns the weights, the KV cache and every logits buffer; they must stay
+ * valid (and the weights unchanged) for the handle's lifetime.  The library copies no weights.
+ * It owns its task tables, activation exchange buffers, RoPE table and status word, all freed
+ * by mbk_destroy.
+ *
+ * Threading / streams: a handle is not thread-safe.  Steps on one handle must be issued in order
+ * on one stream (or on streams ordered by the caller); two steps of one handle must never run
+ * concurrently.  Different handles are independent.
+ *
+ * Errors: every function returning int returns MBK_OK (0) or a negative MBK_ERR_* code.  Host
+ * checks run before any launch and leave device state unchanged.  A device-side failure (a wait
+ * that ran out of time) is recorded in a device status word; it is returned by the next
+ * mbk_decode_step / mbk_kv_fill call on the handle and by mbk_get_status, and is sticky until
+ * mbk_destroy.
+ */
+#ifndef MBK_H
+#define MBK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MBK_OK 0
+#define MBK_ERR_INVALID_ARG (-1)  /* null pointer, out-of-range token/position, bad shape     */
+#define MBK_ERR_UNSUPPORTED (-2)  /* not an sm_10x GPU, or the cooperative grid does not fit */
+#define MBK_ERR_CUDA (-3)         /* a CUDA runtime call failed                              */
+#define MBK_ERR_TIMEOUT (-4)      /* a device-side wait gave up (sticky)                     */
+#define MBK_ERR_NOMEM (-5)        /* device or host allocation failed                        */
+#define MBK_ERR_STATE (-6)        /* the handle is in a sticky error state                   */
+
+typedef struct mbk_handle mbk_handle;
+
+/* Decoder shape.  head_dim must be 64 or 128; n_heads % n_kv_heads == 0; hidden, intermediate
+ * and n_heads*head_dim must be multiples of 8 (16-byte rows for bulk copies). */
+typedef struct {
+  int n_layers;
+  int hidden;        /* H */
+  int intermediate;  /* I */
+  int n_heads;       /* query heads */
+  int n_kv_heads;    /* key/value heads */
+  int head_dim;      /* d */
+  int vocab;         /* V */
+  int kv_capacity;   /* C: cache rows per (layer, K|V, kv head) */
+  double rms_eps;
+  double rope_theta;
+  int qkv_bias;      /* 1: bq, bk, bv are used (Qwen2); 0: ignored */
+} mbk_config;
+
+/* Device pointers of one layer's bf16 tensors ([out][in] for matrices, [n] for vectors).
+ * bq/bk/bv may be NULL when qkv_bias == 0. */
+typedef struct {
+  const void *attn_norm, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
+} mbk_layer_weights;
+
+typedef struct {
+  const void *embed;                /* device bf16 [V][H]; also the tied LM head */
+  const void *final_norm;           /* device bf16 [H] */
+  const mbk_layer_weights *layers;  /* HOST array of n_layers entries (copied at create) */
+} mbk_weights;
+
+/* Builds the static schedule for this shape on `device`, allocates the library's buffers and
+ * computes the RoPE table.  kv_cache: device bf16 buffer of
+ * n_layers*2*n_kv_heads*kv_capacity*head_dim elements (contents are not touched at create).
+ * Every device pointer must be 16-byte aligned.  On success *out receives the handle. */
+int mbk_create(const mbk_config *cfg, const mbk_weights *weights, void *kv_cache, int device, mbk_handle **out);
+
+/* One decode step: embeds token_id, writes K/V at `position` for every layer, attends over
+ * cache rows [0, position] and writes fp32 logits[vocab] to the DEVICE buffer logits_out.
+ * Cache rows below `position` are the caller's responsibility (earlier steps or mbk_kv_fill).
+ * stream: a cudaStream_t (NULL = legacy default stream).  Asynchronous: returns after the launch.
+ * Errors: MBK_ERR_INVALID_ARG if token_id is not in [0, vocab) or position not in
+ * [0, kv_capacity) or logits_out is NULL; a sticky device error from an earlier step. */
+int mbk_decode_step(mbk_handle *h, int32_t token_id, int32_t position, float *logits_out, void *stream);
+
+/* As mbk_decode_step, then copies the logits into the HOST buffer logits_host (vocab floats;
+ * pinned memory makes the copy asynchronous) and synchronises `stream` before returning. */
+int mbk_decode_step_host(mbk_handle *h, int32_t token_id, int32_t position, float *logits_host, void *stream);
+
+/* Loads cache rows [p0, p0+n) of `layer` from pre-RoPE keys and values (device fp32
+ * [n_kv_heads][n][head_dim] each): K is rotated by its position with the same RoPE as a decode
+ * step, then both are rounded to bf16 and stored.  Asynchronous on `stream`. */
+int mbk_kv_fill(mbk_handle *h, int layer, const float *k_raw, const float *v_raw, int32_t p0, int32_t n,
+                void *stream);
+
+/* Device status of the most recently COMPLETED step (synchronise the stream first):
+ * MBK_OK or MBK_ERR_TIMEOUT.  Reading it does not clear it. */
+int mbk_get_status(mbk_handle *h);
+
+/* Human-readable text of an error code (static storage). */
+const char *mbk_error_string(int code);
+
+/* Frees everything the library allocated for the handle.  Waits for the handle's work to finish.
+ * NULL is ignored. */
+void mbk_destroy(mbk_handle *h);
+
+/* ---- diagnostics (for tests and profiling; not needed to decode) ---- */
+
+/* Residual stream of the most recently COMPLETED step (synchronise its stream first), copied to the
+ * HOST buffer taps_out as fp32 [(2*n_layers+1)][hidden]: the embedding row, then the stream after
+ * each layer's attention and MLP sublayers.  Returns MBK_OK or MBK_ERR_INVALID_ARG / MBK_ERR_CUDA. */
+int mbk_debug_taps(mbk_handle *h, float *taps_out);
+
+/* Region-by-region checking: makes the NEXT step read, as the residual stream entering each layer
+ * l >= 1, row l of the HOST buffer x_in ([n_layers][hidden] fp32; row 0 is ignored -- layer 0 reads
+ * the embedding) instead of layer l-1's output, so every layer can be compared with a reference
+ * from identical inputs.  It applies to one step; passing NULL cancels it.  Not for decoding. */
+int mbk_debug_inject(mbk_handle *h, const float *x_in);
+
+/* Static schedule of the handle: writes up to `capacity` rows of 6 int32
+ * {cta, type (1 QKV, 2 ATTN, 3 OPROJ, 4 GATEUP, 5 DOWN, 6 LMHEAD), layer, row0, nrows, nchunks}
+ * in global task order to the HOST buffer `out` and returns the number of tasks (or a negative code). */
+int64_t mbk_debug_plan(mbk_handle *h, int32_t *out, int64_t capacity);
+
+/* Per-task timing: when enabled, every later step records for each task four globaltimer stamps
+ * (ns): {begin, inputs ready, end, first weight stage ready (0 if none)}.  Enabling allocates a
+ * device buffer of 32 bytes per task; disabling frees it.  mbk_trace_read copies the stamps of the
+ * most recently completed traced step (synchronise first) into the HOST buffer `out`
+ * (4 uint64 per task, global task order) and returns the number of tasks (or a negative code). */
+int mbk_trace_enable(mbk_handle *h, int enable);
+int64_t mbk_trace_read(mbk_handle *h, uint64_t *out, int64_t capacity_tasks);
+
+/* ---- introspection of the static schedule (host only; no GPU needed) ---- */
+
+typedef struct {
+  int num_ctas;            /* CTAs the plan was built for (one per SM) */
+  int num_tasks;           /* tasks over all CTAs */
+  int num_chunks;          /* static weight chunks over all CTAs */
+  int stage_bytes;         /* bytes of one shared-memory ring stage */
+  int num_stages;          /* stages in each CTA's ring */
+  int attn_splits;         /* context splits per KV head */
+  int64_t weight_bytes;    /* weight bytes streamed per step by the static chunks */
+  int64_t max_cta_bytes;   /* largest per-CTA share of those bytes */
+  int64_t act_words;       /* 8-byte activation exchange words per step */
+  int smem_bytes;          /* dynamic shared memory per CTA */
+} mbk_plan_info;
+
+/* Builds the schedule for `cfg` as if on a GPU with `num_sms` SMs, checks it (every weight row
+ * covered exactly once, every task's inputs produced by an earlier task in every CTA's order,
+ * every bulk copy 16-byte aligned and within its tensor) and fills *info.  Returns MBK_OK,
+ * MBK_ERR_INVALID_ARG for a shape the kernel does not support, or MBK_ERR_STATE when a check
+ * fails.  Weight addresses are taken from a fake base so no device memory is needed. */
+int mbk_plan_check(const mbk_config *cfg, int num_sms, mbk_plan_info *info);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MBK_H */

@@ -1,0 +1,461 @@
+// mbk_api.cu -- the C ABI (include/mbk.h): handle creation, argument checks, the per-step launch.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/mbk.h"
+#include "mbk_device.h"
+#include "mbk_sched.h"
+
+namespace mbk {
+const void* decode_kernel_ptr();
+cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
+cudaError_t launch_kv_fill(uint16_t* kv_layer, const float* k_raw, const float* v_raw, const float2* rope, int nkv, int C,
+                           int d, int p0, int n, cudaStream_t st);
+}  // namespace mbk
+
+using namespace mbk;
+
+struct mbk_handle {
+  int device = 0;
+  mbk_config cfg{};
+  Plan plan;
+  KernelParams kp{};
+  unsigned tag = 0;           // last step's tag
+  int grid = 0;
+  // device allocations
+  Task* d_tasks = nullptr;
+  uint32_t* d_task_off = nullptr;
+  Chunk* d_chunks = nullptr;
+  uint32_t* d_chunk_off = nullptr;
+  LayerW* d_layers = nullptr;
+  float2* d_rope = nullptr;
+  unsigned long long* d_words = nullptr;
+  unsigned* d_status = nullptr;
+  unsigned* h_status = nullptr;  // mapped pinned host memory
+  float* d_logits_tmp = nullptr; // for mbk_decode_step_host
+  unsigned long long* d_trace = nullptr;
+  unsigned long long* d_inject = nullptr;
+  bool inject_armed = false;
+  int last_token = 0;
+  int sticky = MBK_OK;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+PlanShape shape_of(const mbk_config& c) {
+  PlanShape s;
+  s.L = c.n_layers;
+  s.H = c.hidden;
+  s.I = c.intermediate;
+  s.nq = c.n_heads;
+  s.nkv = c.n_kv_heads;
+  s.d = c.head_dim;
+  s.V = c.vocab;
+  s.C = c.kv_capacity;
+  s.qkv_bias = c.qkv_bias ? 1 : 0;
+  return s;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  return atoi(v);
+}
+
+int config_check(const mbk_config* cfg) {
+  if (!cfg) return MBK_ERR_INVALID_ARG;
+  if (!(cfg->rms_eps >= 0.0) || !(cfg->rope_theta > 0.0) || !std::isfinite(cfg->rope_theta)) return MBK_ERR_INVALID_ARG;
+  if (!validate_shape(shape_of(*cfg)).empty()) return MBK_ERR_INVALID_ARG;
+  return MBK_OK;
+}
+
+void free_all(mbk_handle* h) {
+  cudaFree(h->d_tasks);
+  cudaFree(h->d_task_off);
+  cudaFree(h->d_chunks);
+  cudaFree(h->d_chunk_off);
+  cudaFree(h->d_layers);
+  cudaFree(h->d_rope);
+  cudaFree(h->d_words);
+  cudaFree(h->d_status);
+  cudaFree(h->d_logits_tmp);
+  cudaFree(h->d_trace);
+  cudaFree(h->d_inject);
+  if (h->h_status) cudaFreeHost(h->h_status);
+}
+
+int sticky_status(mbk_handle* h) {
+  if (h->sticky != MBK_OK) return h->sticky;
+  if (h->h_status && *(volatile unsigned*)h->h_status != 0u) h->sticky = MBK_ERR_TIMEOUT;
+  return h->sticky;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mbk_error_string(int code) {
+  switch (code) {
+    case MBK_OK: return "ok";
+    case MBK_ERR_INVALID_ARG: return "invalid argument";
+    case MBK_ERR_UNSUPPORTED: return "unsupported device or configuration";
+    case MBK_ERR_CUDA: return "CUDA runtime error";
+    case MBK_ERR_TIMEOUT: return "a device-side wait timed out";
+    case MBK_ERR_NOMEM: return "out of memory";
+    case MBK_ERR_STATE: return "handle is in an error state";
+    default: return "unknown error";
+  }
+}
+
+int mbk_plan_check(const mbk_config* cfg, int num_sms, mbk_plan_info* info) {
+  if (!cfg || !info || num_sms <= 0) return MBK_ERR_INVALID_ARG;
+  if (config_check(cfg) != MBK_OK) return MBK_ERR_INVALID_ARG;
+  PlanShape s = shape_of(*cfg);
+  WeightAddrs w = fake_weight_addrs(s);
+  Plan p;
+  PlanOptions opt;
+  opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
+  std::string err = build_plan(s, w, num_sms, opt, &p);
+  if (!err.empty()) return MBK_ERR_STATE;
+  info->num_ctas = p.num_ctas;
+  info->num_tasks = (int)p.tasks.size();
+  info->num_chunks = (int)p.chunks.size();
+  info->stage_bytes = kStageBytes;
+  info->num_stages = p.num_stages;
+  info->attn_splits = p.nsplit;
+  info->weight_bytes = p.weight_bytes;
+  info->max_cta_bytes = p.max_cta_bytes;
+  info->act_words = (int64_t)p.act_words;
+  info->smem_bytes = p.smem_bytes;
+  return MBK_OK;
+}
+
+int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache, int device, mbk_handle** out) {
+  if (!out) return MBK_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (config_check(cfg) != MBK_OK || !weights || !weights->embed || !weights->final_norm || !weights->layers || !kv_cache)
+    return MBK_ERR_INVALID_ARG;
+  const PlanShape s = shape_of(*cfg);
+  // every tensor pointer present and 16-byte aligned
+  if (!aligned16(weights->embed) || !aligned16(weights->final_norm) || !aligned16(kv_cache)) return MBK_ERR_INVALID_ARG;
+  WeightAddrs wa;
+  wa.embed = (uint64_t)(uintptr_t)weights->embed;
+  wa.final_norm = (uint64_t)(uintptr_t)weights->final_norm;
+  wa.layers.resize(s.L);
+  for (int l = 0; l < s.L; ++l) {
+    const mbk_layer_weights& lw = weights->layers[l];
+    const void* ptrs[W_NSLOTS] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.bq, lw.bk, lw.bv, lw.wo, lw.mlp_norm, lw.w_gate, lw.w_up, lw.w_down};
+    for (int k = 0; k < W_NSLOTS; ++k) {
+      bool is_bias = (k == W_BQ || k == W_BK || k == W_BV);
+      if (is_bias && !s.qkv_bias) {
+        wa.layers[l][k] = 0;
+        continue;
+      }
+      if (!ptrs[k]) return MBK_ERR_INVALID_ARG;
+      if (!is_bias && k != W_ATTN_NORM && k != W_MLP_NORM && !aligned16(ptrs[k])) return MBK_ERR_INVALID_ARG;
+      wa.layers[l][k] = (uint64_t)(uintptr_t)ptrs[k];
+    }
+  }
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MBK_ERR_UNSUPPORTED;
+  if (cudaSetDevice(device) != cudaSuccess) return MBK_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MBK_ERR_CUDA;
+  if (prop.major != 10) return MBK_ERR_UNSUPPORTED;  // built for sm_103a (Blackwell data-center)
+  int coop = 0, smem_optin = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (!coop) return MBK_ERR_UNSUPPORTED;
+
+  mbk_handle* h = new (std::nothrow) mbk_handle();
+  if (!h) return MBK_ERR_NOMEM;
+  h->device = device;
+  h->cfg = *cfg;
+  PlanOptions opt;
+  opt.smem_limit = smem_optin;
+  opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
+  std::string err = build_plan(s, wa, prop.multiProcessorCount, opt, &h->plan);
+  if (!err.empty()) {
+    delete h;
+    return MBK_ERR_UNSUPPORTED;
+  }
+  // Fault injection for tests (host side only): drop one task, so whoever reads its outputs waits
+  // until its bounded timeout and the step reports MBK_ERR_TIMEOUT.
+  const int drop = env_int("MBK_DEBUG_DROP_TASK", -1);
+  if (drop >= 0 && drop < (int)h->plan.tasks.size()) {
+    Plan& pl = h->plan;
+    const Task victim = pl.tasks[drop];
+    pl.tasks.erase(pl.tasks.begin() + drop);
+    for (uint32_t& o : pl.task_off)
+      if (o > (uint32_t)drop) --o;
+    pl.chunks.erase(pl.chunks.begin() + victim.chunk0, pl.chunks.begin() + victim.chunk0 + victim.nchunks);
+    for (uint32_t& o : pl.chunk_off)
+      if (o > victim.chunk0) o -= victim.nchunks;
+    for (Task& t : pl.tasks)
+      if (t.chunk0 > victim.chunk0) t.chunk0 -= victim.nchunks;
+  }
+  const Plan& p = h->plan;
+  h->grid = p.num_ctas;
+
+  const void* kfn = decode_kernel_ptr();
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess) {
+    delete h;
+    return MBK_ERR_CUDA;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, p.smem_bytes) != cudaSuccess || per_sm < 1) {
+    delete h;
+    return MBK_ERR_UNSUPPORTED;
+  }
+
+  int rc = MBK_OK;
+  auto ck = [&](cudaError_t e) {
+    if (e != cudaSuccess && rc == MBK_OK) rc = (e == cudaErrorMemoryAllocation) ? MBK_ERR_NOMEM : MBK_ERR_CUDA;
+    return e == cudaSuccess;
+  };
+  std::vector<LayerW> lw(s.L);
+  for (int l = 0; l < s.L; ++l)
+    for (int k = 0; k < W_NSLOTS; ++k) lw[l].w[k] = reinterpret_cast<const uint16_t*>(wa.layers[l][k]);
+  const size_t rope_n = (size_t)s.C * (s.d / 2);
+  if (ck(cudaMalloc(&h->d_tasks, sizeof(Task) * p.tasks.size())) &&
+      ck(cudaMalloc(&h->d_task_off, sizeof(uint32_t) * p.task_off.size())) &&
+      ck(cudaMalloc(&h->d_chunks, sizeof(Chunk) * std::max<size_t>(1, p.chunks.size()))) &&
+      ck(cudaMalloc(&h->d_chunk_off, sizeof(uint32_t) * p.chunk_off.size())) &&
+      ck(cudaMalloc(&h->d_layers, sizeof(LayerW) * s.L)) && ck(cudaMalloc(&h->d_rope, sizeof(float2) * rope_n)) &&
+      ck(cudaMalloc(&h->d_words, sizeof(unsigned long long) * p.act_words)) &&
+      ck(cudaMalloc(&h->d_status, 16)) && ck(cudaMalloc(&h->d_logits_tmp, sizeof(float) * s.V)) &&
+      ck(cudaHostAlloc(&h->h_status, 16, cudaHostAllocMapped))) {
+    ck(cudaMemcpy(h->d_tasks, p.tasks.data(), sizeof(Task) * p.tasks.size(), cudaMemcpyHostToDevice));
+    ck(cudaMemcpy(h->d_task_off, p.task_off.data(), sizeof(uint32_t) * p.task_off.size(), cudaMemcpyHostToDevice));
+    if (!p.chunks.empty()) ck(cudaMemcpy(h->d_chunks, p.chunks.data(), sizeof(Chunk) * p.chunks.size(), cudaMemcpyHostToDevice));
+    ck(cudaMemcpy(h->d_chunk_off, p.chunk_off.data(), sizeof(uint32_t) * p.chunk_off.size(), cudaMemcpyHostToDevice));
+    ck(cudaMemcpy(h->d_layers, lw.data(), sizeof(LayerW) * s.L, cudaMemcpyHostToDevice));
+    ck(cudaMemset(h->d_words, 0, sizeof(unsigned long long) * p.act_words));
+    ck(cudaMemset(h->d_status, 0, 16));
+    memset(h->h_status, 0, 16);
+    ck(launch_rope_table(h->d_rope, s.C, s.d, cfg->rope_theta, 0));
+    ck(cudaDeviceSynchronize());
+  }
+  unsigned* h_status_dev = nullptr;
+  if (rc == MBK_OK) ck(cudaHostGetDevicePointer((void**)&h_status_dev, h->h_status, 0));
+  if (rc != MBK_OK) {
+    free_all(h);
+    delete h;
+    return rc;
+  }
+
+  KernelParams& kp = h->kp;
+  kp.L = s.L;
+  kp.H = s.H;
+  kp.I = s.I;
+  kp.nq = s.nq;
+  kp.nkv = s.nkv;
+  kp.d = s.d;
+  kp.V = s.V;
+  kp.C = s.C;
+  kp.g = s.nq / s.nkv;
+  kp.eps = (float)cfg->rms_eps;
+  kp.attn_scale = (float)(1.0 / std::sqrt((double)s.d));
+  kp.qkv_bias = s.qkv_bias;
+  kp.tasks = h->d_tasks;
+  kp.task_off = h->d_task_off;
+  kp.chunks = h->d_chunks;
+  kp.chunk_off = h->d_chunk_off;
+  kp.act = p.act;
+  kp.nsplit = p.nsplit;
+  kp.split_len = p.split_len;
+  kp.rows_per_stage = p.attn_rows_per_stage;
+  kp.num_stages = p.num_stages;
+  kp.off_sv = p.off_sv;
+  kp.off_res = p.off_res;
+  kp.off_resid = p.off_resid;
+  kp.off_ring = p.off_ring;
+  kp.embed = reinterpret_cast<const uint16_t*>(weights->embed);
+  kp.final_norm = reinterpret_cast<const uint16_t*>(weights->final_norm);
+  kp.layers = h->d_layers;
+  kp.kv = reinterpret_cast<uint16_t*>(kv_cache);
+  kp.rope = h->d_rope;
+  kp.words = h->d_words;
+  kp.status = h->d_status;
+  kp.host_status = h_status_dev;
+  kp.timeout_ns = (unsigned long long)env_int("MBK_WAIT_TIMEOUT_MS", 1000) * 1000000ull;
+  *out = h;
+  return MBK_OK;
+}
+
+int mbk_decode_step(mbk_handle* h, int32_t token_id, int32_t position, float* logits_out, void* stream) {
+  if (!h || !logits_out) return MBK_ERR_INVALID_ARG;
+  if (token_id < 0 || token_id >= h->cfg.vocab || position < 0 || position >= h->cfg.kv_capacity) return MBK_ERR_INVALID_ARG;
+  if (int st = sticky_status(h)) return st;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  StepParams sp;
+  sp.token = token_id;
+  sp.pos = position;
+  if (++h->tag == 0) ++h->tag;  // tag 0 marks never-written words
+  sp.tag = h->tag;
+  sp.logits = logits_out;
+  h->last_token = token_id;
+  KernelParams kp = h->kp;
+  if (h->inject_armed) {
+    kp.inject = h->d_inject;  // one step only
+    h->inject_armed = false;
+  }
+  void* args[] = {&kp, &sp};
+  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(), dim3(h->grid), dim3(kThreads), args,
+                                              (size_t)h->plan.smem_bytes, (cudaStream_t)stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;
+}
+
+int mbk_decode_step_host(mbk_handle* h, int32_t token_id, int32_t position, float* logits_host, void* stream) {
+  if (!h || !logits_host) return MBK_ERR_INVALID_ARG;
+  int rc = mbk_decode_step(h, token_id, position, h->d_logits_tmp, stream);
+  if (rc != MBK_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(logits_host, h->d_logits_tmp, sizeof(float) * h->cfg.vocab, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MBK_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MBK_ERR_CUDA;
+  return sticky_status(h);
+}
+
+int mbk_kv_fill(mbk_handle* h, int layer, const float* k_raw, const float* v_raw, int32_t p0, int32_t n, void* stream) {
+  if (!h || !k_raw || !v_raw) return MBK_ERR_INVALID_ARG;
+  const mbk_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers || p0 < 0 || n < 0 || (int64_t)p0 + n > c.kv_capacity) return MBK_ERR_INVALID_ARG;
+  if (int st = sticky_status(h)) return st;
+  if (n == 0) return MBK_OK;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  uint16_t* kv_layer = h->kp.kv + (size_t)layer * 2 * c.n_kv_heads * c.kv_capacity * c.head_dim;
+  cudaError_t e = launch_kv_fill(kv_layer, k_raw, v_raw, h->d_rope, c.n_kv_heads, c.kv_capacity, c.head_dim, p0, n,
+                                 (cudaStream_t)stream);
+  return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;
+}
+
+int mbk_get_status(mbk_handle* h) {
+  if (!h) return MBK_ERR_INVALID_ARG;
+  if (h->sticky != MBK_OK) return h->sticky;
+  unsigned st[4] = {0, 0, 0, 0};
+  if (cudaSetDevice(h->device) != cudaSuccess || cudaMemcpy(st, h->d_status, 16, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MBK_ERR_CUDA;
+  if (st[0] != 0u) h->sticky = MBK_ERR_TIMEOUT;
+  return h->sticky;
+}
+
+int mbk_debug_taps(mbk_handle* h, float* taps_out) {
+  if (!h || !taps_out) return MBK_ERR_INVALID_ARG;
+  const mbk_config& c = h->cfg;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  std::vector<unsigned long long> words(h->plan.act_words);
+  std::vector<uint16_t> emb(c.hidden);
+  if (cudaMemcpy(words.data(), h->d_words, words.size() * 8, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(emb.data(), h->kp.embed + (size_t)h->last_token * c.hidden, c.hidden * 2, cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return MBK_ERR_CUDA;
+  auto val = [](unsigned long long w) {
+    uint32_t u = (uint32_t)w;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+  };
+  for (int i = 0; i < c.hidden; ++i) {
+    uint32_t u = (uint32_t)emb[i] << 16;
+    memcpy(&taps_out[i], &u, 4);
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    const unsigned long long* lw = words.data() + (size_t)l * h->plan.act.per_layer;
+    for (int i = 0; i < c.hidden; ++i) {
+      taps_out[(size_t)(2 * l + 1) * c.hidden + i] = val(lw[h->plan.act.xa + i]);
+      taps_out[(size_t)(2 * l + 2) * c.hidden + i] = val(lw[h->plan.act.xm + i]);
+    }
+  }
+  return MBK_OK;
+}
+
+int mbk_debug_inject(mbk_handle* h, const float* x_in) {
+  if (!h) return MBK_ERR_INVALID_ARG;
+  if (!x_in) {
+    h->inject_armed = false;
+    return MBK_OK;
+  }
+  const mbk_config& c = h->cfg;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  const size_t n = (size_t)c.n_layers * c.hidden;
+  if (!h->d_inject && cudaMalloc(&h->d_inject, n * sizeof(unsigned long long)) != cudaSuccess) return MBK_ERR_NOMEM;
+  unsigned next_tag = h->tag + 1;
+  if (next_tag == 0) next_tag = 1;
+  std::vector<unsigned long long> w(n);
+  for (size_t i = 0; i < n; ++i) {
+    uint32_t u;
+    memcpy(&u, &x_in[i], 4);
+    w[i] = ((unsigned long long)next_tag << 32) | u;
+  }
+  if (cudaMemcpy(h->d_inject, w.data(), n * sizeof(unsigned long long), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MBK_ERR_CUDA;
+  h->inject_armed = true;
+  return MBK_OK;
+}
+
+int64_t mbk_debug_plan(mbk_handle* h, int32_t* out, int64_t capacity) {
+  if (!h || (!out && capacity > 0)) return MBK_ERR_INVALID_ARG;
+  const Plan& p = h->plan;
+  for (int c = 0; c < p.num_ctas; ++c)
+    for (uint32_t i = p.task_off[c]; i < p.task_off[c + 1]; ++i) {
+      if ((int64_t)i >= capacity) continue;
+      const Task& t = p.tasks[i];
+      int32_t* r = out + (size_t)i * 6;
+      r[0] = c;
+      r[1] = t.type;
+      r[2] = t.layer;
+      r[3] = (int32_t)t.row0;
+      r[4] = (int32_t)t.nrows;
+      r[5] = (int32_t)t.nchunks;
+    }
+  return (int64_t)p.tasks.size();
+}
+
+int mbk_trace_enable(mbk_handle* h, int enable) {
+  if (!h) return MBK_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  if (enable && !h->d_trace) {
+    size_t bytes = sizeof(unsigned long long) * 4 * std::max<size_t>(1, h->plan.tasks.size());
+    if (cudaMalloc(&h->d_trace, bytes) != cudaSuccess) return MBK_ERR_NOMEM;
+    if (cudaMemset(h->d_trace, 0, bytes) != cudaSuccess) return MBK_ERR_CUDA;
+  } else if (!enable && h->d_trace) {
+    cudaDeviceSynchronize();
+    cudaFree(h->d_trace);
+  cudaFree(h->d_inject);
+    h->d_trace = nullptr;
+  }
+  h->kp.trace = h->d_trace;
+  return MBK_OK;
+}
+
+int64_t mbk_trace_read(mbk_handle* h, uint64_t* out, int64_t capacity_tasks) {
+  if (!h || !out || !h->d_trace) return MBK_ERR_INVALID_ARG;
+  int64_t n = std::min<int64_t>(capacity_tasks, (int64_t)h->plan.tasks.size());
+  if (cudaSetDevice(h->device) != cudaSuccess ||
+      cudaMemcpy(out, h->d_trace, sizeof(uint64_t) * 4 * n, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MBK_ERR_CUDA;
+  return (int64_t)h->plan.tasks.size();
+}
+
+void mbk_destroy(mbk_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+}
+
+}  // extern "C"

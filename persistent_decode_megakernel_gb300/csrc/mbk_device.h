@@ -1,0 +1,53 @@
+// mbk_device.h -- parameters of the persistent decode kernel (shared by mbk_kernel.cu and mbk_api.cu).
+#pragma once
+#include <stdint.h>
+
+#include "mbk_plan.h"
+
+namespace mbk {
+
+// Device status word values (host maps them to the negative MBK_ERR_* codes).
+enum DeviceStatus : unsigned { DS_OK = 0, DS_TIMEOUT = 4 };
+
+// Per-layer weight pointers, in the order of WeightSlot (mbk_sched.h); bf16 bit patterns.
+enum LayerSlot { LW_ATTN_NORM, LW_Q, LW_K, LW_V, LW_BQ, LW_BK, LW_BV, LW_O, LW_MLP_NORM, LW_GATE, LW_UP, LW_DOWN };
+struct LayerW {
+  const uint16_t* w[12];
+};
+
+// Constant for the lifetime of a handle.
+struct KernelParams {
+  int L, H, I, nq, nkv, d, V, C, g;
+  float eps, attn_scale;
+  int qkv_bias;
+  // schedule
+  const Task* tasks;
+  const uint32_t* task_off;     // [grid + 1]
+  const Chunk* chunks;
+  const uint32_t* chunk_off;    // [grid + 1]
+  ActLayout act;
+  int nsplit, split_len, rows_per_stage, num_stages;
+  uint32_t off_sv, off_res, off_resid, off_ring;
+  // tensors
+  const uint16_t* embed;
+  const uint16_t* final_norm;
+  const LayerW* layers;
+  uint16_t* kv;                 // [L][2][nkv][C][d]
+  const float2* rope;           // [C][d/2] (cos, sin)
+  unsigned long long* words;    // activation exchange words [L * act.per_layer]
+  unsigned* status;             // device status [4]: code, cta, task, detail
+  unsigned* host_status;        // the same, in mapped pinned host memory (may be null)
+  unsigned long long timeout_ns;
+  unsigned long long* trace;    // null, or 4 globaltimer stamps per task (begin, ready, end, first stage)
+  const unsigned long long* inject;  // null, or words [L][H]: row l replaces the input of layer l >= 1
+};
+
+// Changes every step.
+struct StepParams {
+  int token;
+  int pos;
+  unsigned tag;   // step sequence number (never 0): the tag carried by every word written this step
+  float* logits;  // device fp32 [V]
+};
+
+}  // namespace mbk

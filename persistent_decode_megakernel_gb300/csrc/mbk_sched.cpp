@@ -1,0 +1,363 @@
+// mbk_sched.cpp -- host-side static scheduler for the persistent decode kernel.
+//
+// The pages' planner (MegaBake article, "How a model gets in", steps 4-5) groups regions into
+// phases separated by grid barriers and folds small producers into their consumers.  Here the
+// plan is finer grained: every projection is split by output rows into tasks spread over all
+// CTAs (so every SM streams weights every layer), norms/RoPE/SiLU/residual adds are fused into the
+// tasks that need them, and each task depends only on the activation words it reads.  Tasks are
+// appended to CTA lists in one global topological order (layer by layer, op by op), which is what
+// makes the spin-waits deadlock-free when all CTAs are co-resident.
+#include "mbk_sched.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <map>
+
+namespace mbk {
+
+namespace {
+
+struct Seg {          // a run of rows of one weight matrix
+  uint64_t base;      // matrix base address
+  int row_bytes;
+  int first_row;
+  int nrows;
+};
+
+void add_chunks(std::vector<Chunk>& out, const Seg& sg) {
+  int per = kStageBytes / sg.row_bytes;
+  for (int r = 0; r < sg.nrows; r += per) {
+    int n = std::min(per, sg.nrows - r);
+    Chunk c;
+    c.src = sg.base + (uint64_t)(sg.first_row + r) * (uint64_t)sg.row_bytes;
+    c.bytes = (uint32_t)(n * sg.row_bytes);
+    c.rows = (uint32_t)n;
+    out.push_back(c);
+  }
+}
+
+// Warps per weight row for a GEMV task: as many as leave every compute warp busy on the task's
+// largest chunk, while rows x warps-per-row fits the partial-result slots.
+uint32_t warps_per_row(const std::vector<Chunk>& chunks, const Task& t, int res_per_row) {
+  uint32_t max_rows = 1;
+  for (uint32_t k = t.chunk0; k < t.chunk0 + t.nchunks; ++k) max_rows = std::max(max_rows, chunks[k].rows);
+  uint32_t wpr = 1;
+  while (wpr * 2 * max_rows <= (uint32_t)kComputeWarps) wpr *= 2;
+  while (wpr > 1 && (uint64_t)t.nrows * res_per_row * wpr > (uint64_t)kResSlots) wpr /= 2;
+  return wpr;
+}
+
+}  // namespace
+
+std::string validate_shape(const PlanShape& s) {
+  char buf[256];
+  if (s.L <= 0 || s.H <= 0 || s.I <= 0 || s.nq <= 0 || s.nkv <= 0 || s.V <= 0 || s.C <= 0) return "non-positive dimension";
+  if (s.d != 64 && s.d != 128) return "head_dim must be 64 or 128";
+  if (s.nq % s.nkv != 0) return "n_heads must be a multiple of n_kv_heads";
+  if (s.nq / s.nkv > 16) return "at most 16 query heads per KV head";
+  if (s.H % 8 || s.I % 8) return "hidden and intermediate must be multiples of 8";
+  int max_in = std::max(std::max(s.H, s.I), s.nq * s.d);
+  if (max_in * 2 > kStageBytes) {
+    snprintf(buf, sizeof buf, "a weight row of %d bf16 exceeds one %d-byte stage", max_in, kStageBytes);
+    return buf;
+  }
+  if (s.H > kMaxTaskRows) return "hidden larger than the per-task result capacity";
+  if (s.L > 65535) return "too many layers";
+  return "";
+}
+
+WeightAddrs fake_weight_addrs(const PlanShape& s) {
+  WeightAddrs w;
+  uint64_t base = 1ull << 40;
+  auto next = [&](uint64_t bytes) { uint64_t a = base; base += (bytes + 4095) / 4096 * 4096 + 4096; return a; };
+  w.embed = next((uint64_t)s.V * s.H * 2);
+  w.final_norm = next((uint64_t)s.H * 2);
+  w.layers.resize(s.L);
+  uint64_t qd = (uint64_t)s.nq * s.d, kvd = (uint64_t)s.nkv * s.d;
+  for (int l = 0; l < s.L; ++l) {
+    auto& a = w.layers[l];
+    a[W_ATTN_NORM] = next(s.H * 2);
+    a[W_Q] = next(qd * s.H * 2);
+    a[W_K] = next(kvd * s.H * 2);
+    a[W_V] = next(kvd * s.H * 2);
+    a[W_BQ] = s.qkv_bias ? next(qd * 2) : 0;
+    a[W_BK] = s.qkv_bias ? next(kvd * 2) : 0;
+    a[W_BV] = s.qkv_bias ? next(kvd * 2) : 0;
+    a[W_O] = next((uint64_t)s.H * qd * 2);
+    a[W_MLP_NORM] = next(s.H * 2);
+    a[W_GATE] = next((uint64_t)s.I * s.H * 2);
+    a[W_UP] = next((uint64_t)s.I * s.H * 2);
+    a[W_DOWN] = next((uint64_t)s.H * s.I * 2);
+  }
+  return w;
+}
+
+std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, const PlanOptions& opt, Plan* out) {
+  std::string err = validate_shape(s);
+  if (!err.empty()) return err;
+  if (num_ctas <= 0) return "no CTAs";
+  if ((int)w.layers.size() != s.L) return "weight table does not match n_layers";
+  Plan& p = *out;
+  p = Plan();
+  p.num_ctas = num_ctas;
+  const int g = s.nq / s.nkv;
+  const int qd = s.nq * s.d, kvd = s.nkv * s.d;
+
+  // attention context splits: one split for short caches; otherwise splits of at most
+  // kAttnSplitMax positions and at most kAttnSplitStages ring stages (a split holds all its stages)
+  p.attn_rows_per_stage = kStageBytes / (2 * s.d * 2);
+  const int split_cap = std::min(kAttnSplitMax, kAttnSplitStages * p.attn_rows_per_stage);
+  p.split_len = s.C <= split_cap ? s.C : split_cap;
+  p.nsplit = (s.C + p.split_len - 1) / p.split_len;
+
+  // activation words
+  ActLayout a{};
+  a.qkv = 0;
+  a.att = a.qkv + (uint32_t)(qd + 2 * kvd);
+  a.xa = a.att + (uint32_t)(s.nkv * p.nsplit * g * (s.d + 2));
+  a.hh = a.xa + (uint32_t)s.H;
+  a.xm = a.hh + (uint32_t)s.I;
+  a.per_layer = a.xm + (uint32_t)s.H;
+  p.act = a;
+  p.act_words = (uint64_t)a.per_layer * s.L;
+
+  // shared memory layout: [barriers + flags 1 KB][input vector][results][residuals][ring]
+  const int O = g * s.d;
+  int attn_floats = O + g * (p.split_len + 1) + std::max(kComputeWarps * 32, O) + 2 * s.d + 2 * g + 8;
+  p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
+  p.sv_floats = (p.sv_floats + 31) / 32 * 32;
+  p.off_sv = 1024;
+  p.off_res = p.off_sv + (uint32_t)p.sv_floats * 4;
+  p.off_resid = p.off_res + kResSlots * 4;
+  p.off_ring = (p.off_resid + kMaxTaskRows * 4 + 127) / 128 * 128;
+  int avail = opt.smem_limit - (int)p.off_ring;
+  p.num_stages = std::min(kMaxRingStages, avail / kStageBytes);
+  if (p.num_stages < 2) return "not enough shared memory for the weight ring";
+  if (p.num_stages < (p.split_len + p.attn_rows_per_stage - 1) / p.attn_rows_per_stage + 1)
+    return "weight ring too small to hold one attention split";
+  p.smem_bytes = (int)p.off_ring + p.num_stages * kStageBytes;
+
+  // tasks
+  std::vector<std::vector<Task>> cta_tasks(num_ctas);
+  std::vector<std::vector<Chunk>> cta_chunks(num_ctas);
+  std::vector<int64_t> cta_bytes(num_ctas, 0);
+  int cursor = 0;
+  const int max_tasks = opt.max_tasks_per_op > 0 ? std::min(opt.max_tasks_per_op, num_ctas) : num_ctas;
+
+  // row-split GEMV op: `segs_for(r0, r1)` lists the weight segments of output rows [r0, r1)
+  auto gemv_op = [&](TaskType type, int layer, int rows, int res_per_row, int row_bytes, auto segs_for) {
+    int n = std::min(max_tasks, rows);
+    // results per task must fit the result slots, and its chunks the per-task chunk bound
+    const int rpc = kStageBytes / row_bytes;
+    auto chunks_for = [&](int task_rows) { return res_per_row * ((task_rows + rpc - 1) / rpc) + 2; };
+    while ((rows + n - 1) / n * res_per_row > kMaxTaskRows || chunks_for((rows + n - 1) / n) > kMaxTaskChunks) ++n;
+    for (int i = 0; i < n; ++i) {
+      int r0 = (int)((int64_t)rows * i / n), r1 = (int)((int64_t)rows * (i + 1) / n);
+      if (r1 <= r0) continue;
+      int cta = cursor % num_ctas;
+      ++cursor;
+      Task t{};
+      t.type = type;
+      t.layer = (uint16_t)layer;
+      t.row0 = (uint32_t)r0;
+      t.nrows = (uint32_t)(r1 - r0);
+      t.chunk0 = (uint32_t)cta_chunks[cta].size();
+      for (const Seg& sg : segs_for(r0, r1)) add_chunks(cta_chunks[cta], sg);
+      t.nchunks = (uint32_t)(cta_chunks[cta].size() - t.chunk0);
+      for (uint32_t c = t.chunk0; c < t.chunk0 + t.nchunks; ++c) cta_bytes[cta] += cta_chunks[cta][c].bytes;
+      t.wpr = warps_per_row(cta_chunks[cta], t, res_per_row);
+      cta_tasks[cta].push_back(t);
+    }
+  };
+
+  const int hb = s.H * 2;
+  for (int l = 0; l < s.L; ++l) {
+    const auto& W = w.layers[l];
+    gemv_op(T_QKV, l, qd + 2 * kvd, 1, hb, [&](int r0, int r1) {
+      std::vector<Seg> v;
+      int bounds[4] = {0, qd, qd + kvd, qd + 2 * kvd};
+      uint64_t bases[3] = {W[W_Q], W[W_K], W[W_V]};
+      for (int m = 0; m < 3; ++m) {
+        int a0 = std::max(r0, bounds[m]), a1 = std::min(r1, bounds[m + 1]);
+        if (a1 > a0) v.push_back(Seg{bases[m], hb, a0 - bounds[m], a1 - a0});
+      }
+      return v;
+    });
+    for (int kvh = 0; kvh < s.nkv; ++kvh) {
+      for (int sp = 0; sp < p.nsplit; ++sp) {
+        int cta = cursor % num_ctas;
+        ++cursor;
+        Task t{};
+        t.type = T_ATTN;
+        t.layer = (uint16_t)l;
+        t.row0 = (uint32_t)kvh;
+        t.nrows = (uint32_t)sp;
+        t.chunk0 = (uint32_t)cta_chunks[cta].size();
+        t.nchunks = 1;
+        Chunk ph;
+        ph.src = ((uint64_t)l << 48) | ((uint64_t)kvh << 32) | (uint64_t)sp;
+        ph.bytes = 0;
+        ph.rows = kAttnChunk;
+        cta_chunks[cta].push_back(ph);
+        cta_tasks[cta].push_back(t);
+      }
+    }
+    gemv_op(T_OPROJ, l, s.H, 1, qd * 2, [&](int r0, int r1) {
+      return std::vector<Seg>{Seg{W[W_O], qd * 2, r0, r1 - r0}};
+    });
+    gemv_op(T_GATEUP, l, s.I, 2, hb, [&](int r0, int r1) {
+      return std::vector<Seg>{Seg{W[W_GATE], hb, r0, r1 - r0}, Seg{W[W_UP], hb, r0, r1 - r0}};
+    });
+    gemv_op(T_DOWN, l, s.H, 1, s.I * 2, [&](int r0, int r1) {
+      return std::vector<Seg>{Seg{W[W_DOWN], s.I * 2, r0, r1 - r0}};
+    });
+  }
+  {
+    // the LM head is split over every CTA regardless of max_tasks (it is bandwidth bound)
+    int n = num_ctas;
+    const int rows_per_chunk = kStageBytes / hb;
+    while ((s.V + n - 1) / n > kMaxTaskRows || ((s.V + n - 1) / n + rows_per_chunk - 1) / rows_per_chunk > kMaxTaskChunks)
+      n += num_ctas;
+    for (int i = 0; i < n; ++i) {
+      int r0 = (int)((int64_t)s.V * i / n), r1 = (int)((int64_t)s.V * (i + 1) / n);
+      if (r1 <= r0) continue;
+      int cta = cursor % num_ctas;
+      ++cursor;
+      Task t{};
+      t.type = T_LMHEAD;
+      t.layer = (uint16_t)(s.L - 1);
+      t.row0 = (uint32_t)r0;
+      t.nrows = (uint32_t)(r1 - r0);
+      t.chunk0 = (uint32_t)cta_chunks[cta].size();
+      add_chunks(cta_chunks[cta], Seg{w.embed, hb, r0, r1 - r0});
+      t.nchunks = (uint32_t)(cta_chunks[cta].size() - t.chunk0);
+      for (uint32_t c = t.chunk0; c < t.chunk0 + t.nchunks; ++c) cta_bytes[cta] += cta_chunks[cta][c].bytes;
+      t.wpr = warps_per_row(cta_chunks[cta], t, 1);
+      cta_tasks[cta].push_back(t);
+    }
+  }
+
+  // flatten (chunk indices become global)
+  p.task_off.assign(num_ctas + 1, 0);
+  p.chunk_off.assign(num_ctas + 1, 0);
+  for (int c = 0; c < num_ctas; ++c) {
+    uint32_t base = (uint32_t)p.chunks.size();
+    for (Task t : cta_tasks[c]) {
+      t.chunk0 += base;
+      p.tasks.push_back(t);
+    }
+    p.chunks.insert(p.chunks.end(), cta_chunks[c].begin(), cta_chunks[c].end());
+    p.task_off[c + 1] = (uint32_t)p.tasks.size();
+    p.chunk_off[c + 1] = (uint32_t)p.chunks.size();
+  }
+  p.weight_bytes = 0;
+  for (const Chunk& c : p.chunks)
+    if (c.rows != kAttnChunk) p.weight_bytes += c.bytes;
+  p.max_cta_bytes = *std::max_element(cta_bytes.begin(), cta_bytes.end());
+  return check_plan(s, w, p);
+}
+
+namespace {
+int op_rank(const Task& t) { return t.type == T_LMHEAD ? 1 << 30 : t.layer * 8 + t.type; }
+}  // namespace
+
+std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) {
+  char buf[256];
+  const int qd = s.nq * s.d, kvd = s.nkv * s.d;
+  // tensor extents (base -> bytes) for bounds checks
+  std::map<uint64_t, uint64_t> extent;
+  extent[w.embed] = (uint64_t)s.V * s.H * 2;
+  for (int l = 0; l < s.L; ++l) {
+    const auto& W = w.layers[l];
+    extent[W[W_Q]] = (uint64_t)qd * s.H * 2;
+    extent[W[W_K]] = (uint64_t)kvd * s.H * 2;
+    extent[W[W_V]] = (uint64_t)kvd * s.H * 2;
+    extent[W[W_O]] = (uint64_t)s.H * qd * 2;
+    extent[W[W_GATE]] = (uint64_t)s.I * s.H * 2;
+    extent[W[W_UP]] = (uint64_t)s.I * s.H * 2;
+    extent[W[W_DOWN]] = (uint64_t)s.H * s.I * 2;
+  }
+  std::map<uint64_t, std::vector<int>> covered;  // tensor base -> per-row count
+  auto row_bytes_of = [&](uint64_t base) -> int {
+    if (base == w.embed) return s.H * 2;
+    for (int l = 0; l < s.L; ++l) {
+      const auto& W = w.layers[l];
+      if (base == W[W_O]) return qd * 2;
+      if (base == W[W_DOWN]) return s.I * 2;
+    }
+    return s.H * 2;
+  };
+  for (auto& e : extent) covered[e.first].assign(e.second / row_bytes_of(e.first), 0);
+
+  if ((int)p.task_off.size() != p.num_ctas + 1 || (int)p.chunk_off.size() != p.num_ctas + 1) return "offsets size";
+  // every CTA's tasks use exactly its chunk range, in order
+  for (int c = 0; c < p.num_ctas; ++c) {
+    uint32_t next = p.chunk_off[c];
+    for (uint32_t i = p.task_off[c]; i < p.task_off[c + 1]; ++i) {
+      if (p.tasks[i].chunk0 != next) return "task chunks not contiguous in CTA order";
+      next += p.tasks[i].nchunks;
+    }
+    if (next != p.chunk_off[c + 1]) return "CTA chunk range not covered by its tasks";
+  }
+  int attn_tasks = 0;
+  for (int c = 0; c < p.num_ctas; ++c) {
+    int last_rank = -1;
+    for (uint32_t i = p.task_off[c]; i < p.task_off[c + 1]; ++i) {
+      const Task& t = p.tasks[i];
+      int rk = op_rank(t);
+      if (rk < last_rank) {
+        snprintf(buf, sizeof buf, "CTA %d: task %u out of topological order", c, i);
+        return buf;
+      }
+      last_rank = rk;
+      if (t.chunk0 < p.chunk_off[c] || t.chunk0 + t.nchunks > p.chunk_off[c + 1]) return "task chunks outside its CTA";
+      if (t.type == T_ATTN) {
+        ++attn_tasks;
+        if (t.nchunks != 1 || (int)t.row0 >= s.nkv || (int)t.nrows >= p.nsplit) return "bad attention task";
+        const Chunk& ph = p.chunks[t.chunk0];
+        if (ph.rows != kAttnChunk || (int)(ph.src >> 48) != t.layer || (int)((ph.src >> 32) & 0xFFFF) != (int)t.row0 ||
+            (uint32_t)ph.src != t.nrows)
+          return "bad attention placeholder";
+        continue;
+      }
+      int res = t.type == T_GATEUP ? 2 * (int)t.nrows : (int)t.nrows;
+      if (res > kMaxTaskRows || t.nrows == 0) return "task result slots exceeded";
+      if (t.wpr == 0 || t.wpr > (uint32_t)kComputeWarps || (t.wpr & (t.wpr - 1)) || (uint64_t)res * t.wpr > (uint64_t)kResSlots)
+        return "bad warps-per-row";
+      int rows_seen = 0;
+      for (uint32_t k = t.chunk0; k < t.chunk0 + t.nchunks; ++k) {
+        if (k >= p.chunks.size()) return "chunk index out of range";
+        const Chunk& ch = p.chunks[k];
+        if (ch.bytes == 0 || ch.bytes % 16 || ch.src % 16 || ch.bytes > (uint32_t)kStageBytes) {
+          snprintf(buf, sizeof buf, "chunk %u: bad size/alignment (%u bytes at %llx)", k, ch.bytes, (unsigned long long)ch.src);
+          return buf;
+        }
+        auto it = extent.upper_bound(ch.src);
+        if (it == extent.begin()) return "chunk outside every tensor";
+        --it;
+        if (ch.src + ch.bytes > it->first + it->second) return "chunk runs past its tensor";
+        int rb = row_bytes_of(it->first);
+        if ((ch.src - it->first) % rb || ch.bytes != ch.rows * (uint32_t)rb) return "chunk not whole rows";
+        int r0 = (int)((ch.src - it->first) / rb);
+        for (uint32_t r = 0; r < ch.rows; ++r) covered[it->first][r0 + r] += 1;
+        rows_seen += (int)ch.rows;
+      }
+      if (t.nchunks > (uint32_t)kMaxTaskChunks) return "too many chunks in one task";
+      if (rows_seen != res) {
+        snprintf(buf, sizeof buf, "task %u: %d chunk rows for %d results", i, rows_seen, res);
+        return buf;
+      }
+    }
+  }
+  for (auto& cv : covered)
+    for (size_t r = 0; r < cv.second.size(); ++r)
+      if (cv.second[r] != 1) {
+        snprintf(buf, sizeof buf, "weight row %zu of tensor %llx streamed %d times", r, (unsigned long long)cv.first, cv.second[r]);
+        return buf;
+      }
+  if (attn_tasks != s.L * s.nkv * p.nsplit) return "attention task count";
+  if (p.smem_bytes > 232448) return "shared memory over the sm_10x limit";
+  return "";
+}
+
+}  // namespace mbk

@@ -1,0 +1,57 @@
+// mbk_sched.h -- host-side static scheduler: turns a decoder shape into per-CTA task lists.
+#pragma once
+#include <stdint.h>
+
+#include <array>
+#include <string>
+#include <vector>
+
+#include "mbk_plan.h"
+
+namespace mbk {
+
+// Device addresses of the weights (as integers, so the scheduler can also run on fake addresses).
+enum WeightSlot { W_ATTN_NORM, W_Q, W_K, W_V, W_BQ, W_BK, W_BV, W_O, W_MLP_NORM, W_GATE, W_UP, W_DOWN, W_NSLOTS };
+struct WeightAddrs {
+  uint64_t embed = 0, final_norm = 0;
+  std::vector<std::array<uint64_t, W_NSLOTS>> layers;
+};
+
+struct PlanOptions {
+  int max_tasks_per_op = 0;    // split each projection into at most this many tasks (0: one per CTA)
+  int smem_limit = 232448;     // dynamic shared memory available per CTA
+};
+
+struct Plan {
+  int num_ctas = 0;
+  std::vector<Task> tasks;           // every CTA's tasks, CTA-major
+  std::vector<uint32_t> task_off;    // [num_ctas + 1] offsets into tasks
+  std::vector<Chunk> chunks;         // weight chunks and attention placeholders (Task::chunk0), CTA-major
+  std::vector<uint32_t> chunk_off;   // [num_ctas + 1] offsets into chunks
+  ActLayout act{};
+  uint64_t act_words = 0;            // words per step (one parity)
+  int nsplit = 1;                    // context splits per KV head
+  int split_len = 0;                 // positions per split
+  int attn_rows_per_stage = 0;       // cached positions per ring stage
+  int num_stages = 0;
+  int smem_bytes = 0;
+  int sv_floats = 0;                 // floats in the input-vector region
+  uint32_t off_sv = 0, off_res = 0, off_resid = 0, off_ring = 0;  // shared-memory layout (bytes)
+  int64_t weight_bytes = 0;          // static chunk bytes per step
+  int64_t max_cta_bytes = 0;
+};
+
+// Returns an empty string on success, otherwise the reason the shape is unsupported.
+std::string validate_shape(const PlanShape& s);
+
+// Builds the plan.  Returns "" or an error message.
+std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, const PlanOptions& opt, Plan* out);
+
+// Independent consistency checks of a built plan (coverage of every weight row exactly once,
+// per-CTA task order, copy alignment and bounds, stage and result capacities).
+std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p);
+
+// Fake, well-separated weight addresses for planning without device memory.
+WeightAddrs fake_weight_addrs(const PlanShape& s);
+
+}  // namespace mbk

@@ -1,0 +1,268 @@
+"""ctypes binding of the C ABI in include/mbk.h (libmbk.so, built in-tree by build.py).
+
+Argument marshalling only: every step of the decode runs in the library's CUDA kernels.  PyTorch
+is used for device memory and streams.  There is no fallback: if libmbk.so is missing or cannot be
+loaded, `load_library()` raises.
+
+The functions keep the C names (mbk_create, mbk_decode_step, ...).  `Decoder` bundles a workload's
+weights (copied to the GPU with torch), a KV cache and a handle for convenience.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmbk.so")
+
+MBK_OK = 0
+MBK_ERR_INVALID_ARG = -1
+MBK_ERR_UNSUPPORTED = -2
+MBK_ERR_CUDA = -3
+MBK_ERR_TIMEOUT = -4
+MBK_ERR_NOMEM = -5
+MBK_ERR_STATE = -6
+
+EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
+            "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
+            "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject")
+TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
+
+
+class MbkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {mbk_error_string(code)} ({code})")
+
+
+class MbkConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("intermediate", ctypes.c_int),
+                ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("kv_capacity", ctypes.c_int), ("rms_eps", ctypes.c_double),
+                ("rope_theta", ctypes.c_double), ("qkv_bias", ctypes.c_int)]
+
+
+LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")
+
+
+class MbkLayerWeights(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in LAYER_FIELDS]
+
+
+class MbkWeights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(MbkLayerWeights))]
+
+
+class MbkPlanInfo(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int), ("num_tasks", ctypes.c_int), ("num_chunks", ctypes.c_int),
+                ("stage_bytes", ctypes.c_int), ("num_stages", ctypes.c_int), ("attn_splits", ctypes.c_int),
+                ("weight_bytes", ctypes.c_int64), ("max_cta_bytes", ctypes.c_int64), ("act_words", ctypes.c_int64),
+                ("smem_bytes", ctypes.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmbk.so (raises if it is missing: there is no other implementation to fall back to)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is not built; run `python -m persistent_decode_megakernel_gb300.build` "
+                               "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(p)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        lib.mbk_create.argtypes = [ctypes.POINTER(MbkConfig), ctypes.POINTER(MbkWeights), vp, ctypes.c_int,
+                                   ctypes.POINTER(vp)]
+        lib.mbk_create.restype = ctypes.c_int
+        lib.mbk_decode_step.argtypes = [vp, i32, i32, vp, vp]
+        lib.mbk_decode_step.restype = ctypes.c_int
+        lib.mbk_decode_step_host.argtypes = [vp, i32, i32, vp, vp]
+        lib.mbk_decode_step_host.restype = ctypes.c_int
+        lib.mbk_kv_fill.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, vp]
+        lib.mbk_kv_fill.restype = ctypes.c_int
+        lib.mbk_get_status.argtypes = [vp]
+        lib.mbk_get_status.restype = ctypes.c_int
+        lib.mbk_error_string.argtypes = [ctypes.c_int]
+        lib.mbk_error_string.restype = ctypes.c_char_p
+        lib.mbk_destroy.argtypes = [vp]
+        lib.mbk_destroy.restype = None
+        lib.mbk_plan_check.argtypes = [ctypes.POINTER(MbkConfig), ctypes.c_int, ctypes.POINTER(MbkPlanInfo)]
+        lib.mbk_plan_check.restype = ctypes.c_int
+        lib.mbk_debug_taps.argtypes = [vp, vp]
+        lib.mbk_debug_taps.restype = ctypes.c_int
+        lib.mbk_debug_plan.argtypes = [vp, vp, ctypes.c_int64]
+        lib.mbk_debug_plan.restype = ctypes.c_int64
+        lib.mbk_trace_enable.argtypes = [vp, ctypes.c_int]
+        lib.mbk_trace_enable.restype = ctypes.c_int
+        lib.mbk_trace_read.argtypes = [vp, vp, ctypes.c_int64]
+        lib.mbk_trace_read.restype = ctypes.c_int64
+        lib.mbk_debug_inject.argtypes = [vp, vp]
+        lib.mbk_debug_inject.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != MBK_OK:
+        raise MbkError(rc, where)
+
+
+def mbk_error_string(code: int) -> str:
+    return load_library().mbk_error_string(int(code)).decode()
+
+
+def config_from_shape(shape) -> MbkConfig:
+    return MbkConfig(shape.n_layers, shape.hidden, shape.intermediate, shape.n_heads, shape.n_kv_heads,
+                     shape.head_dim, shape.vocab, shape.kv_capacity, float(shape.rms_eps), float(shape.rope_theta),
+                     int(shape.qkv_bias))
+
+
+def mbk_plan_check(cfg: MbkConfig, num_sms: int) -> MbkPlanInfo:
+    info = MbkPlanInfo()
+    _check(load_library().mbk_plan_check(ctypes.byref(cfg), int(num_sms), ctypes.byref(info)), "mbk_plan_check")
+    return info
+
+
+def mbk_create(cfg: MbkConfig, weights: MbkWeights, kv_cache_ptr: int, device: int) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(load_library().mbk_create(ctypes.byref(cfg), ctypes.byref(weights), ctypes.c_void_p(kv_cache_ptr),
+                                      int(device), ctypes.byref(h)), "mbk_create")
+    return h
+
+
+def mbk_decode_step(h, token_id: int, position: int, logits_ptr: int, stream_ptr: int) -> int:
+    return load_library().mbk_decode_step(h, int(token_id), int(position), ctypes.c_void_p(logits_ptr),
+                                          ctypes.c_void_p(stream_ptr))
+
+
+def mbk_decode_step_host(h, token_id: int, position: int, logits_host_ptr: int, stream_ptr: int) -> int:
+    return load_library().mbk_decode_step_host(h, int(token_id), int(position), ctypes.c_void_p(logits_host_ptr),
+                                               ctypes.c_void_p(stream_ptr))
+
+
+def mbk_kv_fill(h, layer: int, k_raw_ptr: int, v_raw_ptr: int, p0: int, n: int, stream_ptr: int) -> int:
+    return load_library().mbk_kv_fill(h, int(layer), ctypes.c_void_p(k_raw_ptr), ctypes.c_void_p(v_raw_ptr), int(p0),
+                                      int(n), ctypes.c_void_p(stream_ptr))
+
+
+def mbk_get_status(h) -> int:
+    return load_library().mbk_get_status(h)
+
+
+def mbk_destroy(h) -> None:
+    if h:
+        load_library().mbk_destroy(h)
+
+
+def mbk_debug_taps(h, n_layers: int, hidden: int):
+    import numpy as np
+    out = np.empty((2 * n_layers + 1, hidden), dtype=np.float32)
+    _check(load_library().mbk_debug_taps(h, out.ctypes.data), "mbk_debug_taps")
+    return out
+
+
+def mbk_debug_plan(h):
+    import numpy as np
+    lib = load_library()
+    n = lib.mbk_debug_plan(h, None, 0)
+    if n < 0:
+        raise MbkError(int(n), "mbk_debug_plan")
+    out = np.empty((n, 6), dtype=np.int32)
+    lib.mbk_debug_plan(h, out.ctypes.data, n)
+    return out
+
+
+def mbk_debug_inject(h, x_in) -> None:
+    """x_in: fp32 numpy [n_layers, hidden] (row l = input of layer l >= 1) for the next step, or None."""
+    import numpy as np
+    if x_in is None:
+        _check(load_library().mbk_debug_inject(h, None), "mbk_debug_inject")
+        return
+    a = np.ascontiguousarray(x_in, dtype=np.float32)
+    _check(load_library().mbk_debug_inject(h, a.ctypes.data), "mbk_debug_inject")
+
+
+def mbk_trace_enable(h, enable: bool) -> None:
+    _check(load_library().mbk_trace_enable(h, int(bool(enable))), "mbk_trace_enable")
+
+
+def mbk_trace_read(h):
+    import numpy as np
+    lib = load_library()
+    n = lib.mbk_debug_plan(h, None, 0)
+    out = np.zeros((n, 4), dtype=np.uint64)
+    r = lib.mbk_trace_read(h, out.ctypes.data, n)
+    if r < 0:
+        raise MbkError(int(r), "mbk_trace_read")
+    return out
+
+
+class Decoder:
+    """A workload's weights on the GPU, a bf16 KV cache and a library handle.
+
+    step() launches one decode step into a device logits tensor on the current torch stream.
+    """
+
+    def __init__(self, wl, device: int = 0):
+        import torch
+        self.torch = torch
+        s = wl.shape
+        self.shape = s
+        dev = torch.device("cuda", device)
+        self.device = dev
+        self.embed = wl.embed.to(dev)
+        self.final_norm = wl.final_norm.to(dev)
+        self.layers = [{k: (None if v is None else v.to(dev)) for k, v in w.items()} for w in wl.layers]
+        self.kv = torch.zeros((s.n_layers, 2, s.n_kv_heads, s.kv_capacity, s.head_dim), dtype=torch.bfloat16, device=dev)
+        arr = (MbkLayerWeights * s.n_layers)()
+        for i, w in enumerate(self.layers):
+            for k in LAYER_FIELDS:
+                t = w.get(k)
+                setattr(arr[i], k, None if t is None else t.data_ptr())
+        self._layer_arr = arr
+        self.weights = MbkWeights(self.embed.data_ptr(), self.final_norm.data_ptr(), arr)
+        self.cfg = config_from_shape(s)
+        self.handle = mbk_create(self.cfg, self.weights, self.kv.data_ptr(), device)
+        self.logits = torch.empty(s.vocab, dtype=torch.float32, device=dev)
+        if s.prefill:
+            self.fill(wl.k_raw, wl.v_raw, 0)
+
+    def fill(self, k_raw, v_raw, p0: int) -> None:
+        """Load cache rows p0.. of every layer from pre-RoPE K and V (fp32 [L][nkv][n][d])."""
+        torch = self.torch
+        stream = torch.cuda.current_stream(self.device).cuda_stream
+        n = k_raw.shape[2]
+        for l in range(self.shape.n_layers):
+            kr = k_raw[l].to(self.device, torch.float32).contiguous()
+            vr = v_raw[l].to(self.device, torch.float32).contiguous()
+            _check(mbk_kv_fill(self.handle, l, kr.data_ptr(), vr.data_ptr(), p0, n, stream), "mbk_kv_fill")
+            torch.cuda.current_stream(self.device).synchronize()
+
+    def step(self, token: int, pos: int, logits=None):
+        out = self.logits if logits is None else logits
+        stream = self.torch.cuda.current_stream(self.device).cuda_stream
+        _check(mbk_decode_step(self.handle, token, pos, out.data_ptr(), stream), "mbk_decode_step")
+        return out
+
+    def status(self) -> int:
+        return mbk_get_status(self.handle)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            mbk_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

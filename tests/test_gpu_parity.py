@@ -1,0 +1,176 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on seeded, teacher-forced
+token streams, for every decoder shape at full size, plus the edge cases of the method."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from persistent_decode_megakernel_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+from parity import run_parity  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from persistent_decode_megakernel_gb300 import build
+    build.build()
+
+
+CONFIGS = ["tiny", "smollm-135m", "qwen2-0.5b", "smollm-135m-long", "smollm-1.7b"]
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_full_config_parity(name):
+    """Every step of the config's teacher-forced stream, each step from the oracle's state."""
+    wl = workloads.generate(name, seed=0)
+    rep = run_parity(wl, mode="sync")
+    print(f"\n{name} sync: {rep}")
+    rep.check()
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_kv_rows_region_by_region(name):
+    """Every new KV-cache row of every layer, each computed from the oracle's input to that layer
+    (teacher forcing of token, cache and layer inputs): within one bf16 ulp."""
+    wl = workloads.generate(name, seed=0)
+    rep = run_parity(wl, mode="layers")
+    print(f"\n{name} layers: {rep}")
+    rep.check()
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_full_config_free_running(name):
+    """The same stream with each side carrying its own cache."""
+    wl = workloads.generate(name, seed=0)
+    rep = run_parity(wl, mode="free")
+    print(f"\n{name} free: {rep}")
+    rep.check()
+
+
+def test_tiny_with_random_gains():
+    rep = run_parity(workloads.generate("tiny", seed=1, random_gains=True))
+    rep.check()
+
+
+def test_last_cache_rows_and_ragged_split():
+    """Decode up to the last cache row (pos = C-1) with a context that spans several splits and a
+    ragged final split."""
+    shape = workloads.scaled_down(workloads.SHAPES["smollm-135m-long"], n_layers=2, kv_capacity=1500, prefill=1494,
+                                  pos0=1494, steps=6, vocab=8192)
+    rep = run_parity(workloads.generate(shape, seed=5))
+    rep.check()
+
+
+def test_split_boundary_positions():
+    """Steps whose position is the first row of a new split (owner split with no history)."""
+    shape = workloads.scaled_down(workloads.SHAPES["smollm-135m-long"], n_layers=2, kv_capacity=2048, prefill=1022,
+                                  pos0=1022, steps=4, vocab=4096)
+    rep = run_parity(workloads.generate(shape, seed=6))
+    rep.check()
+
+
+def test_mha_head_dim_128():
+    shape = workloads.DecoderShape("mha128", 2, 512, 1024, 4, 4, 128, 2048, 64, 1e-5, 1e4, False, steps=12)
+    rep = run_parity(workloads.generate(shape, seed=7))
+    rep.check()
+
+
+def test_bias_small_shape():
+    shape = workloads.scaled_down(workloads.SHAPES["qwen2-0.5b"], n_layers=3, vocab=8192, steps=10)
+    rep = run_parity(workloads.generate(shape, seed=8))
+    rep.check()
+
+
+def test_deterministic_and_resumable():
+    """Bitwise-identical logits on a rerun, and after resuming from a copied cache in a new handle."""
+    from persistent_decode_megakernel_gb300.mbk import Decoder
+    wl = workloads.generate("tiny", seed=0)
+    a = Decoder(wl)
+    full = torch.stack([a.step(int(wl.tokens[i]), i).clone() for i in range(10)])
+    b = Decoder(wl)
+    part = [b.step(int(wl.tokens[i]), i).clone() for i in range(6)]
+    c = Decoder(wl)
+    c.kv.copy_(b.kv)
+    rest = [c.step(int(wl.tokens[i]), i).clone() for i in range(6, 10)]
+    torch.cuda.synchronize()
+    assert torch.equal(full, torch.stack(part + rest))
+    for d in (a, b, c):
+        d.close()
+
+
+def test_host_buffer_step_matches_device_step():
+    from persistent_decode_megakernel_gb300 import mbk
+    wl = workloads.generate("tiny", seed=0)
+    a = mbk.Decoder(wl)
+    b = mbk.Decoder(wl)
+    host = torch.empty(wl.shape.vocab, dtype=torch.float32, pin_memory=True)
+    stream = torch.cuda.current_stream().cuda_stream
+    for i in range(5):
+        dev = a.step(int(wl.tokens[i]), i).clone()
+        rc = mbk.mbk_decode_step_host(b.handle, int(wl.tokens[i]), i, host.data_ptr(), stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert torch.equal(dev.cpu(), host)
+    a.close()
+    b.close()
+
+
+def test_invalid_arguments_do_not_launch():
+    from persistent_decode_megakernel_gb300 import mbk
+    wl = workloads.generate("tiny", seed=0)
+    d = mbk.Decoder(wl)
+    s = wl.shape
+    stream = torch.cuda.current_stream().cuda_stream
+    for tok, pos in [(-1, 0), (s.vocab, 0), (0, -1), (0, s.kv_capacity)]:
+        assert mbk.mbk_decode_step(d.handle, tok, pos, d.logits.data_ptr(), stream) == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_decode_step(d.handle, 0, 0, 0, stream) == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_kv_fill(d.handle, s.n_layers, d.logits.data_ptr(), d.logits.data_ptr(), 0, 1, stream) == \
+        mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_kv_fill(d.handle, 0, d.logits.data_ptr(), d.logits.data_ptr(), s.kv_capacity, 1, stream) == \
+        mbk.MBK_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert d.status() == 0
+    d.close()
+
+
+def test_interleaved_handles_are_independent():
+    from oracle import OracleDecoder
+    from persistent_decode_megakernel_gb300.mbk import Decoder
+    w1 = workloads.generate("tiny", seed=11)
+    w2 = workloads.generate(workloads.scaled_down(workloads.SHAPES["tiny"], n_layers=3, hidden=384, vocab=2048), seed=12)
+    g1, g2 = Decoder(w1), Decoder(w2)
+    o1, o2 = OracleDecoder(w1), OracleDecoder(w2)
+    for i in range(6):
+        a = g1.step(int(w1.tokens[i]), i).cpu().numpy()
+        b = g2.step(int(w2.tokens[i]), i).cpu().numpy()
+        ra, rb = o1.step(int(w1.tokens[i]), i), o2.step(int(w2.tokens[i]), i)
+        assert np.linalg.norm(a - ra) / np.linalg.norm(ra) < 2e-3
+        assert np.linalg.norm(b - rb) / np.linalg.norm(rb) < 2e-3
+    g1.close()
+    g2.close()
+
+
+def test_wait_timeout_is_reported_and_sticky(monkeypatch):
+    """A producer task is dropped (host-side injection), so its consumers' bounded waits run out: the
+    step reports MBK_ERR_TIMEOUT, later calls return it without launching, and the GPU context stays
+    usable for a fresh handle."""
+    from persistent_decode_megakernel_gb300 import mbk
+    wl = workloads.generate("tiny", seed=0)
+    monkeypatch.setenv("MBK_DEBUG_DROP_TASK", "0")
+    monkeypatch.setenv("MBK_WAIT_TIMEOUT_MS", "100")
+    d = mbk.Decoder(wl)
+    monkeypatch.delenv("MBK_DEBUG_DROP_TASK")
+    monkeypatch.delenv("MBK_WAIT_TIMEOUT_MS")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert mbk.mbk_decode_step(d.handle, int(wl.tokens[0]), 0, d.logits.data_ptr(), stream) == mbk.MBK_OK
+    torch.cuda.synchronize()
+    assert d.status() == mbk.MBK_ERR_TIMEOUT
+    assert mbk.mbk_decode_step(d.handle, int(wl.tokens[1]), 1, d.logits.data_ptr(), stream) == mbk.MBK_ERR_TIMEOUT
+    d.close()
+    rep = run_parity(wl, steps=4)
+    rep.check()
