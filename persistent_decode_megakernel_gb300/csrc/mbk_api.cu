@@ -290,6 +290,7 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   kp.status = h->d_status;
   kp.host_status = h_status_dev;
   kp.timeout_ns = (unsigned long long)env_int("MBK_WAIT_TIMEOUT_MS", 1000) * 1000000ull;
+  kp.poll_backoff_ns = (unsigned)std::max(0, env_int("MBK_POLL_BACKOFF_NS", 0));
   *out = h;
   return MBK_OK;
 }

@@ -15,7 +15,7 @@ struct LayerW {
   const uint16_t* w[12];
 };
 
-// Constant for the lifetime of a handle.
+// Constant for the lifetime of a handle (4-byte multiple, copied word by word into shared memory).
 struct KernelParams {
   int L, H, I, nq, nkv, d, V, C, g;
   float eps, attn_scale;
@@ -40,6 +40,7 @@ struct KernelParams {
   unsigned long long timeout_ns;
   unsigned long long* trace;    // null, or 4 globaltimer stamps per task (begin, ready, end, first stage)
   const unsigned long long* inject;  // null, or words [L][H]: row l replaces the input of layer l >= 1
+  unsigned poll_backoff_ns;     // sleep between polls of a word that is not ready yet (0: none)
 };
 
 // Changes every step.

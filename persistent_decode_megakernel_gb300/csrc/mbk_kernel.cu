@@ -14,8 +14,10 @@
 //               travel in one single-copy-atomic store, so no fence, counter or grid barrier is
 //               needed (the pages' counting grid barrier is the thing this replaces).
 // Everything a task needs that does not depend on the token (norm gains, biases, RoPE cos/sin,
-// the next task's descriptor) is loaded before the task waits for its inputs, so the critical path
-// of a task is: inputs arrive -> one block barrier -> GEMV on shared-memory weights -> words out.
+// descriptors) is loaded before the task waits for its inputs -- gains one task ahead -- so the
+// critical path of a task is: inputs arrive -> one block barrier -> GEMV on shared-memory weights
+// -> words out.  All task code is inlined into the kernel so its context stays in registers; only
+// the rare slow paths (a word that is not ready yet, a failure) are out of line.
 // Every spin is bounded by a globaltimer budget; on expiry the CTA records timeout status and
 // finishes its task list without waiting or writing, so the launch always terminates.
 #include <cuda_bf16.h>
@@ -90,7 +92,13 @@ __device__ __forceinline__ float warp_max(float v) {
 
 constexpr int kCT = kComputeWarps * 32;  // compute threads
 
-// Shared-memory control block (first KB of dynamic shared memory).
+// Input vectors of a GEMV live in shared memory in a split layout: element i of n sits at
+// (i/8)*4 + i%4 in the lower half (i%8 < 4) or at n/2 + (i/8)*4 + i%4 - 4 in the upper half, so the
+// two float4 a lane multiplies with one 16-byte weight vector are contiguous across lanes.
+__device__ __forceinline__ int xpos(int i, int n) { return ((i >> 3) << 2) + (i & 3) + ((i & 4) ? (n >> 1) : 0); }
+
+
+// Shared-memory control block (the first kCtlBytes of dynamic shared memory).
 struct Ctl {
   uint64_t full[kMaxRingStages];
   uint64_t empty[kMaxRingStages];
@@ -100,115 +108,152 @@ struct Ctl {
   unsigned skip;        // an earlier step failed: this launch does nothing
   unsigned pad;
   float red[32];        // block reduction scratch
+  float2 rope[64];      // cos/sin of this step's position, i < head_dim / 2
+  const uint16_t* gain[2 * kMaxLayers + 1];  // attn_norm[l] at 2l, mlp_norm[l] at 2l+1, final at 2L
+  const uint16_t* bias[3 * kMaxLayers];      // bq, bk, bv of layer l at 3l..3l+2
+  KernelParams params;  // the launch parameters, copied here: reads through a pointer into the
+                        // parameter window are slow, shared-memory reads are not
 };
-static_assert(sizeof(Ctl) <= 1024, "control block must fit the first KB");
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block too large");
 
+// ------------------------------------------------------------------ out-of-line slow paths
+__device__ __noinline__ void record_failure(unsigned* status, unsigned* host_status, unsigned* abort_flag,
+                                            unsigned task, unsigned detail) {
+  if (atomicCAS(&status[0], 0u, (unsigned)DS_TIMEOUT) == 0u) {
+    status[1] = blockIdx.x;
+    status[2] = task;
+    status[3] = detail;
+    if (host_status) {
+      volatile unsigned* hs = host_status;
+      hs[1] = blockIdx.x;
+      hs[2] = task;
+      hs[3] = detail;
+      __threadfence_system();
+      hs[0] = (unsigned)DS_TIMEOUT;
+    }
+  }
+  *(volatile unsigned*)abort_flag = 1u;
+}
+
+// Keeps polling a word that was not ready at the first load; returns its value (0 on abort).
+__device__ __noinline__ float spin_word(const unsigned long long* p, unsigned tag, unsigned* abort_flag, unsigned* status,
+                                        unsigned* host_status, unsigned long long timeout, unsigned task,
+                                        unsigned detail, unsigned backoff_ns) {
+  if (*(volatile unsigned*)abort_flag) return 0.f;
+  const unsigned long long t0 = global_ns();
+  for (unsigned n = 1;; ++n) {
+    if (backoff_ns) __nanosleep(backoff_ns);
+    const unsigned long long w = ld_word(p);
+    if ((unsigned)(w >> 32) == tag) return __uint_as_float((unsigned)w);
+    if ((n & 63u) == 0u) {
+      if (*(volatile unsigned*)abort_flag) return 0.f;
+      if (*(volatile unsigned*)status != 0u || global_ns() - t0 > timeout) {
+        record_failure(status, host_status, abort_flag, task, detail);
+        return 0.f;
+      }
+    }
+  }
+}
+
+// Waits for a ring stage whose first test failed; records a failure after the timeout.
+__device__ __noinline__ void spin_stage(uint64_t* full, unsigned parity, unsigned* prod_quit, unsigned* status,
+                                        unsigned* host_status, unsigned* abort_flag, unsigned long long timeout,
+                                        unsigned task, unsigned detail) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_test(full, parity)) {
+    if (*(volatile unsigned*)prod_quit) return;  // nothing more will arrive
+    if (global_ns() - t0 > timeout) {
+      record_failure(status, host_status, abort_flag, task, detail);
+      return;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ per-CTA context (registers)
 struct Ctx {
   const KernelParams* P;
-  StepParams S;
   Ctl* ctl;
   unsigned char* ring;
-  unsigned it;          // ring position (same sequence as the producer's)
+  float* logits;
+  unsigned tag;
+  int pos, token;
+  unsigned ns;          // ring stages
+  unsigned stage;       // ring slot of the next stage to consume
+  unsigned phase;       // its parity
   int ctid;             // 0..511 among compute threads
   int warp, lane;       // compute warp 0..15
   unsigned task_index;
   bool first_stage;     // tracing: the task has not yet received a weight stage
 };
 
-// Tracing (off unless P.trace is set): stamp slot k of the current task.
 __device__ __forceinline__ void trace_mark(Ctx& c, int k) {
   if (c.P->trace != nullptr && c.ctid == 0) c.P->trace[(size_t)c.task_index * 4 + k] = global_ns();
 }
-
-__device__ void record_failure(Ctx& c, unsigned detail) {
-  const KernelParams& P = *c.P;
-  if (atomicCAS(&P.status[0], 0u, (unsigned)DS_TIMEOUT) == 0u) {
-    P.status[1] = blockIdx.x;
-    P.status[2] = c.task_index;
-    P.status[3] = detail;
-    if (P.host_status) {
-      volatile unsigned* hs = P.host_status;
-      hs[1] = blockIdx.x;
-      hs[2] = c.task_index;
-      hs[3] = detail;
-      __threadfence_system();
-      hs[0] = (unsigned)DS_TIMEOUT;
-    }
-  }
-  *(volatile unsigned*)&c.ctl->abort = 1u;
-}
-
 __device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile unsigned*)&c.ctl->abort != 0u; }
-
-// Finish waiting for a word that was not ready at the first load; returns its value (0 on abort).
-__device__ __noinline__ float spin_word(Ctx& c, const unsigned long long* p, unsigned detail) {
-  if (aborted(c)) return 0.f;
-  unsigned long long t0 = global_ns();
-  for (unsigned n = 1;; ++n) {
-    const unsigned long long w = ld_word(p);
-    if ((unsigned)(w >> 32) == c.S.tag) return __uint_as_float((unsigned)w);
-    if ((n & 63u) == 0u) {
-      if (aborted(c)) return 0.f;
-      if (*(volatile unsigned*)c.P->status != 0u || global_ns() - t0 > c.P->timeout_ns) {
-        record_failure(c, detail);
-        return 0.f;
-      }
-    }
-  }
-}
 __device__ __forceinline__ float word_value(Ctx& c, unsigned long long w, const unsigned long long* p, unsigned detail) {
-  return (unsigned)(w >> 32) == c.S.tag ? __uint_as_float((unsigned)w) : spin_word(c, p, detail);
+  if ((unsigned)(w >> 32) == c.tag) return __uint_as_float((unsigned)w);
+  return spin_word(p, c.tag, &c.ctl->abort, c.P->status, c.P->host_status, c.P->timeout_ns, c.task_index, detail,
+                   c.P->poll_backoff_ns);
 }
-
 __device__ __forceinline__ void put_word(Ctx& c, unsigned long long* p, float v) {
-  if (!aborted(c)) st_word(p, c.S.tag, v);
+  if (!aborted(c)) st_word(p, c.tag, v);
 }
 
-// Batched polling: this thread's words src[i], i = ctid + k*kCT < n, with up to 8 loads in flight.
+// Batched polling: this thread's words src[i], i = ctid + k*kCT < n, with up to 4 loads in flight.
 template <typename F>
 __device__ __forceinline__ void poll_words(Ctx& c, const unsigned long long* src, int n, unsigned detail, F&& sink) {
-  for (int k0 = 0; k0 * kCT < n; k0 += 8) {
-    unsigned long long w[8];
+  for (int k0 = 0; k0 * kCT < n; k0 += 4) {
+    unsigned long long w[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 4; ++k) {
       const int i = c.ctid + (k0 + k) * kCT;
       w[k] = i < n ? ld_word(src + i) : 0ull;
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 4; ++k) {
       const int i = c.ctid + (k0 + k) * kCT;
-      if (i < n) sink(i, word_value(c, w[k], src + i, detail | (unsigned)i));
+      if (i < n) sink(i, k0 + k, word_value(c, w[k], src + i, detail | (unsigned)i));
     }
   }
 }
 
-// Ring stage `idx` (absolute ring position) once its data has landed.
-__device__ __forceinline__ unsigned char* stage_wait(Ctx& c, unsigned idx) {
-  const unsigned ns = (unsigned)c.P->num_stages;
-  const unsigned s = idx % ns, ph = (idx / ns) & 1u;
-  if (!mbar_test(&c.ctl->full[s], ph)) {
-    unsigned long long t0 = global_ns();
-    while (!mbar_test(&c.ctl->full[s], ph)) {
-      if (*(volatile unsigned*)&c.ctl->prod_quit) break;  // nothing more will arrive
-      if (global_ns() - t0 > c.P->timeout_ns) {
-        record_failure(c, 0xF000u | s);
-        break;
-      }
-    }
+// Ring slot `k` stages after the current one (k < ns): its slot index and parity.
+__device__ __forceinline__ void slot_after(const Ctx& c, unsigned k, unsigned& s, unsigned& ph) {
+  s = c.stage + k;
+  ph = c.phase;
+  if (s >= c.ns) {
+    s -= c.ns;
+    ph ^= 1u;
   }
+}
+// The stage k after the current one, once its data has landed.
+__device__ __forceinline__ unsigned char* stage_wait(Ctx& c, unsigned k) {
+  unsigned s, ph;
+  slot_after(c, k, s, ph);
+  if (!mbar_test(&c.ctl->full[s], ph))
+    spin_stage(&c.ctl->full[s], ph, &c.ctl->prod_quit, c.P->status, c.P->host_status, &c.ctl->abort, c.P->timeout_ns,
+               c.task_index, 0xF000u | s);
   if (c.first_stage) {
     trace_mark(c, 3);
     c.first_stage = false;
   }
   return c.ring + (size_t)s * kStageBytes;
 }
+__device__ __forceinline__ unsigned stage_rows_at(const Ctx& c, unsigned k) {
+  unsigned s, ph;
+  slot_after(c, k, s, ph);
+  return c.ctl->stage_rows[s];
+}
 // Hand `n` stages back to the producer (every compute warp arrives once per stage).
 __device__ __forceinline__ void stages_release(Ctx& c, unsigned n) {
-  const unsigned ns = (unsigned)c.P->num_stages;
   __syncwarp();
-  if (c.lane == 0)
-    for (unsigned k = 0; k < n; ++k) mbar_arrive(&c.ctl->empty[(c.it + k) % ns]);
-  c.it += n;
+  for (unsigned k = 0; k < n; ++k) {
+    if (c.lane == 0) mbar_arrive(&c.ctl->empty[c.stage]);
+    if (++c.stage == c.ns) {
+      c.stage = 0;
+      c.phase ^= 1u;
+    }
+  }
 }
 
 __device__ __forceinline__ unsigned long long* layer_words(const KernelParams& P, int l) {
@@ -221,131 +266,245 @@ __device__ __forceinline__ const unsigned long long* x_in_words(const KernelPara
   return P.inject != nullptr ? P.inject + (size_t)l * P.H : layer_words(P, l - 1) + P.act.xm;
 }
 
-// ------------------------------------------------------------------ fused input fetch + RMSNorm
-// Loads the residual stream entering this task (words, or the embedding row for layer 0) as
-// gain * x into sv and returns 1 / sqrt(mean(x^2) + eps): the norm's scalar is applied to the GEMV
-// results, so RMSNorm costs no barrier of its own (the pages' "folding" of small producers into
-// their consumer).  Gains are loaded before the wait.  Ends with a compute barrier.
-__device__ float fetch_normed(Ctx& c, const unsigned long long* src, const uint16_t* gain, float* sv) {
-  const KernelParams& P = *c.P;
-  const int n = P.H;  // <= kMaxTaskRows = 4 * kCT
-  float gr[4];
+// Norm gain a task applies to its input (null for tasks without a norm).
+__device__ __forceinline__ const uint16_t* task_gain(const Ctl* ctl, const Task& t, int L) {
+  if (t.type == T_QKV) return ctl->gain[2 * t.layer];
+  if (t.type == T_GATEUP) return ctl->gain[2 * t.layer + 1];
+  if (t.type == T_LMHEAD) return ctl->gain[2 * L];
+  return nullptr;
+}
+// This thread's gain values (elements ctid + k*kCT) of a task, loaded ahead of the task.
+__device__ __forceinline__ void load_gains(const Ctx& c, const Task& t, float g[4]) {
+  const uint16_t* gp = task_gain(c.ctl, t, c.P->L);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = c.ctid + k * kCT;
-    gr[k] = i < n ? bf16_to_f32(gain[i]) : 0.f;
+    g[k] = (gp != nullptr && i < c.P->H) ? bf16_to_f32(gp[i]) : 0.f;
   }
-  float ss = 0.f;
+}
+
+// ------------------------------------------------------------------ input vector of a GEMV task
+// Loads n activations (words, or the token's embedding row when src is null) into sv in the split
+// layout.  With a norm (gr != null, n == H), it stores gain * x and leaves this thread's share of
+// sum(x^2) in *ss: RMSNorm's scalar 1/sqrt(mean(x^2)+eps) is applied to the GEMV results instead,
+// so the norm costs no barrier of its own (the pages' "folding" of small producers into their
+// consumer).  No barrier here.
+__device__ __forceinline__ void fetch_input(Ctx& c, const unsigned long long* src, int n, const float* gr, float* sv,
+                                            float* ss) {
+  float acc = 0.f;
   if (src == nullptr) {
-    const uint16_t* e = P.embed + (size_t)c.S.token * n;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    const uint16_t* e = c.P->embed + (size_t)c.token * n;
+    for (int k = 0; k * kCT < n; ++k) {
       const int i = c.ctid + k * kCT;
       if (i < n) {
-        const float x = bf16_to_f32(e[i]);
-        ss = fmaf(x, x, ss);
-        sv[i] = x * gr[k];
+        float x = bf16_to_f32(e[i]);
+        if (gr != nullptr) {
+          acc = fmaf(x, x, acc);
+          x *= gr[k & 3];
+        }
+        sv[xpos(i, n)] = x;
       }
     }
   } else {
-    poll_words(c, src, n, 0x100000u, [&](int i, float x) {
-      ss = fmaf(x, x, ss);
-      sv[i] = x * gr[(i - c.ctid) / kCT];
+    poll_words(c, src, n, 0x100000u, [&](int i, int k, float x) {
+      if (gr != nullptr) {
+        acc = fmaf(x, x, acc);
+        x *= gr[k & 3];
+      }
+      sv[xpos(i, n)] = x;
     });
   }
-  ss = warp_sum(ss);
-  if (c.lane == 0) c.ctl->red[c.warp] = ss;
-  compute_sync();
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < kComputeWarps; ++w) tot += c.ctl->red[w];
-  return 1.0f / sqrtf(tot / (float)n + P.eps);
+  *ss = acc;
 }
 
 // ------------------------------------------------------------------ GEMV on ring stages
-// Partial dot products of the task's rows in chunk order: t.wpr warps share each weight row (each
-// takes a K slice), so small chunks still keep all 16 warps busy.  res[row * wpr + slice] =
-// scale * partial; res_row() sums the slices in a fixed order (results are deterministic).
-// Rows per stage come from the producer.  Ends with a compute barrier.
-__device__ void gemv(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
+// Dot products of the task's weight rows (in chunk order) with x, consuming up to kGemvBatch ring
+// stages at a time.  Warps split K into t.gpr slices; each warp keeps its slice of x in registers
+// (loaded once) and streams rows past it, so shared-memory traffic is the weight bytes alone.  Two
+// bf16 weights multiply two x values per packed fp32x2 FMA (each an ordinary fp32 FMA).
+// res[row * gpr + slice] = scale * partial; res_row() sums the slices in a fixed order, so results
+// are deterministic.  Ends with a compute barrier.
+__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long acc) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(acc));
+  return d;
+}
+__device__ __forceinline__ float sum2(unsigned long long v) {
+  return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
+}
+// bf16 pair in one 32-bit word -> fp32x2 {element 2i, element 2i+1}
+__device__ __forceinline__ unsigned long long bf2(uint32_t w) { return pack2(w << 16, w & 0xffff0000u); }
+
+__device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
   const int nvec = in >> 3;  // 16-byte vectors per row
-  const float4* x4 = reinterpret_cast<const float4*>(x);
-  const unsigned ns = (unsigned)c.P->num_stages;
-  const int wpr = (int)t.wpr, rpp = kComputeWarps / wpr;
-  const int r_in = c.warp / wpr, slice = c.warp % wpr;
-  int rbase = 0;
-  for (uint32_t k = 0; k < t.nchunks; ++k) {
-    const unsigned char* stage = stage_wait(c, c.it);
-    const int rows = (int)c.ctl->stage_rows[c.it % ns];
-    for (int r = r_in; r < rows; r += rpp) {
-      const uint4* row = reinterpret_cast<const uint4*>(stage + (size_t)r * in * 2);
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      for (int v = slice * 32 + c.lane; v < nvec; v += wpr * 32) {
-        const uint4 w = row[v];
-        const float4 p = x4[2 * v], q = x4[2 * v + 1];
-        a0 = fmaf(bf16_lo(w.x), p.x, a0);
-        a1 = fmaf(bf16_hi(w.x), p.y, a1);
-        a2 = fmaf(bf16_lo(w.y), p.z, a2);
-        a3 = fmaf(bf16_hi(w.y), p.w, a3);
-        a0 = fmaf(bf16_lo(w.z), q.x, a0);
-        a1 = fmaf(bf16_hi(w.z), q.y, a1);
-        a2 = fmaf(bf16_lo(w.w), q.z, a2);
-        a3 = fmaf(bf16_hi(w.w), q.w, a3);
-      }
-      const float acc = warp_sum((a0 + a1) + (a2 + a3));
-      if (c.lane == 0) res[(rbase + r) * wpr + slice] = acc * scale;
+  const int gpr = (int)t.gpr, gshift = 31 - __clz(gpr);
+  const int slice = c.warp & (gpr - 1), rw = c.warp >> gshift, rpp = kComputeWarps >> gshift;
+  const int vps = (nvec + gpr - 1) >> gshift;  // vectors per slice
+  const int v0 = slice * vps, v1 = min(nvec, v0 + vps);
+  // this lane's x: vectors v0 + lane + 32k, as packed pairs
+  unsigned long long xp[kGemvXVec][4];
+  const float* xhi = x + (in >> 1);
+#pragma unroll
+  for (int k = 0; k < kGemvXVec; ++k) {
+    const int v = v0 + c.lane + 32 * k;
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), q = p;
+    if (v < v1) {
+      p = reinterpret_cast<const float4*>(x)[v];
+      q = reinterpret_cast<const float4*>(xhi)[v];
     }
-    stages_release(c, 1);
-    rbase += rows;
+    xp[k][0] = pack2(__float_as_uint(p.x), __float_as_uint(p.y));
+    xp[k][1] = pack2(__float_as_uint(p.z), __float_as_uint(p.w));
+    xp[k][2] = pack2(__float_as_uint(q.x), __float_as_uint(q.y));
+    xp[k][3] = pack2(__float_as_uint(q.z), __float_as_uint(q.w));
+  }
+  const size_t row_bytes = (size_t)in * 2;
+  int rbase = 0;
+  for (uint32_t k0 = 0; k0 < t.nchunks; k0 += kGemvBatch) {
+    const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
+    const unsigned char* s0 = stage_wait(c, 0);
+    const unsigned char* s1 = nb > 1 ? stage_wait(c, 1) : s0;
+    const unsigned char* s2 = nb > 2 ? stage_wait(c, 2) : s0;
+    const unsigned char* s3 = nb > 3 ? stage_wait(c, 3) : s0;
+    const int n0 = (int)stage_rows_at(c, 0);
+    const int n1 = nb > 1 ? (int)stage_rows_at(c, 1) : 0;
+    const int n2 = nb > 2 ? (int)stage_rows_at(c, 2) : 0;
+    const int n3 = nb > 3 ? (int)stage_rows_at(c, 3) : 0;
+    const int total = n0 + n1 + n2 + n3;
+    auto row_of = [&](int r) -> const uint4* {
+      const unsigned char* base = s0;
+      if (r >= n0) {
+        r -= n0;
+        base = s1;
+        if (r >= n1) {
+          r -= n1;
+          base = s2;
+          if (r >= n2) {
+            r -= n2;
+            base = s3;
+          }
+        }
+      }
+      return reinterpret_cast<const uint4*>(base + (size_t)r * row_bytes);
+    };
+    // two rows per iteration; the loop bound is uniform across the warp (shuffles below)
+    for (int ra = rw; ra < total; ra += 2 * rpp) {
+      const int rb = ra + rpp;
+      const bool two = rb < total;
+      const uint4* A = row_of(ra);
+      const uint4* B = row_of(two ? rb : ra);
+      unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
+#pragma unroll
+      for (int k = 0; k < kGemvXVec; ++k) {
+        const int v = v0 + c.lane + 32 * k;
+        if (v < v1) {
+          const uint4 wa = A[v];
+          const uint4 wb = B[v];
+          a0 = ffma2(bf2(wa.x), xp[k][0], a0);
+          a1 = ffma2(bf2(wa.y), xp[k][1], a1);
+          a0 = ffma2(bf2(wa.z), xp[k][2], a0);
+          a1 = ffma2(bf2(wa.w), xp[k][3], a1);
+          b0 = ffma2(bf2(wb.x), xp[k][0], b0);
+          b1 = ffma2(bf2(wb.y), xp[k][1], b1);
+          b0 = ffma2(bf2(wb.z), xp[k][2], b0);
+          b1 = ffma2(bf2(wb.w), xp[k][3], b1);
+        }
+      }
+      float sa = sum2(a0) + sum2(a1), sb = sum2(b0) + sum2(b1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+        sb += __shfl_xor_sync(0xffffffffu, sb, o);
+      }
+      if (c.lane == 0) {
+        res[((rbase + ra) << gshift) + slice] = sa * scale;
+        if (two) res[((rbase + rb) << gshift) + slice] = sb * scale;
+      }
+    }
+    stages_release(c, (unsigned)nb);
+    rbase += total;
   }
   compute_sync();
 }
-__device__ __forceinline__ float res_row(const float* res, int i, int wpr) {
+// Small tasks (at most 16 rows per batch, t.gpr == 0): one warp per row over the full K, x read
+// from shared memory -- the fewest instructions when each warp has a row or two.
+__device__ __forceinline__ void gemv_rows(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
+  const int nvec = in >> 3;
+  const float4* xlo = reinterpret_cast<const float4*>(x);
+  const float4* xhi = reinterpret_cast<const float4*>(x + (in >> 1));
+  const size_t row_bytes = (size_t)in * 2;
+  int rbase = 0;
+  for (uint32_t k0 = 0; k0 < t.nchunks; k0 += kGemvBatch) {
+    const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
+    const unsigned char* s0 = stage_wait(c, 0);
+    const unsigned char* s1 = nb > 1 ? stage_wait(c, 1) : s0;
+    const unsigned char* s2 = nb > 2 ? stage_wait(c, 2) : s0;
+    const unsigned char* s3 = nb > 3 ? stage_wait(c, 3) : s0;
+    const int n0 = (int)stage_rows_at(c, 0);
+    const int n1 = nb > 1 ? (int)stage_rows_at(c, 1) : 0;
+    const int n2 = nb > 2 ? (int)stage_rows_at(c, 2) : 0;
+    const int n3 = nb > 3 ? (int)stage_rows_at(c, 3) : 0;
+    const int total = n0 + n1 + n2 + n3;
+    for (int r = c.warp; r < total; r += kComputeWarps) {
+      int rr = r;
+      const unsigned char* base = s0;
+      if (rr >= n0) {
+        rr -= n0;
+        base = s1;
+        if (rr >= n1) {
+          rr -= n1;
+          base = s2;
+          if (rr >= n2) {
+            rr -= n2;
+            base = s3;
+          }
+        }
+      }
+      const uint4* row = reinterpret_cast<const uint4*>(base + (size_t)rr * row_bytes);
+      unsigned long long a0 = 0ull, a1 = 0ull;
+      for (int v = c.lane; v < nvec; v += 32) {
+        const uint4 w = row[v];
+        const float4 p = xlo[v], q = xhi[v];
+        a0 = ffma2(bf2(w.x), pack2(__float_as_uint(p.x), __float_as_uint(p.y)), a0);
+        a1 = ffma2(bf2(w.y), pack2(__float_as_uint(p.z), __float_as_uint(p.w)), a1);
+        a0 = ffma2(bf2(w.z), pack2(__float_as_uint(q.x), __float_as_uint(q.y)), a0);
+        a1 = ffma2(bf2(w.w), pack2(__float_as_uint(q.z), __float_as_uint(q.w)), a1);
+      }
+      const float acc = warp_sum(sum2(a0) + sum2(a1));
+      if (c.lane == 0) res[rbase + r] = acc * scale;
+    }
+    stages_release(c, (unsigned)nb);
+    rbase += total;
+  }
+  compute_sync();
+}
+__device__ __forceinline__ void gemv(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
+  if (t.gpr == 0) gemv_rows(c, t, in, x, res, scale);
+  else gemv_xreg(c, t, in, x, res, scale);
+}
+__device__ __forceinline__ float res_row(const float* res, int i, int gpr) {
+  if (gpr <= 1) return res[i];
   float v = 0.f;
-  for (int s = 0; s < wpr; ++s) v += res[i * wpr + s];
+  for (int s = 0; s < gpr; ++s) v += res[i * gpr + s];
   return v;
 }
 
-// ------------------------------------------------------------------ task bodies
-__device__ void task_qkv(Ctx& c, const Task& t, float* sv, float* res) {
-  const KernelParams& P = *c.P;
-  const int l = t.layer;
-  const int qd = P.nq * P.d, kvd = P.nkv * P.d;
-  float bias[4] = {0.f, 0.f, 0.f, 0.f};
-  if (P.qkv_bias) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = c.ctid + k * kCT;
-      if (i < (int)t.nrows) {
-        const int o = (int)t.row0 + i;
-        const uint16_t* b = o < qd ? P.layers[l].w[LW_BQ] + o
-                                   : (o < qd + kvd ? P.layers[l].w[LW_BK] + (o - qd) : P.layers[l].w[LW_BV] + (o - qd - kvd));
-        bias[k] = bf16_to_f32(*b);
-      }
-    }
-  }
-  const float r = fetch_normed(c, x_in_words(P, l), P.layers[l].w[LW_ATTN_NORM], sv);
-  trace_mark(c, 1);
-  gemv(c, t, P.H, sv, res, r);
-  unsigned long long* out = layer_words(P, l) + P.act.qkv;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = c.ctid + k * kCT;
-    if (i < (int)t.nrows) put_word(c, out + t.row0 + i, res_row(res, i, (int)t.wpr) + bias[k]);
-  }
-}
-
+// ------------------------------------------------------------------ attention task
 // One KV head, one context split.  Cached positions [a, min(a + split_len, pos)) arrive through the
 // ring (all of the task's stages are held at once); the owner split (the one holding `pos`) also
 // takes the current row from the QKV words, rotates and rounds it, appends it to the cache, and
 // attends to it.  Writes per query head o (normalised over this split), m and l.
 // Query heads sharing the KV head are packed into the task, so each K/V row is read once (README,
 // "Current status", decode attention).
-__device__ void task_attn(Ctx& c, const Task& t, float* sv) {
+__device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
   const KernelParams& P = *c.P;
   const int l = t.layer, kvh = (int)t.row0, sp = (int)t.nrows;
   const int d = P.d, g = P.g, R = P.rows_per_stage, half = d / 2;
-  const int pos = c.S.pos;
+  const int pos = c.pos;
   const int a = sp * P.split_len;
   if (a > pos) return;  // inactive split (the producer streamed nothing for it either)
   const int b = min(a + P.split_len, pos);
@@ -358,47 +517,36 @@ __device__ void task_attn(Ctx& c, const Task& t, float* sv) {
 
   float* sq = sv;                 // [g][d]     rotated queries
   float* ss = sq + O;             // [g][SL]    scores, then probabilities
-  float* part = ss + g * SL;      // [max(kCT, O)] partial outputs
-  float* kc = part + max(kCT, O); // [d]        current K (rotated, bf16-rounded)
+  float* part = ss + g * SL;          // [max(2 kCT, O)] partial outputs
+  float* kc = part + max(2 * kCT, O); // [d]        current K (rotated, bf16-rounded)
   float* vc = kc + d;             // [d]        current V (bf16-rounded)
   float* sm = vc + d;             // [g]        max
   float* sl = sm + g;             // [g]        sum
-
-  // token-independent loads first: this position's cos/sin
-  float2 cs_q[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
-  const float2* cs = P.rope + (size_t)pos * half;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int e = c.ctid + k * kCT;
-    if (e < g * half) cs_q[k] = cs[e % half];
-  }
-  const float2 cs_k = c.ctid < half ? cs[c.ctid] : make_float2(1.f, 0.f);
+  const float2* cs = c.ctl->rope;  // this step's cos/sin (loaded at kernel start)
 
   const unsigned long long* w = layer_words(P, l) + P.act.qkv;
   const int qd = P.nq * d, kvd = P.nkv * d;
-  poll_words(c, w + (size_t)kvh * O, O, 0x200000u, [&](int i, float x) { sq[i] = x; });
+  poll_words(c, w + (size_t)kvh * O, O, 0x200000u, [&](int i, int, float x) { sq[i] = x; });
   if (owner) {
-    poll_words(c, w + qd + kvh * d, d, 0x210000u, [&](int i, float x) { kc[i] = x; });
-    poll_words(c, w + qd + kvd + kvh * d, d, 0x220000u, [&](int i, float x) { vc[i] = x; });
+    poll_words(c, w + qd + kvh * d, d, 0x210000u, [&](int i, int, float x) { kc[i] = x; });
+    poll_words(c, w + qd + kvd + kvh * d, d, 0x220000u, [&](int i, int, float x) { vc[i] = x; });
   }
   compute_sync();
   trace_mark(c, 1);
   // RoPE (rotate-half pairs (i, i + d/2)); the current K/V row is rounded to bf16 and appended.
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int e = c.ctid + k * kCT;
-    if (e < g * half) {
-      const int h = e / half, i = e % half;
-      const float x0 = sq[h * d + i], x1 = sq[h * d + i + half];
-      sq[h * d + i] = x0 * cs_q[k].x - x1 * cs_q[k].y;
-      sq[h * d + i + half] = x1 * cs_q[k].x + x0 * cs_q[k].y;
-    }
+  for (int e = c.ctid; e < g * half; e += kCT) {
+    const int h = e / half, i = e - h * half;
+    const float2 r = cs[i];
+    const float x0 = sq[h * d + i], x1 = sq[h * d + i + half];
+    sq[h * d + i] = x0 * r.x - x1 * r.y;
+    sq[h * d + i + half] = x1 * r.x + x0 * r.y;
   }
   if (owner && c.ctid < half) {
     const int i = c.ctid;
+    const float2 r = cs[i];
     const float x0 = kc[i], x1 = kc[i + half];
-    const __nv_bfloat16 k0 = __float2bfloat16_rn(x0 * cs_k.x - x1 * cs_k.y);
-    const __nv_bfloat16 k1 = __float2bfloat16_rn(x1 * cs_k.x + x0 * cs_k.y);
+    const __nv_bfloat16 k0 = __float2bfloat16_rn(x0 * r.x - x1 * r.y);
+    const __nv_bfloat16 k1 = __float2bfloat16_rn(x1 * r.x + x0 * r.y);
     const __nv_bfloat16 v0 = __float2bfloat16_rn(vc[i]);
     const __nv_bfloat16 v1 = __float2bfloat16_rn(vc[i + half]);
     kc[i] = __bfloat162float(k0);
@@ -418,12 +566,13 @@ __device__ void task_attn(Ctx& c, const Task& t, float* sv) {
 
   // the task's cached K/V: stage st holds positions a + st*R .. (K rows, then V rows); R is a power
   // of two and the stages are consecutive ring slots, so no division is needed in the loops below
-  const unsigned ns = (unsigned)P.num_stages;
-  for (int st = 0; st < nst; ++st) stage_wait(c, c.it + st);
+  unsigned s_first = 0, ph_unused = 0;
+  slot_after(c, 0, s_first, ph_unused);
+  for (int st = 0; st < nst; ++st) stage_wait(c, (unsigned)st);
   const int rshift = 31 - __clz(R);
-  const unsigned s0 = c.it % ns;
+  const unsigned ns = c.ns;
   auto kstage = [&](int j) -> const uint16_t* {
-    unsigned s = s0 + (unsigned)(j >> rshift);
+    unsigned s = s_first + (unsigned)(j >> rshift);
     s = s >= ns ? s - ns : s;
     return reinterpret_cast<const uint16_t*>(c.ring + (size_t)s * kStageBytes) + (size_t)(j & (R - 1)) * d;
   };
@@ -449,6 +598,9 @@ __device__ void task_attn(Ctx& c, const Task& t, float* sv) {
           kf[e + 5] = bf16_hi(kw.z);
           kf[e + 6] = bf16_lo(kw.w);
           kf[e + 7] = bf16_hi(kw.w);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) kf[e + q] = 0.f;
         }
       }
     } else {
@@ -494,31 +646,48 @@ __device__ void task_attn(Ctx& c, const Task& t, float* sv) {
     }
   }
   compute_sync();
-  // o = sum_j p_j V_j.  With O <= 512 outputs, the threads form kCT / O groups that split the
-  // positions (one output per thread); otherwise each thread owns outputs o, o + 512, ...
-  const int ngroups = O <= kCT ? kCT / O : 1;
-  auto vsum = [&](int o, int grp) {
-    const int h = o / d, tt = o % d;
+  // o = sum_j p_j V_j, two adjacent outputs per thread (one bf16 pair of V per position).  With
+  // O/2 <= 512 output pairs, the threads form kCT / (O/2) groups that split the positions.
+  const int O2 = O >> 1;
+  const int ngroups = O2 <= kCT ? kCT / O2 : 1;
+  auto vsum = [&](int o2, int grp) {
+    const int o = o2 * 2, h = o / d, tt = o - h * d;
     const float* pr = ss + h * SL;
-    float a0 = 0.f, a1 = 0.f;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
     int j = grp;
     for (; j + ngroups < nh; j += 2 * ngroups) {
-      a0 = fmaf(pr[j], bf16_to_f32(kstage(j)[(size_t)R * d + tt]), a0);
-      a1 = fmaf(pr[j + ngroups], bf16_to_f32(kstage(j + ngroups)[(size_t)R * d + tt]), a1);
+      const uint32_t v0 = *reinterpret_cast<const uint32_t*>(kstage(j) + (size_t)R * d + tt);
+      const uint32_t v1 = *reinterpret_cast<const uint32_t*>(kstage(j + ngroups) + (size_t)R * d + tt);
+      const float p0 = pr[j], p1 = pr[j + ngroups];
+      a0 = fmaf(p0, bf16_lo(v0), a0);
+      a1 = fmaf(p0, bf16_hi(v0), a1);
+      b0 = fmaf(p1, bf16_lo(v1), b0);
+      b1 = fmaf(p1, bf16_hi(v1), b1);
     }
-    for (; j < np; j += ngroups) a0 = fmaf(pr[j], j < nh ? bf16_to_f32(kstage(j)[(size_t)R * d + tt]) : vc[tt], a0);
-    part[grp * O + o] = a0 + a1;
+    for (; j < np; j += ngroups) {
+      const float p0 = pr[j];
+      if (j < nh) {
+        const uint32_t v0 = *reinterpret_cast<const uint32_t*>(kstage(j) + (size_t)R * d + tt);
+        a0 = fmaf(p0, bf16_lo(v0), a0);
+        a1 = fmaf(p0, bf16_hi(v0), a1);
+      } else {
+        a0 = fmaf(p0, vc[tt], a0);
+        a1 = fmaf(p0, vc[tt + 1], a1);
+      }
+    }
+    part[grp * O + o] = a0 + b0;
+    part[grp * O + o + 1] = a1 + b1;
   };
-  if (O <= kCT) {
-    if (c.ctid / O < ngroups) vsum(c.ctid % O, c.ctid / O);
+  if (O2 <= kCT) {
+    if (c.ctid / O2 < ngroups) vsum(c.ctid % O2, c.ctid / O2);
   } else {
-    for (int o = c.ctid; o < O; o += kCT) vsum(o, 0);
+    for (int o2 = c.ctid; o2 < O2; o2 += kCT) vsum(o2, 0);
   }
   stages_release(c, (unsigned)nst);
   compute_sync();
   unsigned long long* out = layer_words(P, l) + P.act.att + (size_t)(kvh * P.nsplit + sp) * g * (d + 2);
   for (int e = c.ctid; e < g * (d + 2); e += kCT) {
-    const int h = e / (d + 2), tt = e % (d + 2);
+    const int h = e / (d + 2), tt = e - h * (d + 2);
     float v;
     if (tt < d) {
       float acc = 0.f;
@@ -533,10 +702,10 @@ __device__ void task_attn(Ctx& c, const Task& t, float* sv) {
 
 // Attention output of every query head into o[nq*d], combining the active context splits of each
 // KV head by their log-sum-exp weights (split-context "flash decoding", README "Current status").
-__device__ void fetch_attention(Ctx& c, int l, float* o) {
+__device__ __forceinline__ void fetch_attention(Ctx& c, int l, float* o) {
   const KernelParams& P = *c.P;
   const int d = P.d, g = P.g;
-  const int nact = c.S.pos / P.split_len + 1;
+  const int nact = c.pos / P.split_len + 1;
   const unsigned long long* base = layer_words(P, l) + P.act.att;
   const int blk = g * (d + 2);  // words per (KV head, split)
   if (nact == 1) {
@@ -547,20 +716,20 @@ __device__ void fetch_attention(Ctx& c, int l, float* o) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int e = c.ctid + (e0 + k) * kCT;
-        const int h = e / d, tt = e % d;
+        const int h = e / d, tt = e - h * d;
         ptr[k] = base + (size_t)(h / g) * P.nsplit * blk + (h % g) * (d + 2) + tt;
         w[k] = e < P.nq * d ? ld_word(ptr[k]) : 0ull;
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int e = c.ctid + (e0 + k) * kCT;
-        if (e < P.nq * d) o[e] = word_value(c, w[k], ptr[k], 0x300000u | e);
+        if (e < P.nq * d) o[xpos(e, P.nq * d)] = word_value(c, w[k], ptr[k], 0x300000u | e);
       }
     }
     return;
   }
   for (int e = c.ctid; e < P.nq * d; e += kCT) {
-    const int h = e / d, tt = e % d, kvh = h / g, hh = h % g;
+    const int h = e / d, tt = e - h * d, kvh = h / g, hh = h - kvh * g;
     float M = -INFINITY;
     for (int s = 0; s < nact; ++s) {
       const unsigned long long* p = base + (size_t)(kvh * P.nsplit + s) * blk + hh * (d + 2) + d;
@@ -575,91 +744,32 @@ __device__ void fetch_attention(Ctx& c, int l, float* o) {
       num = fmaf(wgt, word_value(c, ld_word(bp + tt), bp + tt, 0x340000u | s), num);
       den += wgt;
     }
-    o[e] = num / den;
+    o[xpos(e, P.nq * d)] = num / den;
   }
-}
-
-// Residual rows [row0, row0 + n) of a word vector (or the embedding row) into resid.
-__device__ void fetch_rows(Ctx& c, const unsigned long long* src, int row0, int n, float* resid) {
-  if (src == nullptr) {
-    const uint16_t* e = c.P->embed + (size_t)c.S.token * c.P->H + row0;
-    for (int i = c.ctid; i < n; i += kCT) resid[i] = bf16_to_f32(e[i]);
-  } else {
-    poll_words(c, src + row0, n, 0x400000u, [&](int i, float x) { resid[i] = x; });
-  }
-}
-
-__device__ void task_oproj(Ctx& c, const Task& t, float* sv, float* res, float* resid) {
-  const KernelParams& P = *c.P;
-  const int l = t.layer;
-  fetch_attention(c, l, sv);
-  fetch_rows(c, x_in_words(P, l), (int)t.row0, (int)t.nrows, resid);
-  compute_sync();
-  trace_mark(c, 1);
-  gemv(c, t, P.nq * P.d, sv, res, 1.0f);
-  unsigned long long* out = layer_words(P, l) + P.act.xa;
-  for (int i = c.ctid; i < (int)t.nrows; i += kCT) put_word(c, out + t.row0 + i, resid[i] + res_row(res, i, (int)t.wpr));
-}
-
-__device__ void task_gateup(Ctx& c, const Task& t, float* sv, float* res) {
-  const KernelParams& P = *c.P;
-  const int l = t.layer;
-  const float r = fetch_normed(c, layer_words(P, l) + P.act.xa, P.layers[l].w[LW_MLP_NORM], sv);
-  trace_mark(c, 1);
-  gemv(c, t, P.H, sv, res, r);
-  unsigned long long* out = layer_words(P, l) + P.act.hh;
-  const int n = (int)t.nrows;
-  for (int i = c.ctid; i < n; i += kCT) {
-    const float gt = res_row(res, i, (int)t.wpr), up = res_row(res, n + i, (int)t.wpr);
-    const float silu = gt / (1.0f + expf(-gt));
-    put_word(c, out + t.row0 + i, silu * up);
-  }
-}
-
-__device__ void task_down(Ctx& c, const Task& t, float* sv, float* res, float* resid) {
-  const KernelParams& P = *c.P;
-  const int l = t.layer;
-  poll_words(c, layer_words(P, l) + P.act.hh, P.I, 0x500000u, [&](int i, float x) { sv[i] = x; });
-  fetch_rows(c, layer_words(P, l) + P.act.xa, (int)t.row0, (int)t.nrows, resid);
-  compute_sync();
-  trace_mark(c, 1);
-  gemv(c, t, P.I, sv, res, 1.0f);
-  unsigned long long* out = layer_words(P, l) + P.act.xm;
-  for (int i = c.ctid; i < (int)t.nrows; i += kCT) put_word(c, out + t.row0 + i, resid[i] + res_row(res, i, (int)t.wpr));
-}
-
-__device__ void task_lmhead(Ctx& c, const Task& t, float* sv, float* res) {
-  const KernelParams& P = *c.P;
-  const float r = fetch_normed(c, layer_words(P, P.L - 1) + P.act.xm, P.final_norm, sv);
-  trace_mark(c, 1);
-  gemv(c, t, P.H, sv, res, r);
-  if (!aborted(c))
-    for (int i = c.ctid; i < (int)t.nrows; i += kCT) c.S.logits[t.row0 + i] = res_row(res, i, (int)t.wpr);
 }
 
 // ------------------------------------------------------------------ producer warp
 // Walks the CTA's chunk list (32 descriptors per coalesced load, the next batch loaded while the
 // current one is issued) and fills the ring.  Lane 0 issues; the other lanes only help load.
-__device__ void produce(const KernelParams& P, const StepParams& S, Ctl* ctl, unsigned char* ring, uint32_t c0,
-                        uint32_t c1, int lane) {
+__device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl, unsigned char* ring, uint32_t c0,
+                                        uint32_t c1, int lane) {
   const uint64_t policy = evict_first_policy();
   const unsigned ns = (unsigned)P.num_stages;
-  unsigned it = 0;
+  unsigned stage = 0, uses = 0;  // ring slot and how many times the ring has wrapped
   bool quit = false;
   // lane 0: wait for a free stage, record its rows, arm its barrier; returns null if consumers stall
   auto acquire = [&](unsigned bytes, uint32_t rows) -> unsigned char* {
-    const unsigned s = it % ns, k = it / ns;
-    if (k > 0) {
-      const unsigned ph = (k - 1) & 1u;
-      if (!mbar_test(&ctl->empty[s], ph)) {
-        unsigned long long tstart = global_ns();
-        while (!mbar_test(&ctl->empty[s], ph)) {
+    if (uses > 0) {
+      const unsigned ph = (uses - 1) & 1u;
+      if (!mbar_test(&ctl->empty[stage], ph)) {
+        const unsigned long long tstart = global_ns();
+        while (!mbar_test(&ctl->empty[stage], ph)) {
           // Consumers keep taking stages even after a failed activation wait (they stop waiting
           // for activations instead), so this only expires if a consumer is wedged: stop streaming.
           if (global_ns() - tstart > 4 * P.timeout_ns) {
             if (atomicCAS(&P.status[0], 0u, (unsigned)DS_TIMEOUT) == 0u) {
               P.status[1] = blockIdx.x;
-              P.status[3] = 0xE000u | s;
+              P.status[3] = 0xE000u | stage;
             }
             *(volatile unsigned*)&ctl->prod_quit = 1u;
             return nullptr;
@@ -667,9 +777,15 @@ __device__ void produce(const KernelParams& P, const StepParams& S, Ctl* ctl, un
         }
       }
     }
-    ctl->stage_rows[s] = rows;
-    mbar_expect_tx(&ctl->full[s], bytes);
-    return ring + (size_t)s * kStageBytes;
+    ctl->stage_rows[stage] = rows;
+    mbar_expect_tx(&ctl->full[stage], bytes);
+    return ring + (size_t)stage * kStageBytes;
+  };
+  auto advance = [&]() {
+    if (++stage == ns) {
+      stage = 0;
+      ++uses;
+    }
   };
   Chunk next{};
   if (c0 + lane < c1) next = P.chunks[c0 + lane];
@@ -687,8 +803,8 @@ __device__ void produce(const KernelParams& P, const StepParams& S, Ctl* ctl, un
         if (rows == kAttnChunk) {
           const int layer = (int)(src >> 48), kvh = (int)((src >> 32) & 0xFFFF), sp = (int)(unsigned)src;
           const int a = sp * P.split_len;
-          if (a <= S.pos) {
-            const int b = min(a + P.split_len, S.pos);
+          if (a <= pos) {
+            const int b = min(a + P.split_len, pos);
             const size_t head_off = (((size_t)layer * 2) * P.nkv + kvh) * P.C * P.d;
             const uint16_t* K = P.kv + head_off;
             const uint16_t* V = P.kv + head_off + (size_t)P.nkv * P.C * P.d;
@@ -700,10 +816,9 @@ __device__ void produce(const KernelParams& P, const StepParams& S, Ctl* ctl, un
                 q = 1;
                 break;
               }
-              const unsigned s = it % ns;
-              bulk_load(dst, K + (size_t)jj * P.d, nb, &ctl->full[s], policy);
-              bulk_load(dst + (size_t)P.rows_per_stage * P.d * 2, V + (size_t)jj * P.d, nb, &ctl->full[s], policy);
-              ++it;
+              bulk_load(dst, K + (size_t)jj * P.d, nb, &ctl->full[stage], policy);
+              bulk_load(dst + (size_t)P.rows_per_stage * P.d * 2, V + (size_t)jj * P.d, nb, &ctl->full[stage], policy);
+              advance();
             }
           }
         } else {
@@ -711,8 +826,8 @@ __device__ void produce(const KernelParams& P, const StepParams& S, Ctl* ctl, un
           if (!dst) {
             q = 1;
           } else {
-            bulk_load(dst, reinterpret_cast<const void*>(src), bytes, &ctl->full[it % ns], policy);
-            ++it;
+            bulk_load(dst, reinterpret_cast<const void*>(src), bytes, &ctl->full[stage], policy);
+            advance();
           }
         }
       }
@@ -735,47 +850,147 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // token-independent tables: this step's RoPE row, the norm-gain and bias pointers
+  for (int i = threadIdx.x; i < P.d / 2; i += blockDim.x) ctl->rope[i] = P.rope[(size_t)S.pos * (P.d / 2) + i];
+  for (int i = threadIdx.x; i < P.L; i += blockDim.x) {
+    ctl->gain[2 * i] = P.layers[i].w[LW_ATTN_NORM];
+    ctl->gain[2 * i + 1] = P.layers[i].w[LW_MLP_NORM];
+    ctl->bias[3 * i] = P.layers[i].w[LW_BQ];
+    ctl->bias[3 * i + 1] = P.layers[i].w[LW_BK];
+    ctl->bias[3 * i + 2] = P.layers[i].w[LW_BV];
+  }
+  if (threadIdx.x == 0) ctl->gain[2 * P.L] = P.final_norm;
+  {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&P);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&ctl->params);
+    for (int i = threadIdx.x; i < (int)(sizeof(KernelParams) / 4); i += blockDim.x) dst[i] = src[i];
+  }
   __syncthreads();
   if (ctl->skip) return;
   unsigned char* ring = smem + P.off_ring;
   const int warp = threadIdx.x / 32;
   if (warp == 0) {
-    produce(P, S, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31);
+    produce(ctl->params, S.pos, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31);
     return;
   }
   const uint32_t t0 = P.task_off[blockIdx.x], t1 = P.task_off[blockIdx.x + 1];
   Ctx c;
-  c.P = &P;
-  c.S = S;
+  c.P = &ctl->params;
   c.ctl = ctl;
   c.ring = ring;
-  c.it = 0;
+  c.logits = S.logits;
+  c.tag = S.tag;
+  c.pos = S.pos;
+  c.token = S.token;
+  c.ns = (unsigned)P.num_stages;
+  c.stage = 0;
+  c.phase = 0;
   c.ctid = threadIdx.x - 32;
   c.warp = warp - 1;
   c.lane = threadIdx.x & 31;
   float* sv = reinterpret_cast<float*>(smem + P.off_sv);
   float* res = reinterpret_cast<float*>(smem + P.off_res);
   float* resid = reinterpret_cast<float*>(smem + P.off_resid);
-  Task next{};
-  if (t0 < t1) next = P.tasks[t0];
+  // two-deep descriptor pipeline; the gains of the next task load while the current one runs
+  Task cur{}, nxt{};
+  if (t0 < t1) cur = P.tasks[t0];
+  if (t0 + 1 < t1) nxt = P.tasks[t0 + 1];
+  float gcur[4], gnext[4];
+  load_gains(c, cur, gcur);
   for (uint32_t ti = t0; ti < t1; ++ti) {
-    const Task t = next;
-    if (ti + 1 < t1) next = P.tasks[ti + 1];  // the next descriptor loads while this task runs
+    const Task t = cur;
+    cur = nxt;
+    if (ti + 2 < t1) nxt = P.tasks[ti + 2];
+    if (ti + 1 < t1) load_gains(c, cur, gnext);
     c.task_index = ti;
     c.first_stage = true;
     if (P.trace != nullptr && c.ctid == 0) P.trace[(size_t)ti * 4 + 3] = 0;
     trace_mark(c, 0);
-    switch (t.type) {
-      case T_QKV: task_qkv(c, t, sv, res); break;
-      case T_ATTN: task_attn(c, t, sv); break;
-      case T_OPROJ: task_oproj(c, t, sv, res, resid); break;
-      case T_GATEUP: task_gateup(c, t, sv, res); break;
-      case T_DOWN: task_down(c, t, sv, res, resid); break;
-      case T_LMHEAD: task_lmhead(c, t, sv, res); break;
-      default: break;
+    if (t.type == T_ATTN) {
+      task_attn(c, t, sv);
+    } else {
+      // 1. inputs: one fetch path for every projection type
+      const int l = t.layer;
+      int in = P.H;
+      float ss = 0.f;
+      float bias[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t.type == T_QKV && P.qkv_bias) {
+        const int qd = P.nq * P.d, kvd = P.nkv * P.d;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = c.ctid + k * kCT;
+          if (i < (int)t.nrows) {
+            const int o = (int)t.row0 + i;
+            const uint16_t* b = o < qd ? ctl->bias[3 * l] + o
+                                       : (o < qd + kvd ? ctl->bias[3 * l + 1] + (o - qd) : ctl->bias[3 * l + 2] + (o - qd - kvd));
+            bias[k] = bf16_to_f32(*b);
+          }
+        }
+      }
+      if (t.type == T_OPROJ) {
+        in = P.nq * P.d;
+        fetch_attention(c, l, sv);
+      } else {
+        const unsigned long long* src;
+        if (t.type == T_QKV) src = x_in_words(P, l);
+        else if (t.type == T_GATEUP) src = layer_words(P, l) + P.act.xa;
+        else if (t.type == T_DOWN) src = layer_words(P, l) + P.act.hh;
+        else src = layer_words(P, P.L - 1) + P.act.xm;  // LM head
+        if (t.type == T_DOWN) in = P.I;
+        fetch_input(c, src, in, t.type == T_DOWN ? nullptr : gcur, sv, &ss);
+      }
+      if (t.type == T_OPROJ || t.type == T_DOWN) {
+        const unsigned long long* rsrc = t.type == T_OPROJ ? x_in_words(P, l) : layer_words(P, l) + P.act.xa;
+        if (rsrc == nullptr) {
+          const uint16_t* e = P.embed + (size_t)c.token * P.H + t.row0;
+          for (int i = c.ctid; i < (int)t.nrows; i += kCT) resid[i] = bf16_to_f32(e[i]);
+        } else {
+          poll_words(c, rsrc + t.row0, (int)t.nrows, 0x400000u, [&](int i, int, float x) { resid[i] = x; });
+        }
+      }
+      const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
+      if (norm) {
+        ss = warp_sum(ss);
+        if (c.lane == 0) ctl->red[c.warp] = ss;
+      }
+      compute_sync();
+      float scale = 1.f;
+      if (norm) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) tot += ctl->red[w];
+        scale = 1.0f / sqrtf(tot / (float)P.H + P.eps);
+      }
+      trace_mark(c, 1);
+      // 2. the projection
+      gemv(c, t, in, sv, res, scale);
+      // 3. epilogue
+      const int gpr = (int)t.gpr, n = (int)t.nrows;
+      if (t.type == T_QKV) {
+        unsigned long long* out = layer_words(P, l) + P.act.qkv + t.row0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = c.ctid + k * kCT;
+          if (i < n) put_word(c, out + i, res_row(res, i, gpr) + bias[k]);
+        }
+      } else if (t.type == T_GATEUP) {
+        unsigned long long* out = layer_words(P, l) + P.act.hh + t.row0;
+        for (int i = c.ctid; i < n; i += kCT) {
+          const float gt = res_row(res, i, gpr), up = res_row(res, n + i, gpr);
+          put_word(c, out + i, gt / (1.0f + expf(-gt)) * up);
+        }
+      } else if (t.type == T_LMHEAD) {
+        if (!aborted(c))
+          for (int i = c.ctid; i < n; i += kCT) c.logits[t.row0 + i] = res_row(res, i, gpr);
+      } else {
+        unsigned long long* out = layer_words(P, l) + (t.type == T_OPROJ ? P.act.xa : P.act.xm) + t.row0;
+        for (int i = c.ctid; i < n; i += kCT) put_word(c, out + i, resid[i] + res_row(res, i, gpr));
+      }
     }
     compute_sync();  // the next task reuses the shared vectors
     trace_mark(c, 2);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) gcur[k] = gnext[k];
   }
 }
 

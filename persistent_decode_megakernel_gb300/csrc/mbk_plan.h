@@ -32,8 +32,10 @@ struct Task {
   uint32_t nrows;
   uint32_t chunk0;
   uint32_t nchunks;
-  uint32_t wpr;     // GEMV: compute warps per weight row (a power of two; the row's K range is split)
-  uint32_t pad[2];
+  uint32_t gpr;     // GEMV: 0 = one warp per row (small tasks); else warps sharing one weight row
+                    // (a power of two; each keeps its K slice of the input in registers)
+  uint32_t lpr;     // GEMV: lanes per warp working on a row (always 32)
+  uint32_t pad;
 };
 static_assert(sizeof(Task) == 32, "Task layout");
 
@@ -68,6 +70,10 @@ constexpr int kAttnSplitMax = 512;     // context positions per attention split 
 constexpr int kAttnSplitStages = 8;    // ring stages per attention split
 constexpr int kMaxRingStages = 32;
 constexpr int kMaxTaskChunks = 256;
+constexpr int kGemvBatch = 4;          // ring stages a GEMV consumes together
+constexpr int kGemvXVec = 4;           // 16-byte input vectors a GEMV lane keeps in registers
+constexpr int kCtlBytes = 4096;        // shared-memory control block (barriers, flags, tables)
+constexpr int kMaxLayers = 64;
 
 struct PlanShape {
   int L, H, I, nq, nkv, d, V, C;

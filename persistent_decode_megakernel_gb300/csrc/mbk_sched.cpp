@@ -36,15 +36,41 @@ void add_chunks(std::vector<Chunk>& out, const Seg& sg) {
   }
 }
 
-// Warps per weight row for a GEMV task: as many as leave every compute warp busy on the task's
-// largest chunk, while rows x warps-per-row fits the partial-result slots.
-uint32_t warps_per_row(const std::vector<Chunk>& chunks, const Task& t, int res_per_row) {
+// GEMV layout of a task: t.gpr warps split each weight row's K range (a warp keeps its slice of
+// the input in registers, at most 32 * kGemvXVec vectors), and each warp works on two rows at a
+// time.  Among the feasible splits, the largest one that keeps every lane on at least one vector
+// and no more warps than the task's largest kGemvBatch-chunk batch can use, within the
+// partial-result slots.
+uint32_t pow2_floor(uint32_t v) {
+  uint32_t p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+uint32_t pow2_ceil(uint32_t v) {
+  uint32_t p = 1;
+  while (p < v) p *= 2;
+  return p;
+}
+void gemv_layout(const std::vector<Chunk>& chunks, Task& t, int in, int res_per_row) {
+  const uint32_t nvec = (uint32_t)in / 8;
+  t.lpr = 32;
   uint32_t max_rows = 1;
-  for (uint32_t k = t.chunk0; k < t.chunk0 + t.nchunks; ++k) max_rows = std::max(max_rows, chunks[k].rows);
-  uint32_t wpr = 1;
-  while (wpr * 2 * max_rows <= (uint32_t)kComputeWarps) wpr *= 2;
-  while (wpr > 1 && (uint64_t)t.nrows * res_per_row * wpr > (uint64_t)kResSlots) wpr /= 2;
-  return wpr;
+  for (uint32_t k = 0; k < t.nchunks; k += kGemvBatch) {
+    uint32_t rows = 0;
+    for (uint32_t j = k; j < std::min<uint32_t>(t.nchunks, k + kGemvBatch); ++j) rows += chunks[t.chunk0 + j].rows;
+    max_rows = std::max(max_rows, rows);
+  }
+  if (max_rows <= (uint32_t)kComputeWarps) {  // small task: one warp per row, x from shared memory
+    t.gpr = 0;
+    return;
+  }
+  const uint32_t need = pow2_ceil((nvec + 32 * kGemvXVec - 1) / (32 * kGemvXVec));  // registers bound
+  const uint32_t lanes = pow2_floor(std::max(1u, nvec / 32));                          // a vector per lane
+  const uint32_t work = pow2_floor(std::max(1u, (uint32_t)kComputeWarps / ((max_rows + 1) / 2)));
+  uint32_t gpr = std::max(need, std::min(lanes, work));
+  gpr = std::min<uint32_t>(gpr, kComputeWarps);
+  while (gpr > need && (uint64_t)t.nrows * res_per_row * gpr > (uint64_t)kResSlots) gpr /= 2;
+  t.gpr = gpr;
 }
 
 }  // namespace
@@ -62,7 +88,7 @@ std::string validate_shape(const PlanShape& s) {
     return buf;
   }
   if (s.H > kMaxTaskRows) return "hidden larger than the per-task result capacity";
-  if (s.L > 65535) return "too many layers";
+  if (s.L > kMaxLayers) return "more layers than the kernel's pointer tables hold";
   return "";
 }
 
@@ -123,18 +149,18 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
 
   // shared memory layout: [barriers + flags 1 KB][input vector][results][residuals][ring]
   const int O = g * s.d;
-  int attn_floats = O + g * (p.split_len + 1) + std::max(kComputeWarps * 32, O) + 2 * s.d + 2 * g + 8;
+  int attn_floats = O + g * (p.split_len + 1) + std::max(2 * kComputeWarps * 32, O) + 2 * s.d + 2 * g + 8;
   p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
   p.sv_floats = (p.sv_floats + 31) / 32 * 32;
-  p.off_sv = 1024;
+  p.off_sv = kCtlBytes;
   p.off_res = p.off_sv + (uint32_t)p.sv_floats * 4;
   p.off_resid = p.off_res + kResSlots * 4;
   p.off_ring = (p.off_resid + kMaxTaskRows * 4 + 127) / 128 * 128;
   int avail = opt.smem_limit - (int)p.off_ring;
   p.num_stages = std::min(kMaxRingStages, avail / kStageBytes);
   if (p.num_stages < 2) return "not enough shared memory for the weight ring";
-  if (p.num_stages < (p.split_len + p.attn_rows_per_stage - 1) / p.attn_rows_per_stage + 1)
-    return "weight ring too small to hold one attention split";
+  if (p.num_stages < (p.split_len + p.attn_rows_per_stage - 1) / p.attn_rows_per_stage + 1 || p.num_stages < kGemvBatch)
+    return "weight ring too small to hold one attention split or one GEMV batch";
   p.smem_bytes = (int)p.off_ring + p.num_stages * kStageBytes;
 
   // tasks
@@ -165,7 +191,7 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       for (const Seg& sg : segs_for(r0, r1)) add_chunks(cta_chunks[cta], sg);
       t.nchunks = (uint32_t)(cta_chunks[cta].size() - t.chunk0);
       for (uint32_t c = t.chunk0; c < t.chunk0 + t.nchunks; ++c) cta_bytes[cta] += cta_chunks[cta][c].bytes;
-      t.wpr = warps_per_row(cta_chunks[cta], t, res_per_row);
+      gemv_layout(cta_chunks[cta], t, row_bytes / 2, res_per_row);
       cta_tasks[cta].push_back(t);
     }
   };
@@ -232,7 +258,7 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       add_chunks(cta_chunks[cta], Seg{w.embed, hb, r0, r1 - r0});
       t.nchunks = (uint32_t)(cta_chunks[cta].size() - t.chunk0);
       for (uint32_t c = t.chunk0; c < t.chunk0 + t.nchunks; ++c) cta_bytes[cta] += cta_chunks[cta][c].bytes;
-      t.wpr = warps_per_row(cta_chunks[cta], t, 1);
+      gemv_layout(cta_chunks[cta], t, s.H, 1);
       cta_tasks[cta].push_back(t);
     }
   }
@@ -322,8 +348,13 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
       }
       int res = t.type == T_GATEUP ? 2 * (int)t.nrows : (int)t.nrows;
       if (res > kMaxTaskRows || t.nrows == 0) return "task result slots exceeded";
-      if (t.wpr == 0 || t.wpr > (uint32_t)kComputeWarps || (t.wpr & (t.wpr - 1)) || (uint64_t)res * t.wpr > (uint64_t)kResSlots)
-        return "bad warps-per-row";
+      {
+        const int in = t.type == T_OPROJ ? qd : (t.type == T_DOWN ? s.I : s.H);
+        const uint32_t nvec = (uint32_t)in / 8;
+        if (t.gpr != 0 && ((t.gpr & (t.gpr - 1)) || t.gpr > (uint32_t)kComputeWarps ||
+                           (uint64_t)res * t.gpr > (uint64_t)kResSlots || (nvec + t.gpr - 1) / t.gpr > 32u * kGemvXVec))
+          return "bad GEMV layout";
+      }
       int rows_seen = 0;
       for (uint32_t k = t.chunk0; k < t.chunk0 + t.nchunks; ++k) {
         if (k >= p.chunks.size()) return "chunk index out of range";

@@ -15,7 +15,7 @@ import threading
 from typing import Optional
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmbk.so")
+LIB_PATH = os.environ.get("MBK_LIBRARY") or os.path.join(_PKG, "libmbk.so")
 
 MBK_OK = 0
 MBK_ERR_INVALID_ARG = -1
