@@ -127,6 +127,33 @@ const char *mbk_error_string(int code);
  * NULL is ignored. */
 void mbk_destroy(mbk_handle *h);
 
+/* ---- decoding without device allocation ----
+ * (Not a counterpart of anything in the MegaBake pages: it exists for callers of this library.)
+ *
+ * mbk_decode_step_static is one decode step, computed exactly like mbk_decode_step, for callers
+ * that cannot allocate device memory when they decode: code running under a caller-owned memory
+ * pool or budget that forbids new device allocations, or inside a runtime whose allocator must not
+ * be re-entered.  It calls no cudaMalloc, cudaFree or other allocating routine and needs no handle.
+ * Everything the library keeps for a step (static schedule, activation exchange words, RoPE table,
+ * status word) lives in one device array of MBK_STATIC_SCRATCH_BYTES that is part of the library:
+ * every GPU that loads the library holds it until the process exits.
+ *  - The caller passes the config, the weights, the KV cache, the token, the position and the
+ *    DEVICE logits buffer, as for mbk_create + mbk_decode_step; the current device is used.
+ *  - The first call on a device looks up the array's device address (and sets the kernel's shared
+ *    memory limit) with that device current; make that first call before any stream capture.
+ *  - All calls on a device share the array, which keeps the last call's contents: the schedule is
+ *    rebuilt and uploaded (then the stream is synchronised once) only when the config or any
+ *    pointer differs from the previous call; the exchange words and the status word are cleared
+ *    on every call.  Calls whose GPU work overlaps (two streams, two threads) race on the array:
+ *    order them on one stream.
+ *  - Returns MBK_ERR_INVALID_ARG for the same argument errors as mbk_create / mbk_decode_step and
+ *    when the shape needs more than MBK_STATIC_SCRATCH_BYTES (nothing is launched then);
+ *    MBK_ERR_UNSUPPORTED or MBK_ERR_CUDA as mbk_create.  A device-side wait that times out is not
+ *    reported by this entry point (the launch still ends; its logits are then invalid). */
+#define MBK_STATIC_SCRATCH_BYTES (16u << 20)
+int mbk_decode_step_static(const mbk_config *cfg, const mbk_weights *weights, void *kv_cache, int32_t token_id,
+                           int32_t position, float *logits_out, void *stream);
+
 /* ---- diagnostics (for tests and profiling; not needed to decode) ---- */
 
 /* Residual stream of the most recently COMPLETED step (synchronise its stream first), copied to the

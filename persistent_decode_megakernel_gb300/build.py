@@ -20,7 +20,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmbk.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
-CU_SOURCES = ["mbk_kernel.cu", "mbk_api.cu"]
+CU_SOURCES = ["mbk_kernel.cu", "mbk_api.cu", "mbk_static.cu"]
 CPP_SOURCES = ["mbk_sched.cpp"]
 HEADERS = ["mbk_plan.h", "mbk_device.h", "mbk_sched.h"]
 

@@ -15,7 +15,7 @@ import threading
 from typing import Optional
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.environ.get("MBK_LIBRARY") or os.path.join(_PKG, "libmbk.so")
+LIB_PATH = os.path.join(_PKG, "libmbk.so")
 
 MBK_OK = 0
 MBK_ERR_INVALID_ARG = -1
@@ -27,7 +27,7 @@ MBK_ERR_STATE = -6
 
 EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
-            "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject")
+            "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -106,6 +106,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_trace_read.restype = ctypes.c_int64
         lib.mbk_debug_inject.argtypes = [vp, vp]
         lib.mbk_debug_inject.restype = ctypes.c_int
+        lib.mbk_decode_step_static.argtypes = [ctypes.POINTER(MbkConfig), ctypes.POINTER(MbkWeights), vp, i32, i32, vp, vp]
+        lib.mbk_decode_step_static.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -161,6 +163,14 @@ def mbk_get_status(h) -> int:
 def mbk_destroy(h) -> None:
     if h:
         load_library().mbk_destroy(h)
+
+
+def mbk_decode_step_static(cfg: MbkConfig, weights: MbkWeights, kv_cache_ptr: int, token_id: int, position: int,
+                           logits_ptr: int, stream_ptr: int) -> int:
+    """One decode step that allocates no device memory (see include/mbk.h); returns the C code."""
+    return load_library().mbk_decode_step_static(ctypes.byref(cfg), ctypes.byref(weights), ctypes.c_void_p(kv_cache_ptr),
+                                                 int(token_id), int(position), ctypes.c_void_p(logits_ptr),
+                                                 ctypes.c_void_p(stream_ptr))
 
 
 def mbk_debug_taps(h, n_layers: int, hidden: int):
