@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -247,14 +248,7 @@ def run_ours(args, shape_name):
         ctps, cn, cores = time_oracle(wl, budget, s.steps)
         cpu = {"value": round(ctps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{cn} teacher-forced decode steps of the same workload (time-bounded to {budget:.0f} s)"}
-    traffic = None
-    tp = os.path.join(_ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        with open(tp) as f:
-            tr = json.load(f)
-        ent = tr.get(shape_name)
-        if ent and ent.get("kernel_source_hash") == _kernel_hash():
-            traffic = ent["dram_bytes_per_launch"]
+    traffic = profiled_traffic(shape_name)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s", "n_gpus": world, "steps": steps,
@@ -281,6 +275,21 @@ def run_ours(args, shape_name):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def profiled_traffic(shape_name: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload, or None when the
+    summary is missing or was taken on different kernel sources."""
+    tp = os.path.join(_ROOT, "profiles", f"decode_kernel_{shape_name.replace('-', '').replace('.', '')}.md")
+    if not os.path.exists(tp):
+        return None
+    with open(tp) as f:
+        text = f.read()
+    mh = re.search(r"kernel_source_hash: `([0-9a-f]+)`", text)
+    mb = re.search(r"dram_bytes_per_launch: (\d+)", text)
+    if not mh or not mb or mh.group(1) != _kernel_hash():
+        return None
+    return int(mb.group(1))
 
 
 def _kernel_hash() -> str:
