@@ -280,6 +280,7 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   kp.off_sv = p.off_sv;
   kp.off_res = p.off_res;
   kp.off_resid = p.off_resid;
+  kp.off_tasks = p.off_tasks;
   kp.off_ring = p.off_ring;
   kp.embed = reinterpret_cast<const uint16_t*>(weights->embed);
   kp.final_norm = reinterpret_cast<const uint16_t*>(weights->final_norm);
@@ -435,7 +436,6 @@ int mbk_trace_enable(mbk_handle* h, int enable) {
   } else if (!enable && h->d_trace) {
     cudaDeviceSynchronize();
     cudaFree(h->d_trace);
-  cudaFree(h->d_inject);
     h->d_trace = nullptr;
   }
   h->kp.trace = h->d_trace;

@@ -27,7 +27,7 @@ struct KernelParams {
   const uint32_t* chunk_off;    // [grid + 1]
   ActLayout act;
   int nsplit, split_len, rows_per_stage, num_stages;
-  uint32_t off_sv, off_res, off_resid, off_ring;
+  uint32_t off_sv, off_res, off_resid, off_tasks, off_ring;
   // tensors
   const uint16_t* embed;
   const uint16_t* final_norm;

@@ -2,23 +2,23 @@
 //
 // One cooperative launch per decode step, one CTA per SM (MegaBake article, "What a megakernel is,
 // and why small models want one": resident CTAs working through a task list and synchronising
-// through global memory).  Every CTA runs 17 warps:
+// through global memory).  Every CTA runs 16 warps:
 //   warp 0      streams the weights of its upcoming tasks into a ring of shared-memory stages with
 //               TMA bulk copies (cp.async.bulk + mbarrier transaction counts).  Weights do not depend
 //               on the token, so the stream runs ahead of the data dependencies by up to the ring's
 //               depth -- the "cross-phase prefetch of the next GEMM's weights while a CTA waits" the
 //               article lists as future work ("Checking the 5.5x").
-//   warps 1-16  execute the CTA's tasks in order.  Activations move between CTAs as 64-bit words
+//   warps 1-15  execute the CTA's tasks in order.  Activations move between CTAs as 64-bit words
 //               {tag:32 | fp32 value:32}, each written once per step by exactly one thread; a reader
-//               spins on the word until its tag equals this step's tag.  A value and its readiness
+//               polls the word until its tag equals this step's tag.  A value and its readiness
 //               travel in one single-copy-atomic store, so no fence, counter or grid barrier is
 //               needed (the pages' counting grid barrier is the thing this replaces).
-// Everything a task needs that does not depend on the token (norm gains, biases, RoPE cos/sin,
-// descriptors) is loaded before the task waits for its inputs -- gains one task ahead -- so the
-// critical path of a task is: inputs arrive -> one block barrier -> GEMV on shared-memory weights
-// -> words out.  All task code is inlined into the kernel so its context stays in registers; only
-// the rare slow paths (a word that is not ready yet, a failure) are out of line.
-// Every spin is bounded by a globaltimer budget; on expiry the CTA records timeout status and
+// The step is a long chain of small dependent tasks, so the kernel is built for latency: one code
+// path serves every projection type and one serves attention, keeping the instructions of a task
+// hot in the instruction cache; a projection row's output word is written by the warp that
+// computed it the moment its dot product is done; token-independent loads (norm gains, biases,
+// descriptors) are issued before a task waits for its inputs and consumed after.
+// Every wait is bounded by a globaltimer budget; on expiry the CTA records timeout status and
 // finishes its task list without waiting or writing, so the launch always terminates.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -135,40 +135,6 @@ __device__ __noinline__ void record_failure(unsigned* status, unsigned* host_sta
   *(volatile unsigned*)abort_flag = 1u;
 }
 
-// Keeps polling a word that was not ready at the first load; returns its value (0 on abort).
-__device__ __noinline__ float spin_word(const unsigned long long* p, unsigned tag, unsigned* abort_flag, unsigned* status,
-                                        unsigned* host_status, unsigned long long timeout, unsigned task,
-                                        unsigned detail, unsigned backoff_ns) {
-  if (*(volatile unsigned*)abort_flag) return 0.f;
-  const unsigned long long t0 = global_ns();
-  for (unsigned n = 1;; ++n) {
-    if (backoff_ns) __nanosleep(backoff_ns);
-    const unsigned long long w = ld_word(p);
-    if ((unsigned)(w >> 32) == tag) return __uint_as_float((unsigned)w);
-    if ((n & 63u) == 0u) {
-      if (*(volatile unsigned*)abort_flag) return 0.f;
-      if (*(volatile unsigned*)status != 0u || global_ns() - t0 > timeout) {
-        record_failure(status, host_status, abort_flag, task, detail);
-        return 0.f;
-      }
-    }
-  }
-}
-
-// Waits for a ring stage whose first test failed; records a failure after the timeout.
-__device__ __noinline__ void spin_stage(uint64_t* full, unsigned parity, unsigned* prod_quit, unsigned* status,
-                                        unsigned* host_status, unsigned* abort_flag, unsigned long long timeout,
-                                        unsigned task, unsigned detail) {
-  const unsigned long long t0 = global_ns();
-  while (!mbar_test(full, parity)) {
-    if (*(volatile unsigned*)prod_quit) return;  // nothing more will arrive
-    if (global_ns() - t0 > timeout) {
-      record_failure(status, host_status, abort_flag, task, detail);
-      return;
-    }
-  }
-}
-
 // ------------------------------------------------------------------ per-CTA context (registers)
 struct Ctx {
   const KernelParams* P;
@@ -180,8 +146,8 @@ struct Ctx {
   unsigned ns;          // ring stages
   unsigned stage;       // ring slot of the next stage to consume
   unsigned phase;       // its parity
-  int ctid;             // 0..511 among compute threads
-  int warp, lane;       // compute warp 0..15
+  int ctid;             // 0..kCT-1 among compute threads
+  int warp, lane;       // compute warp 0..kComputeWarps-1
   unsigned task_index;
   bool first_stage;     // tracing: the task has not yet received a weight stage
 };
@@ -190,33 +156,157 @@ __device__ __forceinline__ void trace_mark(Ctx& c, int k) {
   if (c.P->trace != nullptr && c.ctid == 0) c.P->trace[(size_t)c.task_index * 4 + k] = global_ns();
 }
 __device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile unsigned*)&c.ctl->abort != 0u; }
-__device__ __forceinline__ float word_value(Ctx& c, unsigned long long w, const unsigned long long* p, unsigned detail) {
-  if ((unsigned)(w >> 32) == c.tag) return __uint_as_float((unsigned)w);
-  return spin_word(p, c.tag, &c.ctl->abort, c.P->status, c.P->host_status, c.P->timeout_ns, c.task_index, detail,
-                   c.P->poll_backoff_ns);
-}
 __device__ __forceinline__ void put_word(Ctx& c, unsigned long long* p, float v) {
   if (!aborted(c)) st_word(p, c.tag, v);
 }
 
-// Batched polling: this thread's words src[i], i = ctid + k*kCT < n, with up to 4 loads in flight.
-template <typename F>
-__device__ __forceinline__ void poll_words(Ctx& c, const unsigned long long* src, int n, unsigned detail, F&& sink) {
-  for (int k0 = 0; k0 * kCT < n; k0 += 4) {
+// Called every 32 unsuccessful polls with the wait's start time (0 on the first call).  Returns the
+// start time to keep waiting with, or 0 once the wait must end: this CTA aborted, another CTA
+// recorded a failure, or the wait ran past the timeout (which this call then records).  Out of line
+// so that the polling loops stay small; it runs once per 32 polls.
+__device__ __noinline__ unsigned long long wait_check(const KernelParams* P, Ctl* ctl, unsigned long long t0,
+                                                      unsigned task, unsigned detail) {
+  if (*(volatile unsigned*)&ctl->abort) return 0ull;
+  const unsigned long long now = global_ns();
+  if (t0 == 0ull) return now;
+  if (*(volatile unsigned*)P->status != 0u || now - t0 > P->timeout_ns) {
+    record_failure(P->status, P->host_status, &ctl->abort, task, detail);
+    return 0ull;
+  }
+  return t0;
+}
+
+// ------------------------------------------------------------------ activation input of a task
+// A vector a task reads: element e (0 <= e < n) is the word src[e], or -- with src == nullptr --
+// the bf16 value emb[e] (the token's embedding row).  Values land in dst, in the split GEMV layout
+// when xlayout.  With a gain the values stored are x * gain[e] and the sum of squares of x is
+// returned: RMSNorm's 1/sqrt(mean(x^2) + eps) is applied to the GEMV results instead, so the norm
+// costs no pass of its own (the pages' "folding" of small producers into their consumer).
+struct InVec {
+  const unsigned long long* src;
+  const uint16_t* emb;
+  const uint16_t* gain;
+  float* dst;
+  int n, xlayout;
+};
+
+// Every thread polls its elements ctid + k*kCT four at a time; all loads of a group are in flight
+// together and every retry re-loads all words still pending, so a late group costs one round trip
+// per retry, not one per word.  The gains are loaded with the words and used only after the group
+// arrived, so their latency hides behind the wait.  Values are consumed in element order whatever
+// their arrival order, which keeps the sum of squares deterministic.  After a failed wait the
+// remaining words read as 0.
+__device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detail) {
+  float ss = 0.f;
+#pragma unroll 1
+  for (int e0 = c.ctid; e0 < v.n; e0 += 4 * kCT) {
     unsigned long long w[4];
+    uint32_t graw[4];
+    unsigned pend = 0u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int i = c.ctid + (k0 + k) * kCT;
-      w[k] = i < n ? ld_word(src + i) : 0ull;
+      const int e = e0 + k * kCT;
+      w[k] = 0ull;
+      graw[k] = 0x3f80u;  // bf16 1.0
+      if (e < v.n) {
+        if (v.src != nullptr) {
+          w[k] = ld_word(v.src + e);
+          pend |= 1u << k;
+        } else {
+          w[k] = (unsigned long long)((uint32_t)v.emb[e] << 16);
+        }
+        if (v.gain != nullptr) graw[k] = v.gain[e];
+      }
+    }
+    unsigned spins = 0u;
+    unsigned long long t0 = 0ull;
+    while (pend != 0u) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (((pend >> k) & 1u) && (unsigned)(w[k] >> 32) == c.tag) pend &= ~(1u << k);
+      if (pend == 0u) break;
+      if ((++spins & 31u) == 0u && (t0 = wait_check(c.P, c.ctl, t0, c.task_index, detail | (unsigned)e0)) == 0ull) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if ((pend >> k) & 1u) w[k] = 0ull;
+        break;
+      }
+      if (c.P->poll_backoff_ns) __nanosleep(c.P->poll_backoff_ns);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = e0 + k * kCT;
+        if ((pend >> k) & 1u) w[k] = ld_word(v.src + e);
+      }
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int i = c.ctid + (k0 + k) * kCT;
-      if (i < n) sink(i, k0 + k, word_value(c, w[k], src + i, detail | (unsigned)i));
+      const int e = e0 + k * kCT;
+      if (e < v.n) {
+        float x = __uint_as_float((uint32_t)w[k]);
+        if (v.gain != nullptr) {
+          ss = fmaf(x, x, ss);
+          x *= __uint_as_float(graw[k] << 16);
+        }
+        v.dst[v.xlayout ? xpos(e, v.n) : e] = x;
+      }
     }
+  }
+  return ss;
+}
+
+// Polls a set of up to K words of this thread: word k (k < K, valid(k)) at addr(k); sink(k, value)
+// runs once per valid word, k static.  Used by the split combine of long contexts.
+template <int K, typename V, typename A, typename F>
+__device__ __forceinline__ void poll_set(Ctx& c, unsigned detail, V&& valid, A&& addr, F&& sink) {
+  unsigned long long w[K];
+  unsigned pend = 0u;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    w[k] = 0ull;
+    if (valid(k)) {
+      w[k] = ld_word(addr(k));
+      pend |= 1u << k;
+    }
+  }
+  unsigned spins = 0u;
+  unsigned long long t0 = 0ull;
+  for (;;) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if ((pend >> k) & 1u) {
+        if ((unsigned)(w[k] >> 32) == c.tag) {
+          pend &= ~(1u << k);
+          sink(k, __uint_as_float((unsigned)w[k]));
+        }
+      }
+    }
+    if (pend == 0u) return;
+    if ((++spins & 31u) == 0u && (t0 = wait_check(c.P, c.ctl, t0, c.task_index, detail)) == 0ull) {
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        if ((pend >> k) & 1u) sink(k, 0.f);
+      return;
+    }
+    if (c.P->poll_backoff_ns) __nanosleep(c.P->poll_backoff_ns);
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+      if ((pend >> k) & 1u) w[k] = ld_word(addr(k));
   }
 }
 
+// ------------------------------------------------------------------ weight ring (consumer side)
+// Keeps testing a ring stage whose first test failed; records a failure after the timeout.
+__device__ __noinline__ void spin_stage(uint64_t* full, unsigned parity, const KernelParams* P, Ctl* ctl, unsigned task,
+                                        unsigned detail) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_test(full, parity)) {
+    if (*(volatile unsigned*)&ctl->prod_quit) return;  // nothing more will arrive
+    if (global_ns() - t0 > P->timeout_ns) {
+      record_failure(P->status, P->host_status, &ctl->abort, task, detail);
+      return;
+    }
+  }
+}
 // Ring slot `k` stages after the current one (k < ns): its slot index and parity.
 __device__ __forceinline__ void slot_after(const Ctx& c, unsigned k, unsigned& s, unsigned& ph) {
   s = c.stage + k;
@@ -230,9 +320,7 @@ __device__ __forceinline__ void slot_after(const Ctx& c, unsigned k, unsigned& s
 __device__ __forceinline__ unsigned char* stage_wait(Ctx& c, unsigned k) {
   unsigned s, ph;
   slot_after(c, k, s, ph);
-  if (!mbar_test(&c.ctl->full[s], ph))
-    spin_stage(&c.ctl->full[s], ph, &c.ctl->prod_quit, c.P->status, c.P->host_status, &c.ctl->abort, c.P->timeout_ns,
-               c.task_index, 0xF000u | s);
+  if (!mbar_test(&c.ctl->full[s], ph)) spin_stage(&c.ctl->full[s], ph, c.P, c.ctl, c.task_index, 0xF000u | s);
   if (c.first_stage) {
     trace_mark(c, 3);
     c.first_stage = false;
@@ -247,6 +335,7 @@ __device__ __forceinline__ unsigned stage_rows_at(const Ctx& c, unsigned k) {
 // Hand `n` stages back to the producer (every compute warp arrives once per stage).
 __device__ __forceinline__ void stages_release(Ctx& c, unsigned n) {
   __syncwarp();
+#pragma unroll 1
   for (unsigned k = 0; k < n; ++k) {
     if (c.lane == 0) mbar_arrive(&c.ctl->empty[c.stage]);
     if (++c.stage == c.ns) {
@@ -266,64 +355,6 @@ __device__ __forceinline__ const unsigned long long* x_in_words(const KernelPara
   return P.inject != nullptr ? P.inject + (size_t)l * P.H : layer_words(P, l - 1) + P.act.xm;
 }
 
-// Norm gain a task applies to its input (null for tasks without a norm).
-__device__ __forceinline__ const uint16_t* task_gain(const Ctl* ctl, const Task& t, int L) {
-  if (t.type == T_QKV) return ctl->gain[2 * t.layer];
-  if (t.type == T_GATEUP) return ctl->gain[2 * t.layer + 1];
-  if (t.type == T_LMHEAD) return ctl->gain[2 * L];
-  return nullptr;
-}
-// This thread's gain values (elements ctid + k*kCT) of a task, loaded ahead of the task.
-__device__ __forceinline__ void load_gains(const Ctx& c, const Task& t, float g[4]) {
-  const uint16_t* gp = task_gain(c.ctl, t, c.P->L);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = c.ctid + k * kCT;
-    g[k] = (gp != nullptr && i < c.P->H) ? bf16_to_f32(gp[i]) : 0.f;
-  }
-}
-
-// ------------------------------------------------------------------ input vector of a GEMV task
-// Loads n activations (words, or the token's embedding row when src is null) into sv in the split
-// layout.  With a norm (gr != null, n == H), it stores gain * x and leaves this thread's share of
-// sum(x^2) in *ss: RMSNorm's scalar 1/sqrt(mean(x^2)+eps) is applied to the GEMV results instead,
-// so the norm costs no barrier of its own (the pages' "folding" of small producers into their
-// consumer).  No barrier here.
-__device__ __forceinline__ void fetch_input(Ctx& c, const unsigned long long* src, int n, const float* gr, float* sv,
-                                            float* ss) {
-  float acc = 0.f;
-  if (src == nullptr) {
-    const uint16_t* e = c.P->embed + (size_t)c.token * n;
-    for (int k = 0; k * kCT < n; ++k) {
-      const int i = c.ctid + k * kCT;
-      if (i < n) {
-        float x = bf16_to_f32(e[i]);
-        if (gr != nullptr) {
-          acc = fmaf(x, x, acc);
-          x *= gr[k & 3];
-        }
-        sv[xpos(i, n)] = x;
-      }
-    }
-  } else {
-    poll_words(c, src, n, 0x100000u, [&](int i, int k, float x) {
-      if (gr != nullptr) {
-        acc = fmaf(x, x, acc);
-        x *= gr[k & 3];
-      }
-      sv[xpos(i, n)] = x;
-    });
-  }
-  *ss = acc;
-}
-
-// ------------------------------------------------------------------ GEMV on ring stages
-// Dot products of the task's weight rows (in chunk order) with x, consuming up to kGemvBatch ring
-// stages at a time.  Warps split K into t.gpr slices; each warp keeps its slice of x in registers
-// (loaded once) and streams rows past it, so shared-memory traffic is the weight bytes alone.  Two
-// bf16 weights multiply two x values per packed fp32x2 FMA (each an ordinary fp32 FMA).
-// res[row * gpr + slice] = scale * partial; res_row() sums the slices in a fixed order, so results
-// are deterministic.  Ends with a compute barrier.
 __device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
   unsigned long long r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
@@ -343,7 +374,9 @@ __device__ __forceinline__ unsigned long long bf2(uint32_t w) { return pack2(w <
 __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
   const int nvec = in >> 3;  // 16-byte vectors per row
   const int gpr = (int)t.gpr, gshift = 31 - __clz(gpr);
+  // warp = rw * gpr + slice; warps beyond the last whole group (rw >= rpp) take no rows
   const int slice = c.warp & (gpr - 1), rw = c.warp >> gshift, rpp = kComputeWarps >> gshift;
+  const int rstart = rw < rpp ? rw : 1 << 30;
   const int vps = (nvec + gpr - 1) >> gshift;  // vectors per slice
   const int v0 = slice * vps, v1 = min(nvec, v0 + vps);
   // this lane's x: vectors v0 + lane + 32k, as packed pairs
@@ -392,7 +425,7 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
       return reinterpret_cast<const uint4*>(base + (size_t)r * row_bytes);
     };
     // two rows per iteration; the loop bound is uniform across the warp (shuffles below)
-    for (int ra = rw; ra < total; ra += 2 * rpp) {
+    for (int ra = rstart; ra < total; ra += 2 * rpp) {
       const int rb = ra + rpp;
       const bool two = rb < total;
       const uint4* A = row_of(ra);
@@ -430,43 +463,16 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
   }
   compute_sync();
 }
-// Small tasks (at most 16 rows per batch, t.gpr == 0): one warp per row over the full K, x read
-// from shared memory -- the fewest instructions when each warp has a row or two.
-__device__ __forceinline__ void gemv_rows(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
-  const int nvec = in >> 3;
-  const float4* xlo = reinterpret_cast<const float4*>(x);
-  const float4* xhi = reinterpret_cast<const float4*>(x + (in >> 1));
-  const size_t row_bytes = (size_t)in * 2;
-  int rbase = 0;
-  for (uint32_t k0 = 0; k0 < t.nchunks; k0 += kGemvBatch) {
-    const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
-    const unsigned char* s0 = stage_wait(c, 0);
-    const unsigned char* s1 = nb > 1 ? stage_wait(c, 1) : s0;
-    const unsigned char* s2 = nb > 2 ? stage_wait(c, 2) : s0;
-    const unsigned char* s3 = nb > 3 ? stage_wait(c, 3) : s0;
-    const int n0 = (int)stage_rows_at(c, 0);
-    const int n1 = nb > 1 ? (int)stage_rows_at(c, 1) : 0;
-    const int n2 = nb > 2 ? (int)stage_rows_at(c, 2) : 0;
-    const int n3 = nb > 3 ? (int)stage_rows_at(c, 3) : 0;
-    const int total = n0 + n1 + n2 + n3;
-    for (int r = c.warp; r < total; r += kComputeWarps) {
-      int rr = r;
-      const unsigned char* base = s0;
-      if (rr >= n0) {
-        rr -= n0;
-        base = s1;
-        if (rr >= n1) {
-          rr -= n1;
-          base = s2;
-          if (rr >= n2) {
-            rr -= n2;
-            base = s3;
-          }
-        }
-      }
-      const uint4* row = reinterpret_cast<const uint4*>(base + (size_t)rr * row_bytes);
-      unsigned long long a0 = 0ull, a1 = 0ull;
-      for (int v = c.lane; v < nvec; v += 32) {
+
+__device__ __forceinline__ float dot_row(const Ctx& c, const uint4* row, const float4* xlo, const float4* xhi, int nvec) {
+  // eight 16-byte vectors per lane per round, unrolled so their loads are all in flight together
+  unsigned long long a0 = 0ull, a1 = 0ull;
+#pragma unroll 1
+  for (int v0 = c.lane; v0 < nvec; v0 += 256) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int v = v0 + 32 * it;
+      if (v < nvec) {
         const uint4 w = row[v];
         const float4 p = xlo[v], q = xhi[v];
         a0 = ffma2(bf2(w.x), pack2(__float_as_uint(p.x), __float_as_uint(p.y)), a0);
@@ -474,18 +480,46 @@ __device__ __forceinline__ void gemv_rows(Ctx& c, const Task& t, int in, const f
         a0 = ffma2(bf2(w.z), pack2(__float_as_uint(q.x), __float_as_uint(q.y)), a0);
         a1 = ffma2(bf2(w.w), pack2(__float_as_uint(q.z), __float_as_uint(q.w)), a1);
       }
-      const float acc = warp_sum(sum2(a0) + sum2(a1));
-      if (c.lane == 0) res[rbase + r] = acc * scale;
     }
-    stages_release(c, (unsigned)nb);
-    rbase += total;
   }
-  compute_sync();
+  return sum2(a0) + sum2(a1);
 }
-__device__ __forceinline__ void gemv(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
-  if (t.gpr == 0) gemv_rows(c, t, in, x, res, scale);
-  else gemv_xreg(c, t, in, x, res, scale);
+// Rows of the stages of one batch, in chunk order: row r of the batch.
+struct BatchRows {
+  const unsigned char* s[kGemvBatch];
+  int n[kGemvBatch];
+  int total;
+  __device__ __forceinline__ const uint4* row(int r, size_t row_bytes) const {
+    const unsigned char* base = s[0];
+    if (r >= n[0]) {
+      r -= n[0];
+      base = s[1];
+      if (r >= n[1]) {
+        r -= n[1];
+        base = s[2];
+        if (r >= n[2]) {
+          r -= n[2];
+          base = s[3];
+        }
+      }
+    }
+    return reinterpret_cast<const uint4*>(base + (size_t)r * row_bytes);
+  }
+};
+__device__ __forceinline__ BatchRows batch_wait(Ctx& c, int nb) {
+  BatchRows b;
+  b.s[0] = stage_wait(c, 0);
+  b.s[1] = nb > 1 ? stage_wait(c, 1) : b.s[0];
+  b.s[2] = nb > 2 ? stage_wait(c, 2) : b.s[0];
+  b.s[3] = nb > 3 ? stage_wait(c, 3) : b.s[0];
+  b.n[0] = (int)stage_rows_at(c, 0);
+  b.n[1] = nb > 1 ? (int)stage_rows_at(c, 1) : 0;
+  b.n[2] = nb > 2 ? (int)stage_rows_at(c, 2) : 0;
+  b.n[3] = nb > 3 ? (int)stage_rows_at(c, 3) : 0;
+  b.total = b.n[0] + b.n[1] + b.n[2] + b.n[3];
+  return b;
 }
+
 __device__ __forceinline__ float res_row(const float* res, int i, int gpr) {
   if (gpr <= 1) return res[i];
   float v = 0.f;
@@ -494,16 +528,22 @@ __device__ __forceinline__ float res_row(const float* res, int i, int gpr) {
 }
 
 // ------------------------------------------------------------------ attention task
-// One KV head, one context split.  Cached positions [a, min(a + split_len, pos)) arrive through the
-// ring (all of the task's stages are held at once); the owner split (the one holding `pos`) also
-// takes the current row from the QKV words, rotates and rounds it, appends it to the cache, and
-// attends to it.  Writes per query head o (normalised over this split), m and l.
-// Query heads sharing the KV head are packed into the task, so each K/V row is read once (README,
-// "Current status", decode attention).
+// One KV head, one context split: the g query heads sharing the KV head are packed into the task,
+// so each K/V row is read once from HBM (README, "Current status", decode attention).  Cached
+// positions [a, min(a + split_len, pos)) arrive through the ring (all of the task's stages are
+// held at once); the owner split (the one holding `pos`) also takes the current row from the QKV
+// words, rotates and rounds it, appends it to the cache and attends to it.
+// Work items are (32-position block, query head) pairs, spread over the warps; in an item every
+// lane owns one position: it computes that position's score alone (no cross-lane reduction), the
+// warp takes the block's max and sum, and the lanes then accumulate the block's output with each
+// lane owning output elements.  One barrier later the blocks of each head are merged by their
+// log-sum-exp weights.  Writes per query head o (normalised over this split) and (m, l); scores
+// are kept in base-2 units (scaled by log2 e), so m is too.
 __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
   const KernelParams& P = *c.P;
   const int l = t.layer, kvh = (int)t.row0, sp = (int)t.nrows;
   const int d = P.d, g = P.g, R = P.rows_per_stage, half = d / 2;
+  const int dshift = 31 - __clz(d), hshift = dshift - 1;
   const int pos = c.pos;
   const int a = sp * P.split_len;
   if (a > pos) return;  // inactive split (the producer streamed nothing for it either)
@@ -512,47 +552,57 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
   const int nh = b - a;                       // cached positions
   const int np = nh + (owner ? 1 : 0);        // positions attended
   const int nst = (nh + R - 1) / R;           // ring stages of this task
-  const int SL = P.split_len + 1;             // score row stride
-  const int O = g * d;                        // outputs of the task
+  const int O = g * d;
+  const int nblk = (np + 31) >> 5;            // 32-position blocks
+  const int items = nblk * g;
 
-  float* sq = sv;                 // [g][d]     rotated queries
-  float* ss = sq + O;             // [g][SL]    scores, then probabilities
-  float* part = ss + g * SL;          // [max(2 kCT, O)] partial outputs
-  float* kc = part + max(2 * kCT, O); // [d]        current K (rotated, bf16-rounded)
-  float* vc = kc + d;             // [d]        current V (bf16-rounded)
-  float* sm = vc + d;             // [g]        max
-  float* sl = sm + g;             // [g]        sum
-  const float2* cs = c.ctl->rope;  // this step's cos/sin (loaded at kernel start)
+  float* sq = sv;                             // [g][d]  queries (rotated in place)
+  float* kc = sq + O;                         // [d]     current K (raw)
+  float* vc = kc + d;                         // [d]     current V (raw)
+  uint16_t* cur = reinterpret_cast<uint16_t*>(vc + d);  // [2][d] bf16: the rotated K, V row appended
+  float* pw = vc + 2 * d;                     // [items][d + 2]  per-item o, m, l
+  const float2* cs = c.ctl->rope;             // this step's cos/sin (loaded at kernel start)
 
-  const unsigned long long* w = layer_words(P, l) + P.act.qkv;
-  const int qd = P.nq * d, kvd = P.nkv * d;
-  poll_words(c, w + (size_t)kvh * O, O, 0x200000u, [&](int i, int, float x) { sq[i] = x; });
-  if (owner) {
-    poll_words(c, w + qd + kvh * d, d, 0x210000u, [&](int i, int, float x) { kc[i] = x; });
-    poll_words(c, w + qd + kvd + kvh * d, d, 0x220000u, [&](int i, int, float x) { vc[i] = x; });
+  // 1. the packed queries and (owner) the current K/V row
+  {
+    const unsigned long long* w = layer_words(P, l) + P.act.qkv;
+    const int qd = P.nq * d, kvd = P.nkv * d;
+#pragma unroll 1
+    for (int j = 0; j < (owner ? 3 : 1); ++j) {
+      InVec v;
+      v.src = j == 0 ? w + (size_t)kvh * O : (j == 1 ? w + qd + kvh * d : w + qd + kvd + kvh * d);
+      v.emb = nullptr;
+      v.gain = nullptr;
+      v.dst = j == 0 ? sq : (j == 1 ? kc : vc);
+      v.n = j == 0 ? O : d;
+      v.xlayout = 0;
+      poll_vec(c, v, 0x200000u | ((unsigned)j << 16));
+    }
   }
   compute_sync();
   trace_mark(c, 1);
-  // RoPE (rotate-half pairs (i, i + d/2)); the current K/V row is rounded to bf16 and appended.
+  // RoPE (rotate-half pairs (i, i + d/2)); the current K/V row is rounded to bf16 and appended
+#pragma unroll 1
   for (int e = c.ctid; e < g * half; e += kCT) {
-    const int h = e / half, i = e - h * half;
+    const int h = e >> hshift, i = e & (half - 1);
     const float2 r = cs[i];
-    const float x0 = sq[h * d + i], x1 = sq[h * d + i + half];
-    sq[h * d + i] = x0 * r.x - x1 * r.y;
-    sq[h * d + i + half] = x1 * r.x + x0 * r.y;
+    float* q = sq + (h << dshift);
+    const float x0 = q[i], x1 = q[i + half];
+    q[i] = x0 * r.x - x1 * r.y;
+    q[i + half] = x1 * r.x + x0 * r.y;
   }
-  if (owner && c.ctid < half) {
-    const int i = c.ctid;
+  if (owner && c.ctid >= kCT - half) {
+    const int i = c.ctid - (kCT - half);
     const float2 r = cs[i];
     const float x0 = kc[i], x1 = kc[i + half];
     const __nv_bfloat16 k0 = __float2bfloat16_rn(x0 * r.x - x1 * r.y);
     const __nv_bfloat16 k1 = __float2bfloat16_rn(x1 * r.x + x0 * r.y);
     const __nv_bfloat16 v0 = __float2bfloat16_rn(vc[i]);
     const __nv_bfloat16 v1 = __float2bfloat16_rn(vc[i + half]);
-    kc[i] = __bfloat162float(k0);
-    kc[i + half] = __bfloat162float(k1);
-    vc[i] = __bfloat162float(v0);
-    vc[i + half] = __bfloat162float(v1);
+    cur[i] = __bfloat16_as_ushort(k0);
+    cur[i + half] = __bfloat16_as_ushort(k1);
+    cur[d + i] = __bfloat16_as_ushort(v0);
+    cur[d + i + half] = __bfloat16_as_ushort(v1);
     if (!aborted(c)) {
       __nv_bfloat16* Kc = reinterpret_cast<__nv_bfloat16*>(P.kv) + ((((size_t)l * 2 + 0) * P.nkv + kvh) * P.C + pos) * d;
       __nv_bfloat16* Vc = reinterpret_cast<__nv_bfloat16*>(P.kv) + ((((size_t)l * 2 + 1) * P.nkv + kvh) * P.C + pos) * d;
@@ -562,189 +612,309 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
       Vc[i + half] = v1;
     }
   }
-  compute_sync();
-
-  // the task's cached K/V: stage st holds positions a + st*R .. (K rows, then V rows); R is a power
-  // of two and the stages are consecutive ring slots, so no division is needed in the loops below
+  // the task's K/V rows: stage st holds positions a + st*R .. (K rows, then V rows); R is a power of
+  // two and the stages are consecutive ring slots, so no division is needed; position nh (owner)
+  // is the row just appended
   unsigned s_first = 0, ph_unused = 0;
   slot_after(c, 0, s_first, ph_unused);
+#pragma unroll 1
   for (int st = 0; st < nst; ++st) stage_wait(c, (unsigned)st);
+  compute_sync();
   const int rshift = 31 - __clz(R);
   const unsigned ns = c.ns;
-  auto kstage = [&](int j) -> const uint16_t* {
+  auto krow = [&](int j) -> const uint16_t* {
+    if (j >= nh) return cur;
     unsigned s = s_first + (unsigned)(j >> rshift);
     s = s >= ns ? s - ns : s;
-    return reinterpret_cast<const uint16_t*>(c.ring + (size_t)s * kStageBytes) + (size_t)(j & (R - 1)) * d;
+    return reinterpret_cast<const uint16_t*>(c.ring + (size_t)s * kStageBytes) + ((size_t)(j & (R - 1)) << dshift);
   };
+  auto vrow = [&](int j) -> const uint16_t* { return krow(j) + (j >= nh ? d : R * d); };
 
-  // scores: 8 lanes per position; the K row is loaded once and dotted with every packed query head
-  const float scale = P.attn_scale;
-  const int elems = d / 8;  // 8 or 16 per lane
-  for (int jb = c.warp * 4; jb < np; jb += kComputeWarps * 4) {
-    const int j = jb + c.lane / 8, sub = c.lane % 8;
+  // 2. work items: (block, head) -> per-item o (unnormalised), m, l
+  const float scale = P.attn_scale * 1.4426950408889634f;
+  const int nchunk = d >> 3;  // 16-byte K chunks per row
+#pragma unroll 1
+  for (int it = c.warp; it < items; it += kComputeWarps) {
+    const int blk = it / g, h = it - blk * g;
+    const int j = (blk << 5) + c.lane;
     const bool valid = j < np;
-    float kf[16];
-    if (valid && j < nh) {
-      const uint16_t* kr = kstage(j) + sub * elems;
-#pragma unroll
-      for (int e = 0; e < 16; e += 8) {
-        if (e < elems) {
-          const uint4 kw = *reinterpret_cast<const uint4*>(kr + e);
-          kf[e + 0] = bf16_lo(kw.x);
-          kf[e + 1] = bf16_hi(kw.x);
-          kf[e + 2] = bf16_lo(kw.y);
-          kf[e + 3] = bf16_hi(kw.y);
-          kf[e + 4] = bf16_lo(kw.z);
-          kf[e + 5] = bf16_hi(kw.z);
-          kf[e + 6] = bf16_lo(kw.w);
-          kf[e + 7] = bf16_hi(kw.w);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) kf[e + q] = 0.f;
-        }
+    // this lane's score: the full dot product of its K row with the query, chunk order rotated
+    // by lane so that the 32 rows are read without bank conflicts
+    float s = -INFINITY;
+    if (valid) {
+      const uint4* kr = reinterpret_cast<const uint4*>(krow(j));
+      const float4* qh = reinterpret_cast<const float4*>(sq + (h << dshift));
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < nchunk; ++k) {
+        const int cch = (k + c.lane) & (nchunk - 1);
+        const uint4 kw = kr[cch];
+        const float4 q0 = qh[2 * cch], q1 = qh[2 * cch + 1];
+        s0 = fmaf(bf16_lo(kw.x), q0.x, s0);
+        s1 = fmaf(bf16_hi(kw.x), q0.y, s1);
+        s2 = fmaf(bf16_lo(kw.y), q0.z, s2);
+        s3 = fmaf(bf16_hi(kw.y), q0.w, s3);
+        s0 = fmaf(bf16_lo(kw.z), q1.x, s0);
+        s1 = fmaf(bf16_hi(kw.z), q1.y, s1);
+        s2 = fmaf(bf16_lo(kw.w), q1.z, s2);
+        s3 = fmaf(bf16_hi(kw.w), q1.w, s3);
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) kf[e] = (valid && e < elems) ? kc[sub * elems + e] : 0.f;
+      s = ((s0 + s1) + (s2 + s3)) * scale;
     }
-    for (int h = 0; h < g; ++h) {
-      const float* qr = sq + h * d + sub * elems;
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; e += 4) {
-        if (e < elems) {
-          const float4 q = *reinterpret_cast<const float4*>(qr + e);
-          acc = fmaf(kf[e + 0], q.x, acc);
-          acc = fmaf(kf[e + 1], q.y, acc);
-          acc = fmaf(kf[e + 2], q.z, acc);
-          acc = fmaf(kf[e + 3], q.w, acc);
-        }
+    const float m = warp_max(s);
+    const float p = valid ? exp2f(s - m) : 0.f;
+    const float lsum = warp_sum(p);
+    // the block's output: lane owns element pairs 2*lane (+64); position jj's weight comes from lane jj
+    const int nj = min(32, np - (blk << 5));
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+    for (int jj = 0; jj < nj; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);
+      const uint16_t* vr = vrow((blk << 5) + jj);
+      const uint32_t v01 = *reinterpret_cast<const uint32_t*>(vr + 2 * c.lane);
+      a0 = fmaf(pj, bf16_lo(v01), a0);
+      a1 = fmaf(pj, bf16_hi(v01), a1);
+      if (d > 64) {
+        const uint32_t v23 = *reinterpret_cast<const uint32_t*>(vr + 64 + 2 * c.lane);
+        a2 = fmaf(pj, bf16_lo(v23), a2);
+        a3 = fmaf(pj, bf16_hi(v23), a3);
       }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      if (valid && sub == 0) ss[h * SL + j] = acc * scale;
     }
-  }
-  compute_sync();
-  // softmax over this split: warp h handles head h
-  if (c.warp < g) {
-    const int h = c.warp;
-    float mx = -INFINITY;
-    for (int j = c.lane; j < np; j += 32) mx = fmaxf(mx, ss[h * SL + j]);
-    mx = warp_max(mx);
-    float psum = 0.f;
-    for (int j = c.lane; j < np; j += 32) {
-      const float p = expf(ss[h * SL + j] - mx);
-      ss[h * SL + j] = p;
-      psum += p;
+    float* pi = pw + it * (d + 2);
+    pi[2 * c.lane] = a0;
+    pi[2 * c.lane + 1] = a1;
+    if (d > 64) {
+      pi[64 + 2 * c.lane] = a2;
+      pi[64 + 2 * c.lane + 1] = a3;
     }
-    psum = warp_sum(psum);
     if (c.lane == 0) {
-      sm[h] = mx;
-      sl[h] = psum;
+      pi[d] = m;
+      pi[d + 1] = lsum;
     }
-  }
-  compute_sync();
-  // o = sum_j p_j V_j, two adjacent outputs per thread (one bf16 pair of V per position).  With
-  // O/2 <= 512 output pairs, the threads form kCT / (O/2) groups that split the positions.
-  const int O2 = O >> 1;
-  const int ngroups = O2 <= kCT ? kCT / O2 : 1;
-  auto vsum = [&](int o2, int grp) {
-    const int o = o2 * 2, h = o / d, tt = o - h * d;
-    const float* pr = ss + h * SL;
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-    int j = grp;
-    for (; j + ngroups < nh; j += 2 * ngroups) {
-      const uint32_t v0 = *reinterpret_cast<const uint32_t*>(kstage(j) + (size_t)R * d + tt);
-      const uint32_t v1 = *reinterpret_cast<const uint32_t*>(kstage(j + ngroups) + (size_t)R * d + tt);
-      const float p0 = pr[j], p1 = pr[j + ngroups];
-      a0 = fmaf(p0, bf16_lo(v0), a0);
-      a1 = fmaf(p0, bf16_hi(v0), a1);
-      b0 = fmaf(p1, bf16_lo(v1), b0);
-      b1 = fmaf(p1, bf16_hi(v1), b1);
-    }
-    for (; j < np; j += ngroups) {
-      const float p0 = pr[j];
-      if (j < nh) {
-        const uint32_t v0 = *reinterpret_cast<const uint32_t*>(kstage(j) + (size_t)R * d + tt);
-        a0 = fmaf(p0, bf16_lo(v0), a0);
-        a1 = fmaf(p0, bf16_hi(v0), a1);
-      } else {
-        a0 = fmaf(p0, vc[tt], a0);
-        a1 = fmaf(p0, vc[tt + 1], a1);
-      }
-    }
-    part[grp * O + o] = a0 + b0;
-    part[grp * O + o + 1] = a1 + b1;
-  };
-  if (O2 <= kCT) {
-    if (c.ctid / O2 < ngroups) vsum(c.ctid % O2, c.ctid / O2);
-  } else {
-    for (int o2 = c.ctid; o2 < O2; o2 += kCT) vsum(o2, 0);
   }
   stages_release(c, (unsigned)nst);
   compute_sync();
-  unsigned long long* out = layer_words(P, l) + P.act.att + (size_t)(kvh * P.nsplit + sp) * g * (d + 2);
-  for (int e = c.ctid; e < g * (d + 2); e += kCT) {
-    const int h = e / (d + 2), tt = e - h * (d + 2);
-    float v;
-    if (tt < d) {
-      float acc = 0.f;
-      for (int q = 0; q < ngroups; ++q) acc += part[q * O + h * d + tt];
-      v = acc / sl[h];
-    } else {
-      v = tt == d ? sm[h] : sl[h];
+
+  // 3. merge the blocks of each head: o = sum_b o_b 2^(m_b - M) / sum_b l_b 2^(m_b - M)
+  const int hq0 = kvh * g;  // first query head of the task
+  unsigned long long* out_o = layer_words(P, l) + P.act.att + ((size_t)sp * P.nq + hq0) * d;
+  unsigned long long* out_ml = layer_words(P, l) + P.act.att + (size_t)P.nsplit * P.nq * d + ((size_t)sp * P.nq + hq0) * 2;
+  const int istride = g * (d + 2);  // items of one head are g apart
+#pragma unroll 1
+  for (int e = c.ctid; e < O; e += kCT) {
+    const int h = e >> dshift, tt = e & (d - 1);
+    const float* ph = pw + h * (d + 2);
+    float M = -INFINITY;
+    for (int q = 0; q < nblk; ++q) M = fmaxf(M, ph[q * istride + d]);
+    float num = 0.f, den = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < nblk; ++q) {
+      const float f = exp2f(ph[q * istride + d] - M);
+      num = fmaf(ph[q * istride + tt], f, num);
+      den = fmaf(ph[q * istride + d + 1], f, den);
     }
-    put_word(c, out + e, v);
+    st_word(out_o + e, c.tag, num / den);
+    if (tt == 0) {
+      st_word(out_ml + 2 * h, c.tag, M);
+      st_word(out_ml + 2 * h + 1, c.tag, den);
+    }
   }
 }
 
-// Attention output of every query head into o[nq*d], combining the active context splits of each
-// KV head by their log-sum-exp weights (split-context "flash decoding", README "Current status").
-__device__ __forceinline__ void fetch_attention(Ctx& c, int l, float* o) {
+// Attention output of every query head into o[nq*d] (split GEMV layout) when the context has
+// several splits: the active splits of each head are combined by their log-sum-exp weights
+// (split-context "flash decoding", README "Current status").  `ml` is scratch for
+// splits * nq * 2 floats.  Contains one block barrier; none after the last step.
+__device__ __forceinline__ void combine_splits(Ctx& c, int l, float* o, float* ml) {
   const KernelParams& P = *c.P;
-  const int d = P.d, g = P.g;
+  const int d = P.d, nqd = P.nq * d, dshift = 31 - __clz(d);
   const int nact = c.pos / P.split_len + 1;
-  const unsigned long long* base = layer_words(P, l) + P.act.att;
-  const int blk = g * (d + 2);  // words per (KV head, split)
-  if (nact == 1) {
-    // one split: o is the split's normalised output
-    for (int e0 = 0; e0 * kCT < P.nq * d; e0 += 4) {
-      unsigned long long w[4];
-      const unsigned long long* ptr[4];
+  const unsigned long long* ob = layer_words(P, l) + P.act.att;  // o words [split][head][d]
+  // (m, l) of every active split and head: a prefix of the [split][head][2] words
+  {
+    InVec v;
+    v.src = ob + (size_t)P.nsplit * nqd;
+    v.emb = nullptr;
+    v.gain = nullptr;
+    v.dst = ml;
+    v.n = nact * P.nq * 2;
+    v.xlayout = 0;
+    poll_vec(c, v, 0x310000u);
+  }
+  compute_sync();
+  // each output: the weighted mean of the splits' normalised outputs, weights l_s 2^(m_s - max m),
+  // summed in split order
+#pragma unroll 1
+  for (int e = c.ctid; e < nqd; e += kCT) {
+    const int h = e >> dshift;
+    float M = -INFINITY;
+    for (int s = 0; s < nact; ++s) M = fmaxf(M, ml[(s * P.nq + h) * 2]);
+    float num = 0.f, den = 0.f;
+#pragma unroll 1
+    for (int s0 = 0; s0 < nact; s0 += 4) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      poll_set<4>(
+          c, 0x340000u | (unsigned)s0, [&](int k) { return s0 + k < nact; },
+          [&](int k) { return ob + (size_t)(s0 + k) * nqd + e; }, [&](int k, float x) { v[k] = x; });
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int e = c.ctid + (e0 + k) * kCT;
-        const int h = e / d, tt = e - h * d;
-        ptr[k] = base + (size_t)(h / g) * P.nsplit * blk + (h % g) * (d + 2) + tt;
-        w[k] = e < P.nq * d ? ld_word(ptr[k]) : 0ull;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int e = c.ctid + (e0 + k) * kCT;
-        if (e < P.nq * d) o[xpos(e, P.nq * d)] = word_value(c, w[k], ptr[k], 0x300000u | e);
+        if (s0 + k < nact) {
+          const float* m = ml + ((s0 + k) * P.nq + h) * 2;
+          const float wgt = m[1] * exp2f(m[0] - M);
+          num = fmaf(wgt, v[k], num);
+          den += wgt;
+        }
       }
     }
+    o[xpos(e, nqd)] = num / den;
+  }
+}
+
+// One output row of a projection, written by lane 0 of the warp that computed it (or by the
+// thread that summed its slices): QKV adds the q/k/v bias and O/down add the residual (both staged
+// in `add`), gate/up writes silu(gate) * up, the LM head writes a logit.  Words are written even
+// after a failed wait (the step is reported failed; consumers then finish instead of waiting).
+__device__ __forceinline__ void emit_row(Ctx& c, int type, unsigned long long* out, int r, float a, float u,
+                                         const float* add, float* logits) {
+  if (type == T_LMHEAD) {
+    if (!aborted(c)) logits[r] = a;
     return;
   }
-  for (int e = c.ctid; e < P.nq * d; e += kCT) {
-    const int h = e / d, tt = e - h * d, kvh = h / g, hh = h - kvh * g;
-    float M = -INFINITY;
-    for (int s = 0; s < nact; ++s) {
-      const unsigned long long* p = base + (size_t)(kvh * P.nsplit + s) * blk + hh * (d + 2) + d;
-      M = fmaxf(M, word_value(c, ld_word(p), p, 0x310000u | s));
+  const float v = type == T_GATEUP ? a / (1.0f + __expf(-a)) * u : add[r] + a;
+  st_word(out + r, c.tag, v);
+}
+
+// A projection task (QKV, O, gate/up, down, LM head): one code path for every type.  The critical
+// path after the inputs arrive is one block barrier, the row's dot products and the output store:
+// weight stages are checked before the inputs are polled, and the norm scale (a reduction of the
+// per-warp sums of squares) is computed by every warp alongside its dot products.
+__device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, float* res, float* add) {
+  const KernelParams& P = *c.P;
+  const int l = t.layer, type = t.type, n = (int)t.nrows;
+  // 1. what the task reads and writes (word offsets and flags set by the scheduler)
+  const unsigned f = t.flags;
+  const uint16_t* emb_row = P.embed + (size_t)c.token * P.H;
+  const unsigned long long* layer_in = P.inject != nullptr ? P.inject + (size_t)l * P.H : nullptr;
+  InVec x, r;
+  x.src = (f & TF_IN_EMB) ? nullptr : ((f & TF_IN_LAYER) && layer_in ? layer_in : P.words + t.in_off);
+  x.emb = emb_row;
+  x.gain = (f & TF_NORM) ? c.ctl->gain[t.gain] : nullptr;
+  x.dst = sv;
+  x.n = (int)t.in_n;
+  x.xlayout = 1;
+  r.src = (f & TF_RES_EMB) ? nullptr : ((f & TF_RES_LAYER) && layer_in ? layer_in + t.row0 : P.words + t.res_off);
+  r.emb = emb_row + t.row0;
+  r.gain = nullptr;
+  r.dst = add;
+  r.n = (f & TF_RES) ? n : 0;
+  r.xlayout = 0;
+  unsigned long long* out = P.words + t.out_off;
+  const int in = (int)t.in_n;
+  const bool combine = (f & TF_COMBINE) != 0;  // O projection over several context splits
+  // the q/k/v bias of the task's rows: loads issued before the inputs are polled
+  uint32_t braw[kVecPerThread];
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) braw[k] = 0u;
+  if (f & TF_BIAS) {
+    const int qd = P.nq * P.d, kvd = P.nkv * P.d;
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+      const int i = c.ctid + k * kCT;
+      if (i < n) {
+        const int o = (int)t.row0 + i;
+        const uint16_t* b = o < qd ? c.ctl->bias[3 * l] + o
+                                   : (o < qd + kvd ? c.ctl->bias[3 * l + 1] + (o - qd) : c.ctl->bias[3 * l + 2] + (o - qd - kvd));
+        braw[k] = *b;
+      }
     }
-    float num = 0.f, den = 0.f;
-    for (int s = 0; s < nact; ++s) {
-      const unsigned long long* bp = base + (size_t)(kvh * P.nsplit + s) * blk + hh * (d + 2);
-      const float m = word_value(c, ld_word(bp + d), bp + d, 0x320000u | s);
-      const float lsum = word_value(c, ld_word(bp + d + 1), bp + d + 1, 0x330000u | s);
-      const float wgt = lsum * expf(m - M);
-      num = fmaf(wgt, word_value(c, ld_word(bp + tt), bp + tt, 0x340000u | s), num);
-      den += wgt;
+  }
+  // a single-batch task's weights (almost always in shared memory by now) are checked first
+  const bool direct = t.gpr == 0;
+  const bool one_batch = direct && t.nchunks <= (uint32_t)kGemvBatch;
+  BatchRows b0;
+  if (one_batch) b0 = batch_wait(c, (int)t.nchunks);
+  // 2. inputs: the vector, then (O, down) the residual rows -- one polling loop for both
+  float ss = 0.f;
+  if (combine) combine_splits(c, l, sv, res);
+#pragma unroll 1
+  for (int j = combine ? 1 : 0; j < 2; ++j) {
+    InVec v = x;
+    if (j == 1) v = r;
+    if (v.n > 0) {
+      const float s = poll_vec(c, v, j == 0 ? 0x100000u : 0x400000u);
+      if (j == 0) ss = s;
     }
-    o[xpos(e, P.nq * d)] = num / den;
+  }
+  if (type == T_QKV) {
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+      const int i = c.ctid + k * kCT;
+      if (i < n) add[i] = __uint_as_float(braw[k] << 16);
+    }
+  }
+  const bool norm = (f & TF_NORM) != 0;
+  if (norm) {
+    ss = warp_sum(ss);
+    if (c.lane == 0) c.ctl->red[c.warp] = ss;
+  }
+  compute_sync();
+  trace_mark(c, 1);
+  // the norm scale: every warp sums the per-warp partials (broadcast reads, fixed order) and
+  // takes 1/sqrt(mean + eps) as the hardware estimate refined by one Newton step,
+  // y' = y (3 - a y^2) / 2, which brings it to within an ulp or so of the rounded value
+  float scale = 1.f;
+  if (norm) {
+    const float4* r4 = reinterpret_cast<const float4*>(c.ctl->red);
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < (kComputeWarps + 3) / 4; ++w) {
+      const float4 v = r4[w];
+      tot += (v.x + v.y) + (v.z + (4 * w + 3 < kComputeWarps ? v.w : 0.f));
+    }
+    const float arg = tot / (float)P.H + P.eps;
+    const float y = rsqrtf(arg);
+    scale = y * fmaf(-0.5f * arg * y, y, 1.5f);
+  }
+  // 3. the projection and its outputs
+  float* logits = c.logits + t.row0;
+  const bool pairs = (f & TF_PAIRS) != 0;
+  if (direct) {
+    // one warp per row (gate/up: per row pair); lane 0 writes the output as soon as its row is done
+    const int nvec = in >> 3;
+    const float4* xlo = reinterpret_cast<const float4*>(sv);
+    const float4* xhi = reinterpret_cast<const float4*>(sv + (in >> 1));
+    const size_t row_bytes = (size_t)in * 2;
+    int rbase = 0;
+#pragma unroll 1
+    for (uint32_t k0 = 0; k0 < t.nchunks; k0 += kGemvBatch) {
+      const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
+      const BatchRows b = one_batch ? b0 : batch_wait(c, nb);
+      const int rows = pairs ? n : b.total;  // gate/up: one batch holds gate rows, then up rows
+#pragma unroll 1
+      for (int q = c.warp; q < rows; q += kComputeWarps) {
+        float a = dot_row(c, b.row(q, row_bytes), xlo, xhi, nvec), u = 0.f;
+        if (pairs) {
+          u = dot_row(c, b.row(n + q, row_bytes), xlo, xhi, nvec);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            u += __shfl_xor_sync(0xffffffffu, u, o);
+          }
+        } else {
+          a = warp_sum(a);
+        }
+        if (c.lane == 0) emit_row(c, type, out, rbase + q, a * scale, u * scale, add, logits);
+      }
+      stages_release(c, (unsigned)nb);
+      rbase += b.total;
+    }
+  } else {
+    // warps share rows: partial sums in res, summed in a fixed order after the barrier
+    gemv_xreg(c, t, in, sv, res, scale);
+    const int gpr = (int)t.gpr;
+#pragma unroll 1
+    for (int i = c.ctid; i < n; i += kCT)
+      emit_row(c, type, out, i, res_row(res, i, gpr), pairs ? res_row(res, n + i, gpr) : 0.f, add, logits);
   }
 }
 
@@ -837,6 +1007,14 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
 }
 
 // ------------------------------------------------------------------ the kernel
+// Copies n task records to shared memory (threads `tid` of `nt`).
+__device__ __forceinline__ void stage_tasks(const Task* src, Task* dst, int n, int tid, int nt) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  const int n16 = n * (int)(sizeof(Task) / 16);
+  for (int i = tid; i < n16; i += nt) d4[i] = s4[i];
+}
+
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const StepParams S) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
@@ -860,6 +1038,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     ctl->bias[3 * i + 2] = P.layers[i].w[LW_BV];
   }
   if (threadIdx.x == 0) ctl->gain[2 * P.L] = P.final_norm;
+  // this CTA's task records, staged in shared memory kTaskWindow at a time (one window covers a
+  // CTA's whole step for the usual shapes)
+  const uint32_t t0 = P.task_off[blockIdx.x], t1 = P.task_off[blockIdx.x + 1];
+  Task* tasks = reinterpret_cast<Task*>(smem + P.off_tasks);
+  stage_tasks(P.tasks + t0, tasks, (int)min(t1 - t0, (uint32_t)kTaskWindow), threadIdx.x, blockDim.x);
   {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(&P);
     uint32_t* dst = reinterpret_cast<uint32_t*>(&ctl->params);
@@ -873,7 +1056,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     produce(ctl->params, S.pos, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31);
     return;
   }
-  const uint32_t t0 = P.task_off[blockIdx.x], t1 = P.task_off[blockIdx.x + 1];
   Ctx c;
   c.P = &ctl->params;
   c.ctl = ctl;
@@ -890,107 +1072,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   c.lane = threadIdx.x & 31;
   float* sv = reinterpret_cast<float*>(smem + P.off_sv);
   float* res = reinterpret_cast<float*>(smem + P.off_res);
-  float* resid = reinterpret_cast<float*>(smem + P.off_resid);
-  // two-deep descriptor pipeline; the gains of the next task load while the current one runs
-  Task cur{}, nxt{};
-  if (t0 < t1) cur = P.tasks[t0];
-  if (t0 + 1 < t1) nxt = P.tasks[t0 + 1];
-  float gcur[4], gnext[4];
-  load_gains(c, cur, gcur);
+  float* add = reinterpret_cast<float*>(smem + P.off_resid);
+#pragma unroll 1
   for (uint32_t ti = t0; ti < t1; ++ti) {
-    const Task t = cur;
-    cur = nxt;
-    if (ti + 2 < t1) nxt = P.tasks[ti + 2];
-    if (ti + 1 < t1) load_gains(c, cur, gnext);
+    const uint32_t k = ti - t0;
+    if (k != 0 && k % kTaskWindow == 0) {  // the next window (every thread is past the last task)
+      stage_tasks(P.tasks + ti, tasks, (int)min(t1 - ti, (uint32_t)kTaskWindow), c.ctid, kCT);
+      compute_sync();
+    }
+    const Task t = tasks[k % kTaskWindow];
     c.task_index = ti;
     c.first_stage = true;
     if (P.trace != nullptr && c.ctid == 0) P.trace[(size_t)ti * 4 + 3] = 0;
     trace_mark(c, 0);
-    if (t.type == T_ATTN) {
+    if (t.type == T_ATTN)
       task_attn(c, t, sv);
-    } else {
-      // 1. inputs: one fetch path for every projection type
-      const int l = t.layer;
-      int in = P.H;
-      float ss = 0.f;
-      float bias[4] = {0.f, 0.f, 0.f, 0.f};
-      if (t.type == T_QKV && P.qkv_bias) {
-        const int qd = P.nq * P.d, kvd = P.nkv * P.d;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = c.ctid + k * kCT;
-          if (i < (int)t.nrows) {
-            const int o = (int)t.row0 + i;
-            const uint16_t* b = o < qd ? ctl->bias[3 * l] + o
-                                       : (o < qd + kvd ? ctl->bias[3 * l + 1] + (o - qd) : ctl->bias[3 * l + 2] + (o - qd - kvd));
-            bias[k] = bf16_to_f32(*b);
-          }
-        }
-      }
-      if (t.type == T_OPROJ) {
-        in = P.nq * P.d;
-        fetch_attention(c, l, sv);
-      } else {
-        const unsigned long long* src;
-        if (t.type == T_QKV) src = x_in_words(P, l);
-        else if (t.type == T_GATEUP) src = layer_words(P, l) + P.act.xa;
-        else if (t.type == T_DOWN) src = layer_words(P, l) + P.act.hh;
-        else src = layer_words(P, P.L - 1) + P.act.xm;  // LM head
-        if (t.type == T_DOWN) in = P.I;
-        fetch_input(c, src, in, t.type == T_DOWN ? nullptr : gcur, sv, &ss);
-      }
-      if (t.type == T_OPROJ || t.type == T_DOWN) {
-        const unsigned long long* rsrc = t.type == T_OPROJ ? x_in_words(P, l) : layer_words(P, l) + P.act.xa;
-        if (rsrc == nullptr) {
-          const uint16_t* e = P.embed + (size_t)c.token * P.H + t.row0;
-          for (int i = c.ctid; i < (int)t.nrows; i += kCT) resid[i] = bf16_to_f32(e[i]);
-        } else {
-          poll_words(c, rsrc + t.row0, (int)t.nrows, 0x400000u, [&](int i, int, float x) { resid[i] = x; });
-        }
-      }
-      const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
-      if (norm) {
-        ss = warp_sum(ss);
-        if (c.lane == 0) ctl->red[c.warp] = ss;
-      }
-      compute_sync();
-      float scale = 1.f;
-      if (norm) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kComputeWarps; ++w) tot += ctl->red[w];
-        scale = 1.0f / sqrtf(tot / (float)P.H + P.eps);
-      }
-      trace_mark(c, 1);
-      // 2. the projection
-      gemv(c, t, in, sv, res, scale);
-      // 3. epilogue
-      const int gpr = (int)t.gpr, n = (int)t.nrows;
-      if (t.type == T_QKV) {
-        unsigned long long* out = layer_words(P, l) + P.act.qkv + t.row0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = c.ctid + k * kCT;
-          if (i < n) put_word(c, out + i, res_row(res, i, gpr) + bias[k]);
-        }
-      } else if (t.type == T_GATEUP) {
-        unsigned long long* out = layer_words(P, l) + P.act.hh + t.row0;
-        for (int i = c.ctid; i < n; i += kCT) {
-          const float gt = res_row(res, i, gpr), up = res_row(res, n + i, gpr);
-          put_word(c, out + i, gt / (1.0f + expf(-gt)) * up);
-        }
-      } else if (t.type == T_LMHEAD) {
-        if (!aborted(c))
-          for (int i = c.ctid; i < n; i += kCT) c.logits[t.row0 + i] = res_row(res, i, gpr);
-      } else {
-        unsigned long long* out = layer_words(P, l) + (t.type == T_OPROJ ? P.act.xa : P.act.xm) + t.row0;
-        for (int i = c.ctid; i < n; i += kCT) put_word(c, out + i, resid[i] + res_row(res, i, gpr));
-      }
-    }
+    else
+      task_gemv(c, t, sv, res, add);
     compute_sync();  // the next task reuses the shared vectors
     trace_mark(c, 2);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) gcur[k] = gnext[k];
   }
 }
 
@@ -1046,3 +1146,4 @@ cudaError_t launch_kv_fill(uint16_t* kv_layer, const float* k_raw, const float* 
   return cudaGetLastError();
 }
 }  // namespace mbk
+

@@ -21,23 +21,44 @@ enum TaskType : uint16_t {
   T_LMHEAD = 6,  // final rmsnorm(x) -> rows of E -> logits
 };
 
+// What a task reads and writes, decided by the scheduler so that the kernel does no per-type
+// address arithmetic: activation words are indices into the step's word array.
+enum TaskFlags : uint16_t {
+  TF_NORM = 1,        // the input is RMS-normalised with gain table entry `gain`
+  TF_PAIRS = 2,       // gate/up: rows r and nrows + r of the task pair up (silu(gate) * up)
+  TF_BIAS = 4,        // q/k/v bias added to the rows
+  TF_IN_EMB = 8,      // the input is the token's embedding row (layer 0)
+  TF_IN_LAYER = 16,   // the input is the layer's input stream (replaceable by injected words)
+  TF_RES = 32,        // the rows add a residual
+  TF_RES_EMB = 64,    // ... taken from the token's embedding row (layer 0)
+  TF_RES_LAYER = 128, // ... taken from the layer's input stream (replaceable by injected words)
+  TF_COMBINE = 256,   // the input is the attention output of several context splits
+  TF_LOGITS = 512,    // the rows are logits (written to the caller's buffer, not as words)
+};
+
 // One task of one CTA.  GEMV tasks: output rows [row0, row0 + nrows) of the op's output space
 // (QKV: the concatenation q|k|v; GATEUP: rows of I, results g then u), weights in static chunks
 // [chunk0, chunk0 + nchunks).  ATTN tasks: row0 = KV head, nrows = context split index; their
-// chunks (cached K/V rows) are derived on the device from the step's position.
+// chunks (cached K/V rows) are derived on the device from the step's position; in_off/out_off
+// are the layer's q|k|v and attention-output words.
 struct Task {
   uint16_t type;
   uint16_t layer;
+  uint16_t gpr;     // GEMV: 0 = one warp per row (small tasks); else warps sharing one weight row
+                    // (a power of two; each keeps its K slice of the input in registers)
+  uint16_t flags;   // TaskFlags
   uint32_t row0;
   uint32_t nrows;
   uint32_t chunk0;
   uint32_t nchunks;
-  uint32_t gpr;     // GEMV: 0 = one warp per row (small tasks); else warps sharing one weight row
-                    // (a power of two; each keeps its K slice of the input in registers)
-  uint32_t lpr;     // GEMV: lanes per warp working on a row (always 32)
+  uint32_t in_off;  // first input word
+  uint32_t in_n;    // input length
+  uint32_t res_off; // first residual word (TF_RES, from words)
+  uint32_t out_off; // first output word
+  uint32_t gain;    // gain table entry (TF_NORM): attn_norm of layer l at 2l, mlp_norm at 2l+1, final at 2L
   uint32_t pad;
 };
-static_assert(sizeof(Task) == 32, "Task layout");
+static_assert(sizeof(Task) == 48, "Task layout");
 
 // One bulk copy into one ring stage: `rows` whole weight rows starting at `src` (bytes = rows *
 // row bytes; a multiple of 16, src 16-byte aligned).  An attention task owns one placeholder chunk
@@ -54,7 +75,8 @@ static_assert(sizeof(Chunk) == 16, "Chunk layout");
 // Offsets (in 8-byte words) of one layer's activation exchange words.
 struct ActLayout {
   uint32_t qkv;       // (nq + 2 nkv) * d   raw projections, pre-RoPE
-  uint32_t att;       // nkv * nsplit * g * (d + 2)   per split: o (normalised), m, l per head
+  uint32_t att;       // nsplit * nq * (d + 2): o [split][head][d] (normalised per split), then
+                      // (m, l) [split][head][2] -- the active splits of a step are a prefix of each
   uint32_t xa;        // H   residual stream after the attention sublayer
   uint32_t hh;        // I   silu(g) * u
   uint32_t xm;        // H   residual stream after the MLP sublayer (input of the next layer)
@@ -64,16 +86,21 @@ struct ActLayout {
 constexpr int kStageBytes = 16384;     // one ring stage
 constexpr int kMaxTaskRows = 2048;     // output rows per task
 constexpr int kResSlots = 4096;        // per-task partial results (rows x warps per row)
-constexpr int kComputeWarps = 16;
-constexpr int kThreads = 32 * (kComputeWarps + 1);  // warp 0 streams weights, warps 1..16 compute
+// 15 compute warps + the producer = 16 warps, four per SM sub-partition, so every thread may use
+// 128 registers (a 17th warp would cap them at 96 and push live state to local memory)
+constexpr int kComputeWarps = 15;
+constexpr int kThreads = 32 * (kComputeWarps + 1);  // warp 0 streams weights, warps 1..15 compute
+constexpr int kMaxHidden = 2048;       // largest hidden size
+constexpr int kVecPerThread = (kMaxHidden + kComputeWarps * 32 - 1) / (kComputeWarps * 32);  // H or task rows / thread
 constexpr int kAttnSplitMax = 512;     // context positions per attention split (long contexts)
 constexpr int kAttnSplitStages = 8;    // ring stages per attention split
 constexpr int kMaxRingStages = 32;
 constexpr int kMaxTaskChunks = 256;
 constexpr int kGemvBatch = 4;          // ring stages a GEMV consumes together
 constexpr int kGemvXVec = 4;           // 16-byte input vectors a GEMV lane keeps in registers
-constexpr int kCtlBytes = 4096;        // shared-memory control block (barriers, flags, tables)
+constexpr int kCtlBytes = 4224;        // shared-memory control block (barriers, flags, tables, parameters)
 constexpr int kMaxLayers = 64;
+constexpr int kTaskWindow = 160;      // task records staged in shared memory at a time
 
 struct PlanShape {
   int L, H, I, nq, nkv, d, V, C;

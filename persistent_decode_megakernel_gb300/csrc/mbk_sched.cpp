@@ -53,14 +53,20 @@ uint32_t pow2_ceil(uint32_t v) {
 }
 void gemv_layout(const std::vector<Chunk>& chunks, Task& t, int in, int res_per_row) {
   const uint32_t nvec = (uint32_t)in / 8;
-  t.lpr = 32;
   uint32_t max_rows = 1;
   for (uint32_t k = 0; k < t.nchunks; k += kGemvBatch) {
     uint32_t rows = 0;
     for (uint32_t j = k; j < std::min<uint32_t>(t.nchunks, k + kGemvBatch); ++j) rows += chunks[t.chunk0 + j].rows;
     max_rows = std::max(max_rows, rows);
   }
-  if (max_rows <= (uint32_t)kComputeWarps) {  // small task: one warp per row, x from shared memory
+  if (res_per_row == 2) {
+    // gate/up: with one batch and at most one row pair per warp, a warp takes gate row r and up row
+    // r together and writes silu(gate) * up itself
+    if (t.nchunks <= (uint32_t)kGemvBatch && t.nrows <= (uint32_t)kComputeWarps) {
+      t.gpr = 0;
+      return;
+    }
+  } else if (max_rows <= (uint32_t)kComputeWarps) {  // small task: one warp per row, x from shared memory
     t.gpr = 0;
     return;
   }
@@ -68,7 +74,7 @@ void gemv_layout(const std::vector<Chunk>& chunks, Task& t, int in, int res_per_
   const uint32_t lanes = pow2_floor(std::max(1u, nvec / 32));                          // a vector per lane
   const uint32_t work = pow2_floor(std::max(1u, (uint32_t)kComputeWarps / ((max_rows + 1) / 2)));
   uint32_t gpr = std::max(need, std::min(lanes, work));
-  gpr = std::min<uint32_t>(gpr, kComputeWarps);
+  gpr = std::min<uint32_t>(gpr, pow2_floor(kComputeWarps));
   while (gpr > need && (uint64_t)t.nrows * res_per_row * gpr > (uint64_t)kResSlots) gpr /= 2;
   t.gpr = gpr;
 }
@@ -118,6 +124,58 @@ WeightAddrs fake_weight_addrs(const PlanShape& s) {
   return w;
 }
 
+namespace {
+// The words a task reads and writes (indices into the step's word array) and its flags.
+void fill_task_io(const PlanShape& s, const Plan& p, Task& t) {
+  const ActLayout& a = p.act;
+  const uint32_t l = t.layer, pl = a.per_layer;
+  const uint32_t lw = l * pl, prev = l > 0 ? (l - 1) * pl + a.xm : 0;  // this layer's words; its input stream
+  t.flags = 0;
+  t.in_off = t.in_n = t.res_off = t.out_off = t.gain = t.pad = 0;
+  switch (t.type) {
+    case T_QKV:
+      t.flags = TF_NORM | (l == 0 ? TF_IN_EMB : TF_IN_LAYER) | (s.qkv_bias ? TF_BIAS : 0);
+      t.in_off = prev;
+      t.in_n = (uint32_t)s.H;
+      t.gain = 2 * l;
+      t.out_off = lw + a.qkv + t.row0;
+      break;
+    case T_ATTN:
+      t.in_off = lw + a.qkv;
+      t.in_n = (uint32_t)((s.nq + 2 * s.nkv) * s.d);
+      t.out_off = lw + a.att;
+      break;
+    case T_OPROJ:
+      t.flags = TF_RES | (l == 0 ? TF_RES_EMB : TF_RES_LAYER) | (p.nsplit > 1 ? TF_COMBINE : 0);
+      t.in_off = lw + a.att;
+      t.in_n = (uint32_t)(s.nq * s.d);
+      t.res_off = prev + t.row0;
+      t.out_off = lw + a.xa + t.row0;
+      break;
+    case T_GATEUP:
+      t.flags = TF_NORM | TF_PAIRS;
+      t.in_off = lw + a.xa;
+      t.in_n = (uint32_t)s.H;
+      t.gain = 2 * l + 1;
+      t.out_off = lw + a.hh + t.row0;
+      break;
+    case T_DOWN:
+      t.flags = TF_RES;
+      t.in_off = lw + a.hh;
+      t.in_n = (uint32_t)s.I;
+      t.res_off = lw + a.xa + t.row0;
+      t.out_off = lw + a.xm + t.row0;
+      break;
+    default:  // LM head
+      t.flags = TF_NORM | TF_LOGITS;
+      t.in_off = (uint32_t)(s.L - 1) * pl + a.xm;
+      t.in_n = (uint32_t)s.H;
+      t.gain = 2 * (uint32_t)s.L;
+      break;
+  }
+}
+}  // namespace
+
 std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, const PlanOptions& opt, Plan* out) {
   std::string err = validate_shape(s);
   if (!err.empty()) return err;
@@ -135,6 +193,8 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   const int split_cap = std::min(kAttnSplitMax, kAttnSplitStages * p.attn_rows_per_stage);
   p.split_len = s.C <= split_cap ? s.C : split_cap;
   p.nsplit = (s.C + p.split_len - 1) / p.split_len;
+  // the split combine keeps (m, l) of every query head and split in the results area
+  if (s.nq * p.nsplit * 2 > kResSlots) return "KV capacity too long for the attention split combine";
 
   // activation words
   ActLayout a{};
@@ -149,19 +209,12 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
 
   // shared memory layout: [barriers + flags 1 KB][input vector][results][residuals][ring]
   const int O = g * s.d;
-  int attn_floats = O + g * (p.split_len + 1) + std::max(2 * kComputeWarps * 32, O) + 2 * s.d + 2 * g + 8;
+  // attention: rotated queries, current K/V (raw, then the bf16 row appended) and the partial
+  // output (o, m, l) of every (32-position block, query head) item of a split
+  const int attn_items = (p.split_len + 31) / 32 * g;
+  int attn_floats = O + 3 * s.d + attn_items * (s.d + 2);
   p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
   p.sv_floats = (p.sv_floats + 31) / 32 * 32;
-  p.off_sv = kCtlBytes;
-  p.off_res = p.off_sv + (uint32_t)p.sv_floats * 4;
-  p.off_resid = p.off_res + kResSlots * 4;
-  p.off_ring = (p.off_resid + kMaxTaskRows * 4 + 127) / 128 * 128;
-  int avail = opt.smem_limit - (int)p.off_ring;
-  p.num_stages = std::min(kMaxRingStages, avail / kStageBytes);
-  if (p.num_stages < 2) return "not enough shared memory for the weight ring";
-  if (p.num_stages < (p.split_len + p.attn_rows_per_stage - 1) / p.attn_rows_per_stage + 1 || p.num_stages < kGemvBatch)
-    return "weight ring too small to hold one attention split or one GEMV batch";
-  p.smem_bytes = (int)p.off_ring + p.num_stages * kStageBytes;
 
   // tasks
   std::vector<std::vector<Task>> cta_tasks(num_ctas);
@@ -171,8 +224,13 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   const int max_tasks = opt.max_tasks_per_op > 0 ? std::min(opt.max_tasks_per_op, num_ctas) : num_ctas;
 
   // row-split GEMV op: `segs_for(r0, r1)` lists the weight segments of output rows [r0, r1)
+  // CTAs that ran this layer's attention tasks: the O projection that follows skips them, since
+  // they finish their attention last (when other CTAs are left)
+  std::vector<char> busy(num_ctas, 0);
+  int n_busy = 0;
   auto gemv_op = [&](TaskType type, int layer, int rows, int res_per_row, int row_bytes, auto segs_for) {
     int n = std::min(max_tasks, rows);
+    if (type == T_OPROJ && n_busy < num_ctas) n = std::min(n, num_ctas - n_busy);  // one task per free CTA
     // results per task must fit the result slots, and its chunks the per-task chunk bound
     const int rpc = kStageBytes / row_bytes;
     auto chunks_for = [&](int task_rows) { return res_per_row * ((task_rows + rpc - 1) / rpc) + 2; };
@@ -182,6 +240,12 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       if (r1 <= r0) continue;
       int cta = cursor % num_ctas;
       ++cursor;
+      if (type == T_OPROJ && n_busy < num_ctas) {
+        while (busy[cta]) {
+          cta = cursor % num_ctas;
+          ++cursor;
+        }
+      }
       Task t{};
       t.type = type;
       t.layer = (uint16_t)layer;
@@ -209,10 +273,14 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       }
       return v;
     });
+    std::fill(busy.begin(), busy.end(), 0);
+    n_busy = 0;
     for (int kvh = 0; kvh < s.nkv; ++kvh) {
       for (int sp = 0; sp < p.nsplit; ++sp) {
         int cta = cursor % num_ctas;
         ++cursor;
+        if (!busy[cta]) ++n_busy;
+        busy[cta] = 1;
         Task t{};
         t.type = T_ATTN;
         t.layer = (uint16_t)l;
@@ -263,13 +331,29 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
     }
   }
 
-  // flatten (chunk indices become global)
+  // shared memory layout: [control block][input vector][results][residuals][task records][ring]
+  p.max_cta_tasks = 0;
+  for (const auto& v : cta_tasks) p.max_cta_tasks = std::max(p.max_cta_tasks, (int)v.size());
+  p.off_sv = kCtlBytes;
+  p.off_res = p.off_sv + (uint32_t)p.sv_floats * 4;
+  p.off_resid = p.off_res + kResSlots * 4;
+  p.off_tasks = p.off_resid + kMaxTaskRows * 4;
+  p.off_ring = (p.off_tasks + (uint32_t)std::min(p.max_cta_tasks, kTaskWindow) * (uint32_t)sizeof(Task) + 127) / 128 * 128;
+  int avail = opt.smem_limit - (int)p.off_ring;
+  p.num_stages = std::min(kMaxRingStages, avail / kStageBytes);
+  if (p.num_stages < 2) return "not enough shared memory for the weight ring";
+  if (p.num_stages < (p.split_len + p.attn_rows_per_stage - 1) / p.attn_rows_per_stage + 1 || p.num_stages < kGemvBatch)
+    return "weight ring too small to hold one attention split or one GEMV batch";
+  p.smem_bytes = (int)p.off_ring + p.num_stages * kStageBytes;
+
+  // flatten (chunk indices become global); every task gets its word offsets and flags
   p.task_off.assign(num_ctas + 1, 0);
   p.chunk_off.assign(num_ctas + 1, 0);
   for (int c = 0; c < num_ctas; ++c) {
     uint32_t base = (uint32_t)p.chunks.size();
     for (Task t : cta_tasks[c]) {
       t.chunk0 += base;
+      fill_task_io(s, p, t);
       p.tasks.push_back(t);
     }
     p.chunks.insert(p.chunks.end(), cta_chunks[c].begin(), cta_chunks[c].end());
@@ -351,6 +435,8 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
       {
         const int in = t.type == T_OPROJ ? qd : (t.type == T_DOWN ? s.I : s.H);
         const uint32_t nvec = (uint32_t)in / 8;
+        if (t.gpr == 0 && t.type == T_GATEUP && (t.nchunks > (uint32_t)kGemvBatch || t.nrows > (uint32_t)kComputeWarps))
+          return "gate/up row pairs do not fit one batch";
         if (t.gpr != 0 && ((t.gpr & (t.gpr - 1)) || t.gpr > (uint32_t)kComputeWarps ||
                            (uint64_t)res * t.gpr > (uint64_t)kResSlots || (nvec + t.gpr - 1) / t.gpr > 32u * kGemvXVec))
           return "bad GEMV layout";
@@ -388,6 +474,33 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
       }
   if (attn_tasks != s.L * s.nkv * p.nsplit) return "attention task count";
   if (p.smem_bytes > 232448) return "shared memory over the sm_10x limit";
+  // every GEMV output word of every layer is written by exactly one task; all word ranges in bounds
+  {
+    std::vector<uint8_t> cov(p.act_words, 0);
+    for (const Task& t : p.tasks) {
+      if (t.type == T_ATTN) {
+        if ((uint64_t)t.in_off + t.in_n > p.act_words) return "attention input words out of range";
+        continue;
+      }
+      if ((uint64_t)t.in_off + t.in_n > p.act_words) return "task input words out of range";
+      if ((t.flags & TF_RES) && !(t.flags & TF_RES_EMB) && (uint64_t)t.res_off + t.nrows > p.act_words)
+        return "task residual words out of range";
+      if (t.type == T_LMHEAD) continue;
+      if ((uint64_t)t.out_off + t.nrows > p.act_words) return "task output words out of range";
+      for (uint32_t r = 0; r < t.nrows; ++r) ++cov[t.out_off + r];
+    }
+    const ActLayout& a = p.act;
+    for (int l = 0; l < s.L; ++l) {
+      const uint64_t b = (uint64_t)l * a.per_layer;
+      auto once = [&](uint32_t off, int n) {
+        for (int i = 0; i < n; ++i)
+          if (cov[b + off + i] != 1) return false;
+        return true;
+      };
+      if (!once(a.qkv, qd + 2 * kvd) || !once(a.xa, s.H) || !once(a.hh, s.I) || !once(a.xm, s.H))
+        return "an output word is not written exactly once";
+    }
+  }
   return "";
 }
 

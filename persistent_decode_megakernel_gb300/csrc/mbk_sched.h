@@ -36,7 +36,8 @@ struct Plan {
   int num_stages = 0;
   int smem_bytes = 0;
   int sv_floats = 0;                 // floats in the input-vector region
-  uint32_t off_sv = 0, off_res = 0, off_resid = 0, off_ring = 0;  // shared-memory layout (bytes)
+  int max_cta_tasks = 0;             // tasks of the busiest CTA (records staged in shared memory, kTaskWindow at a time)
+  uint32_t off_sv = 0, off_res = 0, off_resid = 0, off_tasks = 0, off_ring = 0;  // shared-memory layout (bytes)
   int64_t weight_bytes = 0;          // static chunk bytes per step
   int64_t max_cta_bytes = 0;
 };

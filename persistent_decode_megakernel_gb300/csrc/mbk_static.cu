@@ -186,6 +186,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     kp.off_sv = plan.off_sv;
     kp.off_res = plan.off_res;
     kp.off_resid = plan.off_resid;
+    kp.off_tasks = plan.off_tasks;
     kp.off_ring = plan.off_ring;
     kp.embed = reinterpret_cast<const uint16_t*>(weights->embed);
     kp.final_norm = reinterpret_cast<const uint16_t*>(weights->final_norm);

@@ -86,10 +86,13 @@ def test_bias_small_shape():
     rep.check()
 
 
-def test_deterministic_and_resumable():
-    """Bitwise-identical logits on a rerun, and after resuming from a copied cache in a new handle."""
+@pytest.mark.parametrize("shape", ["tiny", "smollm-135m"])
+def test_deterministic_and_resumable(shape):
+    """Bitwise-identical logits on a rerun, and after resuming from a copied cache in a new handle.
+    (The 135M shape has more activation words than compute threads, so each thread sums several
+    late-arriving words: the result must not depend on their arrival order.)"""
     from persistent_decode_megakernel_gb300.mbk import Decoder
-    wl = workloads.generate("tiny", seed=0)
+    wl = workloads.generate(shape, seed=0)
     a = Decoder(wl)
     full = torch.stack([a.step(int(wl.tokens[i]), i).clone() for i in range(10)])
     b = Decoder(wl)
