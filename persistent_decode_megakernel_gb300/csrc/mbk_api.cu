@@ -267,6 +267,7 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   kp.g = s.nq / s.nkv;
   kp.eps = (float)cfg->rms_eps;
   kp.attn_scale = (float)(1.0 / std::sqrt((double)s.d));
+  kp.inv_H = (float)(1.0 / (double)kp.H);
   kp.qkv_bias = s.qkv_bias;
   kp.tasks = h->d_tasks;
   kp.task_off = h->d_task_off;

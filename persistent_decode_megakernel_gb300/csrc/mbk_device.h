@@ -18,7 +18,7 @@ struct LayerW {
 // Constant for the lifetime of a handle (4-byte multiple, copied word by word into shared memory).
 struct KernelParams {
   int L, H, I, nq, nkv, d, V, C, g;
-  float eps, attn_scale;
+  float eps, attn_scale, inv_H;  // inv_H = 1/H rounded to fp32
   int qkv_bias;
   // schedule
   const Task* tasks;

@@ -188,7 +188,15 @@ struct InVec {
   const uint16_t* gain;
   float* dst;
   int n, xlayout;
+  // up to three segments: elements [0, n1) from src, [n1, n1 + n2) from src2, the rest from src3
+  // (one poll for a KV head's queries, key and value); n1 = n for a plain vector
+  const unsigned long long* src2;
+  const unsigned long long* src3;
+  int n1, n2;
 };
+__device__ __forceinline__ const unsigned long long* word_addr(const InVec& v, int e) {
+  return e < v.n1 ? v.src + e : (e < v.n1 + v.n2 ? v.src2 + (e - v.n1) : v.src3 + (e - v.n1 - v.n2));
+}
 
 // Every thread polls its elements ctid + k*kCT four at a time; all loads of a group are in flight
 // together and every retry re-loads all words still pending, so a late group costs one round trip
@@ -210,7 +218,7 @@ __device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detai
       graw[k] = 0x3f80u;  // bf16 1.0
       if (e < v.n) {
         if (v.src != nullptr) {
-          w[k] = ld_word(v.src + e);
+          w[k] = ld_word(word_addr(v, e));
           pend |= 1u << k;
         } else {
           w[k] = (unsigned long long)((uint32_t)v.emb[e] << 16);
@@ -235,7 +243,7 @@ __device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detai
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int e = e0 + k * kCT;
-        if ((pend >> k) & 1u) w[k] = ld_word(v.src + e);
+        if ((pend >> k) & 1u) w[k] = ld_word(word_addr(v, e));
       }
     }
 #pragma unroll
@@ -432,19 +440,27 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
       const uint4* B = row_of(two ? rb : ra);
       unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
 #pragma unroll
-      for (int k = 0; k < kGemvXVec; ++k) {
-        const int v = v0 + c.lane + 32 * k;
-        if (v < v1) {
-          const uint4 wa = A[v];
-          const uint4 wb = B[v];
-          a0 = ffma2(bf2(wa.x), xp[k][0], a0);
-          a1 = ffma2(bf2(wa.y), xp[k][1], a1);
-          a0 = ffma2(bf2(wa.z), xp[k][2], a0);
-          a1 = ffma2(bf2(wa.w), xp[k][3], a1);
-          b0 = ffma2(bf2(wb.x), xp[k][0], b0);
-          b1 = ffma2(bf2(wb.y), xp[k][1], b1);
-          b0 = ffma2(bf2(wb.z), xp[k][2], b0);
-          b1 = ffma2(bf2(wb.w), xp[k][3], b1);
+      for (int k2 = 0; k2 < kGemvXVec; k2 += 2) {
+        uint4 wa4[2], wb4[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // loads first (clamped index, zeroed weights past the slice)
+          const int v = v0 + c.lane + 32 * (k2 + k);
+          const int vi = v < v1 ? v : 0;
+          wa4[k] = A[vi];
+          wb4[k] = B[vi];
+          if (v >= v1) wa4[k] = wb4[k] = make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const unsigned long long* xk = xp[k2 + k];
+          a0 = ffma2(bf2(wa4[k].x), xk[0], a0);
+          a1 = ffma2(bf2(wa4[k].y), xk[1], a1);
+          a0 = ffma2(bf2(wa4[k].z), xk[2], a0);
+          a1 = ffma2(bf2(wa4[k].w), xk[3], a1);
+          b0 = ffma2(bf2(wb4[k].x), xk[0], b0);
+          b1 = ffma2(bf2(wb4[k].y), xk[1], b1);
+          b0 = ffma2(bf2(wb4[k].z), xk[2], b0);
+          b1 = ffma2(bf2(wb4[k].w), xk[3], b1);
         }
       }
       float sa = sum2(a0) + sum2(a1), sb = sum2(b0) + sum2(b1);
@@ -464,25 +480,69 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
   compute_sync();
 }
 
+// Loads of one round are issued unconditionally (an index past the row end is clamped to the row
+// start and its weights zeroed), so they are all in flight before the first FMA.
 __device__ __forceinline__ float dot_row(const Ctx& c, const uint4* row, const float4* xlo, const float4* xhi, int nvec) {
-  // eight 16-byte vectors per lane per round, unrolled so their loads are all in flight together
   unsigned long long a0 = 0ull, a1 = 0ull;
 #pragma unroll 1
-  for (int v0 = c.lane; v0 < nvec; v0 += 256) {
+  for (int v0 = c.lane; v0 < nvec; v0 += 128) {
+    uint4 w[4];
+    float4 p[4], q[4];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < 4; ++it) {
       const int v = v0 + 32 * it;
-      if (v < nvec) {
-        const uint4 w = row[v];
-        const float4 p = xlo[v], q = xhi[v];
-        a0 = ffma2(bf2(w.x), pack2(__float_as_uint(p.x), __float_as_uint(p.y)), a0);
-        a1 = ffma2(bf2(w.y), pack2(__float_as_uint(p.z), __float_as_uint(p.w)), a1);
-        a0 = ffma2(bf2(w.z), pack2(__float_as_uint(q.x), __float_as_uint(q.y)), a0);
-        a1 = ffma2(bf2(w.w), pack2(__float_as_uint(q.z), __float_as_uint(q.w)), a1);
-      }
+      const int vi = v < nvec ? v : v0;
+      w[it] = row[vi];
+      p[it] = xlo[vi];
+      q[it] = xhi[vi];
+      if (v >= nvec) w[it] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      a0 = ffma2(bf2(w[it].x), pack2(__float_as_uint(p[it].x), __float_as_uint(p[it].y)), a0);
+      a1 = ffma2(bf2(w[it].y), pack2(__float_as_uint(p[it].z), __float_as_uint(p[it].w)), a1);
+      a0 = ffma2(bf2(w[it].z), pack2(__float_as_uint(q[it].x), __float_as_uint(q[it].y)), a0);
+      a1 = ffma2(bf2(w[it].w), pack2(__float_as_uint(q[it].z), __float_as_uint(q[it].w)), a1);
     }
   }
   return sum2(a0) + sum2(a1);
+}
+// Two rows against the same x (gate and up rows): the x vectors are loaded once for both.
+__device__ __forceinline__ void dot_row2(const Ctx& c, const uint4* ra, const uint4* rb, const float4* xlo,
+                                         const float4* xhi, int nvec, float& sa, float& sb) {
+  unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
+#pragma unroll 1
+  for (int v0 = c.lane; v0 < nvec; v0 += 64) {
+    uint4 wa[2], wb[2];
+    float4 p[2], q[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int v = v0 + 32 * it;
+      const int vi = v < nvec ? v : v0;
+      wa[it] = ra[vi];
+      wb[it] = rb[vi];
+      p[it] = xlo[vi];
+      q[it] = xhi[vi];
+      if (v >= nvec) wa[it] = wb[it] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const unsigned long long x0 = pack2(__float_as_uint(p[it].x), __float_as_uint(p[it].y));
+      const unsigned long long x1 = pack2(__float_as_uint(p[it].z), __float_as_uint(p[it].w));
+      const unsigned long long x2 = pack2(__float_as_uint(q[it].x), __float_as_uint(q[it].y));
+      const unsigned long long x3 = pack2(__float_as_uint(q[it].z), __float_as_uint(q[it].w));
+      a0 = ffma2(bf2(wa[it].x), x0, a0);
+      a1 = ffma2(bf2(wa[it].y), x1, a1);
+      a0 = ffma2(bf2(wa[it].z), x2, a0);
+      a1 = ffma2(bf2(wa[it].w), x3, a1);
+      b0 = ffma2(bf2(wb[it].x), x0, b0);
+      b1 = ffma2(bf2(wb[it].y), x1, b1);
+      b0 = ffma2(bf2(wb[it].z), x2, b0);
+      b1 = ffma2(bf2(wb[it].w), x3, b1);
+    }
+  }
+  sa = sum2(a0) + sum2(a1);
+  sb = sum2(b0) + sum2(b1);
 }
 // Rows of the stages of one batch, in chunk order: row r of the batch.
 struct BatchRows {
@@ -563,21 +623,22 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
   float* pw = vc + 2 * d;                     // [items][d + 2]  per-item o, m, l
   const float2* cs = c.ctl->rope;             // this step's cos/sin (loaded at kernel start)
 
-  // 1. the packed queries and (owner) the current K/V row
+  // 1. the packed queries and (owner) the current K/V row, in one poll: they land in sq|kc|vc
   {
     const unsigned long long* w = layer_words(P, l) + P.act.qkv;
     const int qd = P.nq * d, kvd = P.nkv * d;
-#pragma unroll 1
-    for (int j = 0; j < (owner ? 3 : 1); ++j) {
-      InVec v;
-      v.src = j == 0 ? w + (size_t)kvh * O : (j == 1 ? w + qd + kvh * d : w + qd + kvd + kvh * d);
-      v.emb = nullptr;
-      v.gain = nullptr;
-      v.dst = j == 0 ? sq : (j == 1 ? kc : vc);
-      v.n = j == 0 ? O : d;
-      v.xlayout = 0;
-      poll_vec(c, v, 0x200000u | ((unsigned)j << 16));
-    }
+    InVec v;
+    v.src = w + (size_t)kvh * O;
+    v.src2 = w + qd + kvh * d;
+    v.src3 = w + qd + kvd + kvh * d;
+    v.n1 = O;
+    v.n2 = d;
+    v.n = owner ? O + 2 * d : O;
+    v.emb = nullptr;
+    v.gain = nullptr;
+    v.dst = sq;
+    v.xlayout = 0;
+    poll_vec(c, v, 0x200000u);
   }
   compute_sync();
   trace_mark(c, 1);
@@ -640,6 +701,8 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
     const bool valid = j < np;
     // this lane's score: the full dot product of its K row with the query, chunk order rotated
     // by lane so that the 32 rows are read without bank conflicts
+    const int j0b = blk << 5;
+    const int nj = min(32, np - j0b);
     float s = -INFINITY;
     if (valid) {
       const uint4* kr = reinterpret_cast<const uint4*>(krow(j));
@@ -664,18 +727,34 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
     const float m = warp_max(s);
     const float p = valid ? exp2f(s - m) : 0.f;
     const float lsum = warp_sum(p);
-    // the block's output: lane owns element pairs 2*lane (+64); position jj's weight comes from lane jj
-    const int nj = min(32, np - (blk << 5));
+    // the block's output: lane owns element pairs 2*lane (+64); position jj's weight comes from lane
+    // jj.  A block's cached rows are consecutive rows of one stage (32 divides R); the appended
+    // row, if the block holds it, comes last.
+    const int ncache = max(0, min(nj, nh - j0b));
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 4
-    for (int jj = 0; jj < nj; ++jj) {
-      const float pj = __shfl_sync(0xffffffffu, p, jj);
-      const uint16_t* vr = vrow((blk << 5) + jj);
-      const uint32_t v01 = *reinterpret_cast<const uint32_t*>(vr + 2 * c.lane);
+    if (ncache > 0) {
+      const uint16_t* vb = vrow(j0b) + 2 * c.lane;
+#pragma unroll 8
+      for (int jj = 0; jj < ncache; ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+        const uint32_t v01 = *reinterpret_cast<const uint32_t*>(vb + jj * d);
+        a0 = fmaf(pj, bf16_lo(v01), a0);
+        a1 = fmaf(pj, bf16_hi(v01), a1);
+        if (d > 64) {
+          const uint32_t v23 = *reinterpret_cast<const uint32_t*>(vb + jj * d + 64);
+          a2 = fmaf(pj, bf16_lo(v23), a2);
+          a3 = fmaf(pj, bf16_hi(v23), a3);
+        }
+      }
+    }
+    if (nj > ncache) {  // the appended row
+      const float pj = __shfl_sync(0xffffffffu, p, ncache);
+      const uint16_t* vr = cur + d + 2 * c.lane;
+      const uint32_t v01 = *reinterpret_cast<const uint32_t*>(vr);
       a0 = fmaf(pj, bf16_lo(v01), a0);
       a1 = fmaf(pj, bf16_hi(v01), a1);
       if (d > 64) {
-        const uint32_t v23 = *reinterpret_cast<const uint32_t*>(vr + 64 + 2 * c.lane);
+        const uint32_t v23 = *reinterpret_cast<const uint32_t*>(vr + 64);
         a2 = fmaf(pj, bf16_lo(v23), a2);
         a3 = fmaf(pj, bf16_hi(v23), a3);
       }
@@ -739,6 +818,9 @@ __device__ __forceinline__ void combine_splits(Ctx& c, int l, float* o, float* m
     v.dst = ml;
     v.n = nact * P.nq * 2;
     v.xlayout = 0;
+    v.src2 = v.src3 = nullptr;
+    v.n1 = v.n;
+    v.n2 = 0;
     poll_vec(c, v, 0x310000u);
   }
   compute_sync();
@@ -802,12 +884,18 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
   x.dst = sv;
   x.n = (int)t.in_n;
   x.xlayout = 1;
+  x.src2 = x.src3 = nullptr;
+  x.n1 = x.n;
+  x.n2 = 0;
   r.src = (f & TF_RES_EMB) ? nullptr : ((f & TF_RES_LAYER) && layer_in ? layer_in + t.row0 : P.words + t.res_off);
   r.emb = emb_row + t.row0;
   r.gain = nullptr;
   r.dst = add;
   r.n = (f & TF_RES) ? n : 0;
   r.xlayout = 0;
+  r.src2 = r.src3 = nullptr;
+  r.n1 = r.n;
+  r.n2 = 0;
   unsigned long long* out = P.words + t.out_off;
   const int in = (int)t.in_n;
   const bool combine = (f & TF_COMBINE) != 0;  // O projection over several context splits
@@ -859,11 +947,11 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
   }
   compute_sync();
   trace_mark(c, 1);
-  // the norm scale: every warp sums the per-warp partials (broadcast reads, fixed order) and
-  // takes 1/sqrt(mean + eps) as the hardware estimate refined by one Newton step,
-  // y' = y (3 - a y^2) / 2, which brings it to within an ulp or so of the rounded value
-  float scale = 1.f;
-  if (norm) {
+  // the norm scale (every warp sums the per-warp partials with broadcast reads, fixed order); taken
+  // after the warp's first dot product so its latency overlaps the GEMV.  1/sqrt(mean + eps) is the
+  // hardware estimate refined by one Newton step, y' = y (3 - a y^2) / 2, to within about an ulp.
+  auto norm_scale = [&]() -> float {
+    if (!norm) return 1.f;
     const float4* r4 = reinterpret_cast<const float4*>(c.ctl->red);
     float tot = 0.f;
 #pragma unroll
@@ -871,10 +959,11 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
       const float4 v = r4[w];
       tot += (v.x + v.y) + (v.z + (4 * w + 3 < kComputeWarps ? v.w : 0.f));
     }
-    const float arg = tot / (float)P.H + P.eps;
+    const float arg = fmaf(tot, P.inv_H, P.eps);
     const float y = rsqrtf(arg);
-    scale = y * fmaf(-0.5f * arg * y, y, 1.5f);
-  }
+    return y * fmaf(-0.5f * arg * y, y, 1.5f);
+  };
+  float scale = 0.f;
   // 3. the projection and its outputs
   float* logits = c.logits + t.row0;
   const bool pairs = (f & TF_PAIRS) != 0;
@@ -892,17 +981,18 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
       const int rows = pairs ? n : b.total;  // gate/up: one batch holds gate rows, then up rows
 #pragma unroll 1
       for (int q = c.warp; q < rows; q += kComputeWarps) {
-        float a = dot_row(c, b.row(q, row_bytes), xlo, xhi, nvec), u = 0.f;
+        float a, u = 0.f;
         if (pairs) {
-          u = dot_row(c, b.row(n + q, row_bytes), xlo, xhi, nvec);
+          dot_row2(c, b.row(q, row_bytes), b.row(n + q, row_bytes), xlo, xhi, nvec, a, u);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             a += __shfl_xor_sync(0xffffffffu, a, o);
             u += __shfl_xor_sync(0xffffffffu, u, o);
           }
         } else {
-          a = warp_sum(a);
+          a = warp_sum(dot_row(c, b.row(q, row_bytes), xlo, xhi, nvec));
         }
+        if (scale == 0.f) scale = norm_scale();
         if (c.lane == 0) emit_row(c, type, out, rbase + q, a * scale, u * scale, add, logits);
       }
       stages_release(c, (unsigned)nb);
@@ -910,7 +1000,7 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
     }
   } else {
     // warps share rows: partial sums in res, summed in a fixed order after the barrier
-    gemv_xreg(c, t, in, sv, res, scale);
+    gemv_xreg(c, t, in, sv, res, norm_scale());
     const int gpr = (int)t.gpr;
 #pragma unroll 1
     for (int i = c.ctid; i < n; i += kCT)
@@ -934,6 +1024,9 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
       if (!mbar_test(&ctl->empty[stage], ph)) {
         const unsigned long long tstart = global_ns();
         while (!mbar_test(&ctl->empty[stage], ph)) {
+          // The ring is full and the stream is far ahead of the consumers: sleep between tests so
+          // that this warp leaves its sub-partition's issue slots to the compute warps.
+          __nanosleep(128);
           // Consumers keep taking stages even after a failed activation wait (they stop waiting
           // for activations instead), so this only expires if a consumer is wedged: stop streaming.
           if (global_ns() - tstart > 4 * P.timeout_ns) {

@@ -173,6 +173,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     kp.g = s.nq / s.nkv;
     kp.eps = (float)cfg->rms_eps;
     kp.attn_scale = (float)(1.0 / std::sqrt((double)s.d));
+    kp.inv_H = (float)(1.0 / (double)kp.H);
     kp.qkv_bias = s.qkv_bias;
     kp.tasks = reinterpret_cast<const Task*>(b + o_tasks);
     kp.task_off = reinterpret_cast<const uint32_t*>(b + o_toff);
