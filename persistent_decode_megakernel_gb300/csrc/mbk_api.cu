@@ -125,6 +125,7 @@ int mbk_plan_check(const mbk_config* cfg, int num_sms, mbk_plan_info* info) {
   Plan p;
   PlanOptions opt;
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
+  opt.fuse_attention = env_int("MBK_FUSE_ATTENTION", -1);
   std::string err = build_plan(s, w, num_sms, opt, &p);
   if (!err.empty()) return MBK_ERR_STATE;
   info->num_ctas = p.num_ctas;
@@ -185,6 +186,7 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   PlanOptions opt;
   opt.smem_limit = smem_optin;
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
+  opt.fuse_attention = env_int("MBK_FUSE_ATTENTION", -1);
   std::string err = build_plan(s, wa, prop.multiProcessorCount, opt, &h->plan);
   if (!err.empty()) {
     delete h;
@@ -378,7 +380,15 @@ int mbk_debug_taps(mbk_handle* h, float* taps_out) {
   for (int l = 0; l < c.n_layers; ++l) {
     const unsigned long long* lw = words.data() + (size_t)l * h->plan.act.per_layer;
     for (int i = 0; i < c.hidden; ++i) {
-      taps_out[(size_t)(2 * l + 1) * c.hidden + i] = val(lw[h->plan.act.xa + i]);
+      float xa;
+      if (h->plan.fused_attn) {
+        // x_attn is not stored: the layer input plus the heads' partials, summed as the kernel does
+        xa = taps_out[(size_t)(2 * l) * c.hidden + i];
+        for (int s = 0; s < c.n_kv_heads; ++s) xa += val(lw[h->plan.act.ap + (size_t)s * c.hidden + i]);
+      } else {
+        xa = val(lw[h->plan.act.xa + i]);
+      }
+      taps_out[(size_t)(2 * l + 1) * c.hidden + i] = xa;
       taps_out[(size_t)(2 * l + 2) * c.hidden + i] = val(lw[h->plan.act.xm + i]);
     }
   }

@@ -193,6 +193,10 @@ struct InVec {
   const unsigned long long* src2;
   const unsigned long long* src3;
   int n1, n2;
+  // with nterm > 0 every element also adds nterm words terms[t * tstride + e] (the per-KV-head
+  // partial O projections), summed in t order after the base value (poll_sum)
+  const unsigned long long* terms;
+  int nterm, tstride;
 };
 __device__ __forceinline__ const unsigned long long* word_addr(const InVec& v, int e) {
   return e < v.n1 ? v.src + e : (e < v.n1 + v.n2 ? v.src2 + (e - v.n1) : v.src3 + (e - v.n1 - v.n2));
@@ -251,6 +255,86 @@ __device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detai
       const int e = e0 + k * kCT;
       if (e < v.n) {
         float x = __uint_as_float((uint32_t)w[k]);
+        if (v.gain != nullptr) {
+          ss = fmaf(x, x, ss);
+          x *= __uint_as_float(graw[k] << 16);
+        }
+        v.dst[v.xlayout ? xpos(e, v.n) : e] = x;
+      }
+    }
+  }
+  return ss;
+}
+
+// poll_vec for vectors that are sums: element e = base word (or embedding value) + the nterm
+// partial words of e, two elements per thread at a time with every word of both in flight together.
+// The sum is taken in a fixed order (base, then heads in order), so it is deterministic.
+__device__ __forceinline__ float poll_sum(Ctx& c, const InVec& v, unsigned detail) {
+  constexpr int T = 1 + kMaxFusedKvHeads;
+  const int nt = 1 + v.nterm;
+  float ss = 0.f;
+#pragma unroll 1
+  for (int e0 = c.ctid; e0 < v.n; e0 += 2 * kCT) {
+    unsigned long long w[2][T];
+    uint32_t graw[2];
+    unsigned pend = 0u;  // bit k * T + t
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int e = e0 + k * kCT;
+      graw[k] = 0x3f80u;
+#pragma unroll
+      for (int t = 0; t < T; ++t) w[k][t] = 0ull;
+      if (e < v.n) {
+        if (v.src != nullptr) {
+          w[k][0] = ld_word(v.src + e);
+          pend |= 1u << (k * T);
+        } else {
+          w[k][0] = (unsigned long long)((uint32_t)v.emb[e] << 16);
+        }
+#pragma unroll
+        for (int t = 1; t < T; ++t)
+          if (t < nt) {
+            w[k][t] = ld_word(v.terms + (size_t)(t - 1) * v.tstride + e);
+            pend |= 1u << (k * T + t);
+          }
+        if (v.gain != nullptr) graw[k] = v.gain[e];
+      }
+    }
+    unsigned spins = 0u;
+    unsigned long long t0 = 0ull;
+    while (pend != 0u) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+          if (((pend >> (k * T + t)) & 1u) && (unsigned)(w[k][t] >> 32) == c.tag) pend &= ~(1u << (k * T + t));
+      if (pend == 0u) break;
+      if ((++spins & 31u) == 0u && (t0 = wait_check(c.P, c.ctl, t0, c.task_index, detail | (unsigned)e0)) == 0ull) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int t = 0; t < T; ++t)
+            if ((pend >> (k * T + t)) & 1u) w[k][t] = 0ull;
+        break;
+      }
+      if (c.P->poll_backoff_ns) __nanosleep(c.P->poll_backoff_ns);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = e0 + k * kCT;
+        if ((pend >> (k * T)) & 1u) w[k][0] = ld_word(v.src + e);
+#pragma unroll
+        for (int t = 1; t < T; ++t)
+          if ((pend >> (k * T + t)) & 1u) w[k][t] = ld_word(v.terms + (size_t)(t - 1) * v.tstride + e);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int e = e0 + k * kCT;
+      if (e < v.n) {
+        float x = __uint_as_float((uint32_t)w[k][0]);
+#pragma unroll
+        for (int t = 1; t < T; ++t)
+          if (t < nt) x += __uint_as_float((uint32_t)w[k][t]);
         if (v.gain != nullptr) {
           ss = fmaf(x, x, ss);
           x *= __uint_as_float(graw[k] << 16);
@@ -599,9 +683,10 @@ __device__ __forceinline__ float res_row(const float* res, int i, int gpr) {
 // lane owning output elements.  One barrier later the blocks of each head are merged by their
 // log-sum-exp weights.  Writes per query head o (normalised over this split) and (m, l); scores
 // are kept in base-2 units (scaled by log2 e), so m is too.
-__device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
+__device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, float* res) {
   const KernelParams& P = *c.P;
-  const int l = t.layer, kvh = (int)t.row0, sp = (int)t.nrows;
+  const bool wo = (t.flags & TF_WO) != 0;  // fused O projection: KV head in aux, output rows row0..
+  const int l = t.layer, kvh = wo ? (int)t.aux : (int)t.row0, sp = wo ? 0 : (int)t.nrows;
   const int d = P.d, g = P.g, R = P.rows_per_stage, half = d / 2;
   const int dshift = 31 - __clz(d), hshift = dshift - 1;
   const int pos = c.pos;
@@ -638,6 +723,9 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
     v.gain = nullptr;
     v.dst = sq;
     v.xlayout = 0;
+    v.terms = nullptr;
+    v.nterm = 0;
+    v.tstride = 0;
     poll_vec(c, v, 0x200000u);
   }
   compute_sync();
@@ -664,7 +752,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
     cur[i + half] = __bfloat16_as_ushort(k1);
     cur[d + i] = __bfloat16_as_ushort(v0);
     cur[d + i + half] = __bfloat16_as_ushort(v1);
-    if (!aborted(c)) {
+    if (!aborted(c) && (!wo || (t.flags & TF_KV_APPEND))) {  // one task per head appends the row
       __nv_bfloat16* Kc = reinterpret_cast<__nv_bfloat16*>(P.kv) + ((((size_t)l * 2 + 0) * P.nkv + kvh) * P.C + pos) * d;
       __nv_bfloat16* Vc = reinterpret_cast<__nv_bfloat16*>(P.kv) + ((((size_t)l * 2 + 1) * P.nkv + kvh) * P.C + pos) * d;
       Kc[i] = k0;
@@ -792,11 +880,36 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv) {
       num = fmaf(ph[q * istride + tt], f, num);
       den = fmaf(ph[q * istride + d + 1], f, den);
     }
-    st_word(out_o + e, c.tag, num / den);
-    if (tt == 0) {
-      st_word(out_ml + 2 * h, c.tag, M);
-      st_word(out_ml + 2 * h + 1, c.tag, den);
+    if (wo) {
+      res[xpos(e, O)] = num / den;  // this head group's o, input of its Wo columns
+    } else {
+      st_word(out_o + e, c.tag, num / den);
+      if (tt == 0) {
+        st_word(out_ml + 2 * h, c.tag, M);
+        st_word(out_ml + 2 * h + 1, c.tag, den);
+      }
     }
+  }
+  if (!wo) return;
+  // 4. (fused) output rows of this KV head's columns of Wo: partial sums, one word per row
+  compute_sync();
+  const int nvec = O >> 3;
+  const float4* xlo = reinterpret_cast<const float4*>(res);
+  const float4* xhi = reinterpret_cast<const float4*>(res + (O >> 1));
+  const size_t row_bytes = (size_t)O * 2;
+  unsigned long long* out = P.words + t.out_off;
+  int rbase = 0;
+#pragma unroll 1
+  for (uint32_t k0 = 1; k0 < t.nchunks; k0 += kGemvBatch) {
+    const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
+    const BatchRows b = batch_wait(c, nb);
+#pragma unroll 1
+    for (int q = c.warp; q < b.total; q += kComputeWarps) {
+      const float a = warp_sum(dot_row(c, b.row(q, row_bytes), xlo, xhi, nvec));
+      if (c.lane == 0) st_word(out + rbase + q, c.tag, a);
+    }
+    stages_release(c, (unsigned)nb);
+    rbase += b.total;
   }
 }
 
@@ -821,6 +934,9 @@ __device__ __forceinline__ void combine_splits(Ctx& c, int l, float* o, float* m
     v.src2 = v.src3 = nullptr;
     v.n1 = v.n;
     v.n2 = 0;
+    v.terms = nullptr;
+    v.nterm = 0;
+    v.tstride = 0;
     poll_vec(c, v, 0x310000u);
   }
   compute_sync();
@@ -887,6 +1003,9 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
   x.src2 = x.src3 = nullptr;
   x.n1 = x.n;
   x.n2 = 0;
+  x.terms = P.words + t.aux;
+  x.nterm = (f & TF_IN_SUM) ? P.nkv : 0;
+  x.tstride = P.H;
   r.src = (f & TF_RES_EMB) ? nullptr : ((f & TF_RES_LAYER) && layer_in ? layer_in + t.row0 : P.words + t.res_off);
   r.emb = emb_row + t.row0;
   r.gain = nullptr;
@@ -896,6 +1015,9 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
   r.src2 = r.src3 = nullptr;
   r.n1 = r.n;
   r.n2 = 0;
+  r.terms = P.words + t.aux;
+  r.nterm = (f & TF_RES_SUM) ? P.nkv : 0;
+  r.tstride = P.H;
   unsigned long long* out = P.words + t.out_off;
   const int in = (int)t.in_n;
   const bool combine = (f & TF_COMBINE) != 0;  // O projection over several context splits
@@ -929,7 +1051,8 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
     InVec v = x;
     if (j == 1) v = r;
     if (v.n > 0) {
-      const float s = poll_vec(c, v, j == 0 ? 0x100000u : 0x400000u);
+      const unsigned detail = j == 0 ? 0x100000u : 0x400000u;
+      const float s = v.nterm > 0 ? poll_sum(c, v, detail) : poll_vec(c, v, detail);
       if (j == 0) ss = s;
     }
   }
@@ -1084,6 +1207,19 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
               advance();
             }
           }
+        } else if (rows & kStridedRows) {
+          // one KV head's columns of Wo: a segment per output row, packed back to back
+          const unsigned n = rows & ~kStridedRows, seg = bytes / n;
+          const size_t stride = (size_t)P.nq * P.d * 2;
+          unsigned char* dst = acquire(bytes, n);
+          if (!dst) {
+            q = 1;
+          } else {
+            for (unsigned r = 0; r < n; ++r)
+              bulk_load(dst + (size_t)r * seg, reinterpret_cast<const unsigned char*>(src) + r * stride, seg,
+                        &ctl->full[stage], policy);
+            advance();
+          }
         } else {
           unsigned char* dst = acquire(bytes, rows);
           if (!dst) {
@@ -1179,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (P.trace != nullptr && c.ctid == 0) P.trace[(size_t)ti * 4 + 3] = 0;
     trace_mark(c, 0);
     if (t.type == T_ATTN)
-      task_attn(c, t, sv);
+      task_attn(c, t, sv, res);
     else
       task_gemv(c, t, sv, res, add);
     compute_sync();  // the next task reuses the shared vectors

@@ -34,13 +34,21 @@ enum TaskFlags : uint16_t {
   TF_RES_LAYER = 128, // ... taken from the layer's input stream (replaceable by injected words)
   TF_COMBINE = 256,   // the input is the attention output of several context splits
   TF_LOGITS = 512,    // the rows are logits (written to the caller's buffer, not as words)
+  TF_WO = 1024,       // attention task that also applies its KV head's columns of Wo to output rows
+                      // [row0, row0 + nrows) (KV head in aux), writing that head's partial sums
+  TF_KV_APPEND = 2048,// this attention task appends the step's K/V row to the cache
+  TF_IN_SUM = 4096,   // the input adds the per-KV-head attention partials (words aux + s*H + e)
+  TF_RES_SUM = 8192,  // the residual rows add the per-KV-head attention partials (words aux + s*H + r)
 };
 
 // One task of one CTA.  GEMV tasks: output rows [row0, row0 + nrows) of the op's output space
 // (QKV: the concatenation q|k|v; GATEUP: rows of I, results g then u), weights in static chunks
 // [chunk0, chunk0 + nchunks).  ATTN tasks: row0 = KV head, nrows = context split index; their
 // chunks (cached K/V rows) are derived on the device from the step's position; in_off/out_off
-// are the layer's q|k|v and attention-output words.
+// are the layer's q|k|v and attention-output words.  With TF_WO (one context split, few KV heads)
+// the attention task of KV head aux also owns output rows [row0, row0 + nrows) of the O projection
+// restricted to that head's columns: the O projection needs no task and no exchange of its own, and
+// its consumers sum the heads' partials.
 struct Task {
   uint16_t type;
   uint16_t layer;
@@ -56,7 +64,7 @@ struct Task {
   uint32_t res_off; // first residual word (TF_RES, from words)
   uint32_t out_off; // first output word
   uint32_t gain;    // gain table entry (TF_NORM): attn_norm of layer l at 2l, mlp_norm at 2l+1, final at 2L
-  uint32_t pad;
+  uint32_t aux;     // TF_WO: the KV head; TF_IN_SUM / TF_RES_SUM: first word of the attention partials
 };
 static_assert(sizeof(Task) == 48, "Task layout");
 
@@ -70,6 +78,10 @@ struct Chunk {
   uint32_t rows;
 };
 constexpr uint32_t kAttnChunk = 0xFFFFFFFFu;
+// A strided chunk (rows has this bit): rows & ~kStridedRows segments of bytes / rows bytes each,
+// the first at src, the next one O-projection row (n_heads * head_dim bf16) further on, packed
+// back to back in the stage.  Used for a KV head's columns of Wo.
+constexpr uint32_t kStridedRows = 1u << 30;
 static_assert(sizeof(Chunk) == 16, "Chunk layout");
 
 // Offsets (in 8-byte words) of one layer's activation exchange words.
@@ -77,9 +89,10 @@ struct ActLayout {
   uint32_t qkv;       // (nq + 2 nkv) * d   raw projections, pre-RoPE
   uint32_t att;       // nsplit * nq * (d + 2): o [split][head][d] (normalised per split), then
                       // (m, l) [split][head][2] -- the active splits of a step are a prefix of each
-  uint32_t xa;        // H   residual stream after the attention sublayer
+  uint32_t xa;        // H   residual stream after the attention sublayer (unused with TF_WO)
   uint32_t hh;        // I   silu(g) * u
   uint32_t xm;        // H   residual stream after the MLP sublayer (input of the next layer)
+  uint32_t ap;        // nkv * H  per-KV-head partial O projections (TF_WO plans; else empty)
   uint32_t per_layer; // words per layer
 };
 
@@ -102,6 +115,7 @@ static_assert(kGemvXVec % 2 == 0, "the GEMV loads its weights in pairs of vector
 constexpr int kCtlBytes = 4224;        // shared-memory control block (barriers, flags, tables, parameters)
 constexpr int kMaxLayers = 64;
 constexpr int kTaskWindow = 160;      // task records staged in shared memory at a time
+constexpr int kMaxFusedKvHeads = 4;   // the O projection is fused into attention for at most this many KV heads
 
 struct PlanShape {
   int L, H, I, nq, nkv, d, V, C;

@@ -130,8 +130,11 @@ void fill_task_io(const PlanShape& s, const Plan& p, Task& t) {
   const ActLayout& a = p.act;
   const uint32_t l = t.layer, pl = a.per_layer;
   const uint32_t lw = l * pl, prev = l > 0 ? (l - 1) * pl + a.xm : 0;  // this layer's words; its input stream
-  t.flags = 0;
-  t.in_off = t.in_n = t.res_off = t.out_off = t.gain = t.pad = 0;
+  const uint32_t keep_aux = t.type == T_ATTN ? t.aux : 0;  // an attention task's KV head (TF_WO)
+  const uint16_t keep_flags = t.type == T_ATTN ? (uint16_t)(t.flags & (TF_WO | TF_KV_APPEND)) : 0;
+  t.flags = keep_flags;
+  t.in_off = t.in_n = t.res_off = t.out_off = t.gain = 0;
+  t.aux = keep_aux;
   switch (t.type) {
     case T_QKV:
       t.flags = TF_NORM | (l == 0 ? TF_IN_EMB : TF_IN_LAYER) | (s.qkv_bias ? TF_BIAS : 0);
@@ -143,7 +146,7 @@ void fill_task_io(const PlanShape& s, const Plan& p, Task& t) {
     case T_ATTN:
       t.in_off = lw + a.qkv;
       t.in_n = (uint32_t)((s.nq + 2 * s.nkv) * s.d);
-      t.out_off = lw + a.att;
+      t.out_off = (t.flags & TF_WO) ? lw + a.ap + t.aux * (uint32_t)s.H + t.row0 : lw + a.att;
       break;
     case T_OPROJ:
       t.flags = TF_RES | (l == 0 ? TF_RES_EMB : TF_RES_LAYER) | (p.nsplit > 1 ? TF_COMBINE : 0);
@@ -154,7 +157,13 @@ void fill_task_io(const PlanShape& s, const Plan& p, Task& t) {
       break;
     case T_GATEUP:
       t.flags = TF_NORM | TF_PAIRS;
-      t.in_off = lw + a.xa;
+      if (p.fused_attn) {  // x_attn = layer input + the heads' partial O projections
+        t.flags |= TF_IN_SUM | (l == 0 ? TF_IN_EMB : TF_IN_LAYER);
+        t.in_off = prev;
+        t.aux = lw + a.ap;
+      } else {
+        t.in_off = lw + a.xa;
+      }
       t.in_n = (uint32_t)s.H;
       t.gain = 2 * l + 1;
       t.out_off = lw + a.hh + t.row0;
@@ -163,7 +172,13 @@ void fill_task_io(const PlanShape& s, const Plan& p, Task& t) {
       t.flags = TF_RES;
       t.in_off = lw + a.hh;
       t.in_n = (uint32_t)s.I;
-      t.res_off = lw + a.xa + t.row0;
+      if (p.fused_attn) {  // residual rows of x_attn, summed the same way
+        t.flags |= TF_RES_SUM | (l == 0 ? TF_RES_EMB : TF_RES_LAYER);
+        t.res_off = prev + t.row0;
+        t.aux = lw + a.ap + t.row0;
+      } else {
+        t.res_off = lw + a.xa + t.row0;
+      }
       t.out_off = lw + a.xm + t.row0;
       break;
     default:  // LM head
@@ -196,6 +211,10 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   // the split combine keeps (m, l) of every query head and split in the results area
   if (s.nq * p.nsplit * 2 > kResSlots) return "KV capacity too long for the attention split combine";
 
+  // the O projection fused into the attention tasks: one context split and few KV heads (its
+  // consumers sum n_kv + 1 vectors)
+  p.fused_attn = p.nsplit == 1 && s.nkv <= kMaxFusedKvHeads && opt.fuse_attention != 0;
+
   // activation words
   ActLayout a{};
   a.qkv = 0;
@@ -203,7 +222,8 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   a.xa = a.att + (uint32_t)(s.nkv * p.nsplit * g * (s.d + 2));
   a.hh = a.xa + (uint32_t)s.H;
   a.xm = a.hh + (uint32_t)s.I;
-  a.per_layer = a.xm + (uint32_t)s.H;
+  a.ap = a.xm + (uint32_t)s.H;
+  a.per_layer = a.ap + (p.fused_attn ? (uint32_t)(s.nkv * s.H) : 0u);
   p.act = a;
   p.act_words = (uint64_t)a.per_layer * s.L;
 
@@ -273,9 +293,50 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       }
       return v;
     });
+    if (p.fused_attn) {
+      // attention with the O projection: per KV head, its columns of Wo split by output rows over
+      // the CTAs; each task recomputes the head's attention (every task of a head rounds the
+      // appended K/V row identically; the first one writes it to the cache)
+      const int seg = g * s.d * 2;                        // bytes of one row's segment
+      const int rpc = kStageBytes / seg;                  // segments per stage
+      const int per_head = std::max(1, std::min(s.H, std::min(max_tasks, num_ctas) / s.nkv));
+      for (int kvh = 0; kvh < s.nkv; ++kvh) {
+        for (int i = 0; i < per_head; ++i) {
+          const int r0 = (int)((int64_t)s.H * i / per_head), r1 = (int)((int64_t)s.H * (i + 1) / per_head);
+          if (r1 <= r0) continue;
+          int cta = cursor % num_ctas;
+          ++cursor;
+          Task t{};
+          t.type = T_ATTN;
+          t.layer = (uint16_t)l;
+          t.row0 = (uint32_t)r0;
+          t.nrows = (uint32_t)(r1 - r0);
+          t.aux = (uint32_t)kvh;
+          t.flags = (uint16_t)(TF_WO | (i == 0 ? TF_KV_APPEND : 0));
+          t.chunk0 = (uint32_t)cta_chunks[cta].size();
+          Chunk ph;
+          ph.src = ((uint64_t)l << 48) | ((uint64_t)kvh << 32);
+          ph.bytes = 0;
+          ph.rows = kAttnChunk;
+          cta_chunks[cta].push_back(ph);
+          for (int r = r0; r < r1; r += rpc) {
+            const int n = std::min(rpc, r1 - r);
+            Chunk ch;
+            ch.src = W[W_O] + (uint64_t)r * qd * 2 + (uint64_t)kvh * seg;
+            ch.bytes = (uint32_t)(n * seg);
+            ch.rows = (uint32_t)n | kStridedRows;
+            cta_chunks[cta].push_back(ch);
+            cta_bytes[cta] += ch.bytes;
+          }
+          t.nchunks = (uint32_t)(cta_chunks[cta].size() - t.chunk0);
+          t.gpr = 0;
+          cta_tasks[cta].push_back(t);
+        }
+      }
+    }
     std::fill(busy.begin(), busy.end(), 0);
     n_busy = 0;
-    for (int kvh = 0; kvh < s.nkv; ++kvh) {
+    for (int kvh = 0; kvh < s.nkv && !p.fused_attn; ++kvh) {
       for (int sp = 0; sp < p.nsplit; ++sp) {
         int cta = cursor % num_ctas;
         ++cursor;
@@ -296,9 +357,10 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
         cta_tasks[cta].push_back(t);
       }
     }
-    gemv_op(T_OPROJ, l, s.H, 1, qd * 2, [&](int r0, int r1) {
-      return std::vector<Seg>{Seg{W[W_O], qd * 2, r0, r1 - r0}};
-    });
+    if (!p.fused_attn)
+      gemv_op(T_OPROJ, l, s.H, 1, qd * 2, [&](int r0, int r1) {
+        return std::vector<Seg>{Seg{W[W_O], qd * 2, r0, r1 - r0}};
+      });
     gemv_op(T_GATEUP, l, s.I, 2, hb, [&](int r0, int r1) {
       return std::vector<Seg>{Seg{W[W_GATE], hb, r0, r1 - r0}, Seg{W[W_UP], hb, r0, r1 - r0}};
     });
@@ -398,6 +460,13 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
     return s.H * 2;
   };
   for (auto& e : extent) covered[e.first].assign(e.second / row_bytes_of(e.first), 0);
+  // fused plans stream Wo as per-KV-head segments of each row: (row, head) -> count
+  std::map<uint64_t, std::vector<int>> covered_wo;
+  if (p.fused_attn)
+    for (int l = 0; l < s.L; ++l) {
+      covered.erase(w.layers[l][W_O]);
+      covered_wo[w.layers[l][W_O]].assign((size_t)s.H * s.nkv, 0);
+    }
 
   if ((int)p.task_off.size() != p.num_ctas + 1 || (int)p.chunk_off.size() != p.num_ctas + 1) return "offsets size";
   // every CTA's tasks use exactly its chunk range, in order
@@ -422,12 +491,35 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
       last_rank = rk;
       if (t.chunk0 < p.chunk_off[c] || t.chunk0 + t.nchunks > p.chunk_off[c + 1]) return "task chunks outside its CTA";
       if (t.type == T_ATTN) {
-        ++attn_tasks;
-        if (t.nchunks != 1 || (int)t.row0 >= s.nkv || (int)t.nrows >= p.nsplit) return "bad attention task";
         const Chunk& ph = p.chunks[t.chunk0];
-        if (ph.rows != kAttnChunk || (int)(ph.src >> 48) != t.layer || (int)((ph.src >> 32) & 0xFFFF) != (int)t.row0 ||
-            (uint32_t)ph.src != t.nrows)
+        if (!(t.flags & TF_WO)) {
+          ++attn_tasks;
+          if (p.fused_attn || t.nchunks != 1 || (int)t.row0 >= s.nkv || (int)t.nrows >= p.nsplit) return "bad attention task";
+          if (ph.rows != kAttnChunk || (int)(ph.src >> 48) != t.layer || (int)((ph.src >> 32) & 0xFFFF) != (int)t.row0 ||
+              (uint32_t)ph.src != t.nrows)
+            return "bad attention placeholder";
+          continue;
+        }
+        // attention with its KV head's columns of Wo for output rows [row0, row0 + nrows)
+        if (!p.fused_attn || p.nsplit != 1 || (int)t.aux >= s.nkv || t.nrows == 0 || t.row0 + t.nrows > (uint32_t)s.H)
+          return "bad fused attention task";
+        if (t.flags & TF_KV_APPEND) ++attn_tasks;
+        if (ph.rows != kAttnChunk || (int)(ph.src >> 48) != t.layer || (int)((ph.src >> 32) & 0xFFFF) != (int)t.aux ||
+            (uint32_t)ph.src != 0u)
           return "bad attention placeholder";
+        const uint64_t wo = w.layers[t.layer][W_O];
+        const uint32_t seg = (uint32_t)((s.nq / s.nkv) * s.d * 2);
+        uint32_t r = t.row0;
+        for (uint32_t k = t.chunk0 + 1; k < t.chunk0 + t.nchunks; ++k) {
+          const Chunk& ch = p.chunks[k];
+          const uint32_t n = ch.rows & ~kStridedRows;
+          if (!(ch.rows & kStridedRows) || n == 0 || ch.bytes != n * seg || ch.bytes > (uint32_t)kStageBytes || ch.src % 16 ||
+              seg % 16 || ch.src != wo + (uint64_t)r * qd * 2 + (uint64_t)t.aux * seg)
+            return "bad Wo segment chunk";
+          for (uint32_t q = 0; q < n; ++q) covered_wo[wo][(size_t)(r + q) * s.nkv + t.aux] += 1;
+          r += n;
+        }
+        if (r != t.row0 + t.nrows) return "Wo segments do not match the task's rows";
         continue;
       }
       int res = t.type == T_GATEUP ? 2 * (int)t.nrows : (int)t.nrows;
@@ -472,6 +564,9 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
         snprintf(buf, sizeof buf, "weight row %zu of tensor %llx streamed %d times", r, (unsigned long long)cv.first, cv.second[r]);
         return buf;
       }
+  for (auto& cv : covered_wo)
+    for (size_t i = 0; i < cv.second.size(); ++i)
+      if (cv.second[i] != 1) return "a Wo row segment is not streamed exactly once";
   if (attn_tasks != s.L * s.nkv * p.nsplit) return "attention task count";
   if (p.smem_bytes > 232448) return "shared memory over the sm_10x limit";
   // every GEMV output word of every layer is written by exactly one task; all word ranges in bounds
@@ -480,8 +575,15 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
     for (const Task& t : p.tasks) {
       if (t.type == T_ATTN) {
         if ((uint64_t)t.in_off + t.in_n > p.act_words) return "attention input words out of range";
+        if (t.flags & TF_WO) {
+          if ((uint64_t)t.out_off + t.nrows > p.act_words) return "attention partial words out of range";
+          for (uint32_t r = 0; r < t.nrows; ++r) ++cov[t.out_off + r];
+        }
         continue;
       }
+      if ((t.flags & (TF_IN_SUM | TF_RES_SUM)) &&
+          (uint64_t)t.aux + (uint64_t)(s.nkv - 1) * s.H + ((t.flags & TF_IN_SUM) ? (uint64_t)s.H : t.nrows) > p.act_words)
+        return "attention partial words out of range";
       if ((uint64_t)t.in_off + t.in_n > p.act_words) return "task input words out of range";
       if ((t.flags & TF_RES) && !(t.flags & TF_RES_EMB) && (uint64_t)t.res_off + t.nrows > p.act_words)
         return "task residual words out of range";
@@ -497,8 +599,9 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
           if (cov[b + off + i] != 1) return false;
         return true;
       };
-      if (!once(a.qkv, qd + 2 * kvd) || !once(a.xa, s.H) || !once(a.hh, s.I) || !once(a.xm, s.H))
+      if (!once(a.qkv, qd + 2 * kvd) || !once(a.hh, s.I) || !once(a.xm, s.H))
         return "an output word is not written exactly once";
+      if (p.fused_attn ? !once(a.ap, s.nkv * s.H) : !once(a.xa, s.H)) return "an attention output word is not written exactly once";
     }
   }
   return "";

@@ -19,6 +19,7 @@ struct WeightAddrs {
 
 struct PlanOptions {
   int max_tasks_per_op = 0;    // split each projection into at most this many tasks (0: one per CTA)
+  int fuse_attention = -1;     // fold the O projection into the attention tasks: -1 where it applies, 0 never
   int smem_limit = 232448;     // dynamic shared memory available per CTA
 };
 
@@ -30,6 +31,7 @@ struct Plan {
   std::vector<uint32_t> chunk_off;   // [num_ctas + 1] offsets into chunks
   ActLayout act{};
   uint64_t act_words = 0;            // words per step (one parity)
+  bool fused_attn = false;           // attention tasks also apply Wo (TF_WO); no O-projection tasks
   int nsplit = 1;                    // context splits per KV head
   int split_len = 0;                 // positions per split
   int attn_rows_per_stage = 0;       // cached positions per ring stage

@@ -80,6 +80,16 @@ def test_mha_head_dim_128():
     rep.check()
 
 
+@pytest.mark.parametrize("fuse", ["0", "1"])
+def test_o_projection_fused_and_separate(fuse, monkeypatch):
+    """The O projection runs either inside the attention tasks (per-KV-head partial sums) or as tasks
+    of its own; both schedules must meet the parity bars on a GQA shape with one context split."""
+    monkeypatch.setenv("MBK_FUSE_ATTENTION", fuse)
+    shape = workloads.scaled_down(workloads.SHAPES["smollm-135m"], n_layers=4, vocab=8192, steps=12)
+    rep = run_parity(workloads.generate(shape, seed=9))
+    rep.check()
+
+
 def test_bias_small_shape():
     shape = workloads.scaled_down(workloads.SHAPES["qwen2-0.5b"], n_layers=3, vocab=8192, steps=10)
     rep = run_parity(workloads.generate(shape, seed=8))
