@@ -70,6 +70,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
+// L2 prefetch of a global range (no shared-memory destination), kept with the given policy.
+__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -516,46 +526,46 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
       }
       return reinterpret_cast<const uint4*>(base + (size_t)r * row_bytes);
     };
-    // two rows per iteration; the loop bound is uniform across the warp (shuffles below)
-    for (int ra = rstart; ra < total; ra += 2 * rpp) {
-      const int rb = ra + rpp;
-      const bool two = rb < total;
-      const uint4* A = row_of(ra);
-      const uint4* B = row_of(two ? rb : ra);
-      unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
+    // four rows per iteration (independent accumulator chains); the loop bound is uniform across
+    // the warp (shuffles below)
+    for (int ra = rstart; ra < total; ra += 4 * rpp) {
+      const uint4* R[4];
 #pragma unroll
-      for (int k2 = 0; k2 < kGemvXVec; k2 += 2) {
-        uint4 wa4[2], wb4[2];
+      for (int i = 0; i < 4; ++i) R[i] = row_of(ra + i * rpp < total ? ra + i * rpp : ra);
+      unsigned long long acc[4][2];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {  // loads first (clamped index, zeroed weights past the slice)
-          const int v = v0 + c.lane + 32 * (k2 + k);
-          const int vi = v < v1 ? v : 0;
-          wa4[k] = A[vi];
-          wb4[k] = B[vi];
-          if (v >= v1) wa4[k] = wb4[k] = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0ull;
+#pragma unroll
+      for (int k = 0; k < kGemvXVec; ++k) {
+        const int v = v0 + c.lane + 32 * k;
+        const int vi = v < v1 ? v : 0;  // clamped index; its x registers are zero
+        uint4 w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = R[i][vi];
+        if (v >= v1) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const unsigned long long* xk = xp[k2 + k];
-          a0 = ffma2(bf2(wa4[k].x), xk[0], a0);
-          a1 = ffma2(bf2(wa4[k].y), xk[1], a1);
-          a0 = ffma2(bf2(wa4[k].z), xk[2], a0);
-          a1 = ffma2(bf2(wa4[k].w), xk[3], a1);
-          b0 = ffma2(bf2(wb4[k].x), xk[0], b0);
-          b1 = ffma2(bf2(wb4[k].y), xk[1], b1);
-          b0 = ffma2(bf2(wb4[k].z), xk[2], b0);
-          b1 = ffma2(bf2(wb4[k].w), xk[3], b1);
+        for (int i = 0; i < 4; ++i) {
+          acc[i][0] = ffma2(bf2(w[i].x), xp[k][0], acc[i][0]);
+          acc[i][1] = ffma2(bf2(w[i].y), xp[k][1], acc[i][1]);
+          acc[i][0] = ffma2(bf2(w[i].z), xp[k][2], acc[i][0]);
+          acc[i][1] = ffma2(bf2(w[i].w), xp[k][3], acc[i][1]);
         }
       }
-      float sa = sum2(a0) + sum2(a1), sb = sum2(b0) + sum2(b1);
+      float sm[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sm[i] = sum2(acc[i][0]) + sum2(acc[i][1]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        sa += __shfl_xor_sync(0xffffffffu, sa, o);
-        sb += __shfl_xor_sync(0xffffffffu, sb, o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sm[i] += __shfl_xor_sync(0xffffffffu, sm[i], o);
       }
       if (c.lane == 0) {
-        res[((rbase + ra) << gshift) + slice] = sa * scale;
-        if (two) res[((rbase + rb) << gshift) + slice] = sb * scale;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (ra + i * rpp < total) res[((rbase + ra + i * rpp) << gshift) + slice] = sm[i] * scale;
       }
     }
     stages_release(c, (unsigned)nb);
@@ -1167,6 +1177,31 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
     mbar_expect_tx(&ctl->full[stage], bytes);
     return ring + (size_t)stage * kStageBytes;
   };
+  // A few layers before the LM head, the LM head's rows beyond what the ring will hold when it
+  // starts are prefetched into L2: HBM is mostly idle during the layers, and the LM head then
+  // refills the ring from L2 instead of waiting on HBM at the end of the step.
+  uint32_t lm0 = 0xFFFFFFFFu, lm1 = 0;
+  {
+    const uint32_t t0 = P.task_off[blockIdx.x], t1 = P.task_off[blockIdx.x + 1];
+    if (t1 > t0) {
+      const Task last = P.tasks[t1 - 1];
+      if (last.type == T_LMHEAD) {
+        lm0 = last.chunk0;
+        lm1 = last.chunk0 + last.nchunks;
+      }
+    }
+  }
+  bool lm_prefetched = false;
+  auto prefetch_lm_head = [&]() {
+    lm_prefetched = true;
+    const uint64_t keep = evict_last_policy();
+    unsigned bytes = 0;
+    for (uint32_t k = lm0 + ns; k < lm1 && bytes < kLmPrefetchBytes; ++k) {
+      const Chunk ch = P.chunks[k];
+      prefetch_l2(reinterpret_cast<const void*>(ch.src), ch.bytes, keep);
+      bytes += ch.bytes;
+    }
+  };
   auto advance = [&]() {
     if (++stage == ns) {
       stage = 0;
@@ -1186,6 +1221,7 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
       const unsigned rows = __shfl_sync(0xffffffffu, mine.rows, j);
       int q = 0;
       if (lane == 0) {
+        if (!lm_prefetched && lm0 != 0xFFFFFFFFu && base + (uint32_t)j + kLmPrefetchLead >= lm0) prefetch_lm_head();
         if (rows == kAttnChunk) {
           const int layer = (int)(src >> 48), kvh = (int)((src >> 32) & 0xFFFF), sp = (int)(unsigned)src;
           const int a = sp * P.split_len;
