@@ -190,15 +190,28 @@ def run_ours(args, shape_name):
     s = wl.shape
     dec = mbk.Decoder(wl, device=local)
     stream = torch.cuda.current_stream()
-    steps, warm = args.steps, args.warmup
+    # one call decodes `spc` consecutive teacher-forced positions (mbk_decode_steps; 1 = mbk_decode_step)
+    spc = args.steps_per_call if args.steps_per_call > 0 else s.steps
+    if s.steps % spc:
+        raise SystemExit(f"--steps-per-call must divide the workload's {s.steps} positions")
+    steps = (args.steps + spc - 1) // spc * spc
+    warm = (args.warmup + spc - 1) // spc * spc
     toks = [int(wl.tokens[i % s.steps]) for i in range(steps + warm)]
     poss = [s.pos0 + (i % s.steps) for i in range(steps + warm)]
-    out = dec.logits
-    for i in range(warm):
-        dec.step(toks[i], poss[i], out)
+    out = dec.logits if spc == 1 else torch.empty((spc, s.vocab), dtype=torch.float32, device=dec.device)
+
+    def call(i):  # the call that decodes steps i .. i + spc - 1
+        if spc == 1:
+            dec.step(toks[i], poss[i], out)
+        else:
+            dec.steps(toks[i:i + spc], poss[i], out)
+
+    for i in range(0, warm, spc):
+        call(i)
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ncalls = steps // spc
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ncalls)]
     sampler = ClockSampler()
     sampler.start()
     time.sleep(0.3)
@@ -206,10 +219,10 @@ def run_ours(args, shape_name):
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(steps):
-        ev[i][0].record(stream)
-        dec.step(toks[warm + i], poss[warm + i], out)
-        ev[i][1].record(stream)
+    for k in range(ncalls):
+        ev[k][0].record(stream)
+        call(warm + k * spc)
+        ev[k][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -221,19 +234,44 @@ def run_ours(args, shape_name):
     clocks = sampler.stop(bus)
     assert dec.status() == 0, "device-side wait timed out during the benchmark"
     total_ms = max_over_ranks(start.elapsed_time(end), world, torch.device("cuda", local))
-    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) / spc for a, b in ev]  # per decode step
     kernel_avg_ms = statistics.fmean(kern_ms)
 
-    # end to end through the C ABI with host buffers (token from the host, logits to pinned memory)
-    host = torch.empty(s.vocab, dtype=torch.float32, pin_memory=True)
-    e2e_steps = min(steps, 2000)
-    for i in range(min(warm, 8)):
-        mbk.mbk_decode_step_host(dec.handle, toks[i], poss[i], host.data_ptr(), stream.cuda_stream)
+    # the same workload one step per launch (mbk_decode_step), for reference
+    single_tps = None
+    if spc > 1:
+        n1 = min(steps, 1024)
+        for i in range(8):
+            dec.step(toks[i], poss[i], dec.logits)
+        torch.cuda.synchronize()
+        a1, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a1.record(stream)
+        for i in range(n1):
+            dec.step(toks[warm + i], poss[warm + i], dec.logits)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        single_tps = n1 / (a1.elapsed_time(b1) * 1e-3)
+
+    # end to end through the C ABI with host buffers: token ids from the host, every step's logits
+    # back to pinned host memory, the stream synchronised after each call
+    host = torch.empty((spc, s.vocab), dtype=torch.float32, pin_memory=True)
+    e2e_steps = min(steps, 2048 // spc * spc if spc <= 2048 else spc)
+
+    def call_host(i):
+        if spc == 1:
+            rc = mbk.mbk_decode_step_host(dec.handle, toks[i], poss[i], host.data_ptr(), stream.cuda_stream)
+            assert rc == 0, mbk.mbk_error_string(rc)
+        else:
+            dec.steps(toks[i:i + spc], poss[i], out)
+            host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+    for i in range(0, min(warm, 2 * spc), spc):
+        call_host(i)
     barrier(world)
     t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        rc = mbk.mbk_decode_step_host(dec.handle, toks[warm + i], poss[warm + i], host.data_ptr(), stream.cuda_stream)
-        assert rc == 0, mbk.mbk_error_string(rc)
+    for i in range(0, e2e_steps, spc):
+        call_host(warm + i)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, torch.device("cuda", local))
 
     positions = [poss[warm + i] for i in range(steps)]
@@ -259,6 +297,8 @@ def run_ours(args, shape_name):
                        "positions": f"{s.pos0}..{s.pos0 + s.steps - 1} cycling", "kv_capacity": s.kv_capacity,
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "inputs larger than L2 (weights stream evict-first)",
+                       "steps_per_call": spc,
+                       "single_step_tokens_per_s": round(single_tps, 2) if single_tps else None,
                        "vs_baseline_note": "pages' H200 MIG 60-SM number, context only"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
@@ -266,7 +306,7 @@ def run_ours(args, shape_name):
                          "kernel": "mbk::decode_kernel"},
             "e2e": {"value": round(e2e_steps * world / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": s.vocab * 4},
-            "gpu_launches": steps,
+            "gpu_launches": ncalls,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
@@ -309,6 +349,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="smollm-135m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--steps-per-call", type=int, default=0,
+                    help="teacher-forced steps per launch (default: the workload's positions; 1 = one launch per step)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -106,6 +106,20 @@ int mbk_create(const mbk_config *cfg, const mbk_weights *weights, void *kv_cache
  * [0, kv_capacity) or logits_out is NULL; a sticky device error from an earlier step. */
 int mbk_decode_step(mbk_handle *h, int32_t token_id, int32_t position, float *logits_out, void *stream);
 
+/* n_steps consecutive decode steps in ONE launch: token tokens[i] (a HOST array of n_steps ids,
+ * copied before the call returns) at position position + i, logits of step i written to the
+ * DEVICE buffer logits_out + i * vocab (n_steps * vocab floats).  The results are those of n_steps
+ * calls of mbk_decode_step (teacher-forced decoding: the tokens are given, e.g. a prompt or a draft
+ * to verify); one launch saves the per-launch gap, the kernel prologue and the cold start of the
+ * weight stream at every step but the first.  Inside the launch each step's K/V copies wait until
+ * every CTA has finished the step before (the cache rows it appended).  The pages have no
+ * multi-step call; the MegaBake website lists multi-step decoding under "Next".
+ * Errors: MBK_ERR_INVALID_ARG if n_steps < 1, a token is not in [0, vocab), or
+ * [position, position + n_steps) is not inside [0, kv_capacity); MBK_ERR_STATE if a diagnostic
+ * injection is armed (it applies to single steps only); a sticky device error. */
+int mbk_decode_steps(mbk_handle *h, const int32_t *tokens, int32_t n_steps, int32_t position, float *logits_out,
+                     void *stream);
+
 /* As mbk_decode_step, then copies the logits into the HOST buffer logits_host (vocab floats;
  * pinned memory makes the copy asynchronous) and synchronises `stream` before returning. */
 int mbk_decode_step_host(mbk_handle *h, int32_t token_id, int32_t position, float *logits_host, void *stream);

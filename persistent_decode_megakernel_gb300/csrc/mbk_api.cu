@@ -41,6 +41,9 @@ struct mbk_handle {
   unsigned* d_status = nullptr;
   unsigned* h_status = nullptr;  // mapped pinned host memory
   float* d_logits_tmp = nullptr; // for mbk_decode_step_host
+  int32_t* d_tokens = nullptr;    // [kv_capacity] token ids of a multi-step call
+  unsigned long long* d_sync = nullptr;  // inter-step counter of multi-step launches
+  unsigned long long sync_count = 0;     // its value after the last launch
   unsigned long long* d_trace = nullptr;
   unsigned long long* d_inject = nullptr;
   bool inject_armed = false;
@@ -89,6 +92,8 @@ void free_all(mbk_handle* h) {
   cudaFree(h->d_words);
   cudaFree(h->d_status);
   cudaFree(h->d_logits_tmp);
+  cudaFree(h->d_tokens);
+  cudaFree(h->d_sync);
   cudaFree(h->d_trace);
   cudaFree(h->d_inject);
   if (h->h_status) cudaFreeHost(h->h_status);
@@ -237,6 +242,8 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
       ck(cudaMalloc(&h->d_layers, sizeof(LayerW) * s.L)) && ck(cudaMalloc(&h->d_rope, sizeof(float2) * rope_n)) &&
       ck(cudaMalloc(&h->d_words, sizeof(unsigned long long) * p.act_words)) &&
       ck(cudaMalloc(&h->d_status, 16)) && ck(cudaMalloc(&h->d_logits_tmp, sizeof(float) * s.V)) &&
+      ck(cudaMalloc(&h->d_tokens, sizeof(int32_t) * s.C)) && ck(cudaMalloc(&h->d_sync, 8)) &&
+      ck(cudaMemset(h->d_sync, 0, 8)) &&
       ck(cudaHostAlloc(&h->h_status, 16, cudaHostAllocMapped))) {
     ck(cudaMemcpy(h->d_tasks, p.tasks.data(), sizeof(Task) * p.tasks.size(), cudaMemcpyHostToDevice));
     ck(cudaMemcpy(h->d_task_off, p.task_off.data(), sizeof(uint32_t) * p.task_off.size(), cudaMemcpyHostToDevice));
@@ -299,18 +306,22 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   return MBK_OK;
 }
 
-int mbk_decode_step(mbk_handle* h, int32_t token_id, int32_t position, float* logits_out, void* stream) {
-  if (!h || !logits_out) return MBK_ERR_INVALID_ARG;
-  if (token_id < 0 || token_id >= h->cfg.vocab || position < 0 || position >= h->cfg.kv_capacity) return MBK_ERR_INVALID_ARG;
-  if (int st = sticky_status(h)) return st;
-  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+namespace {
+// One launch of n consecutive steps from pos0 (tokens on the device, or `token` when n == 1).
+int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, int32_t pos0, float* logits, void* stream) {
   StepParams sp;
-  sp.token = token_id;
-  sp.pos = position;
-  if (++h->tag == 0) ++h->tag;  // tag 0 marks never-written words
-  sp.tag = h->tag;
-  sp.logits = logits_out;
-  h->last_token = token_id;
+  sp.token = token;
+  sp.pos = pos0;
+  // tags tag+1 .. tag+n; tag 0 marks never-written words, so a range that would wrap restarts at 1
+  if (h->tag + (unsigned)n < h->tag || h->tag + (unsigned)n == 0u) h->tag = 0;
+  sp.tag = h->tag + 1u;
+  h->tag += (unsigned)n;
+  sp.logits = logits;
+  sp.tokens = d_tokens;
+  sp.n = n;
+  sp.sync = n > 1 ? h->d_sync : nullptr;
+  sp.sync_base = h->sync_count;
+  if (n > 1) h->sync_count += (unsigned long long)n * (unsigned long long)h->grid;
   KernelParams kp = h->kp;
   if (h->inject_armed) {
     kp.inject = h->d_inject;  // one step only
@@ -321,6 +332,33 @@ int mbk_decode_step(mbk_handle* h, int32_t token_id, int32_t position, float* lo
                                               (size_t)h->plan.smem_bytes, (cudaStream_t)stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;
+}
+}  // namespace
+
+int mbk_decode_step(mbk_handle* h, int32_t token_id, int32_t position, float* logits_out, void* stream) {
+  if (!h || !logits_out) return MBK_ERR_INVALID_ARG;
+  if (token_id < 0 || token_id >= h->cfg.vocab || position < 0 || position >= h->cfg.kv_capacity) return MBK_ERR_INVALID_ARG;
+  if (int st = sticky_status(h)) return st;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  h->last_token = token_id;
+  return launch_steps(h, token_id, nullptr, 1, position, logits_out, stream);
+}
+
+int mbk_decode_steps(mbk_handle* h, const int32_t* tokens, int32_t n_steps, int32_t position, float* logits_out,
+                     void* stream) {
+  if (!h || !tokens || !logits_out || n_steps < 1) return MBK_ERR_INVALID_ARG;
+  if (position < 0 || n_steps > h->cfg.kv_capacity || position > h->cfg.kv_capacity - n_steps) return MBK_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_steps; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
+  if (h->inject_armed) return MBK_ERR_STATE;  // injection is defined for single steps only
+  if (int st = sticky_status(h)) return st;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  if (cudaMemcpyAsync(h->d_tokens, tokens, sizeof(int32_t) * (size_t)n_steps, cudaMemcpyHostToDevice,
+                      (cudaStream_t)stream) != cudaSuccess)
+    return MBK_ERR_CUDA;
+  h->last_token = tokens[n_steps - 1];
+  if (n_steps == 1) return launch_steps(h, tokens[0], nullptr, 1, position, logits_out, stream);
+  return launch_steps(h, 0, h->d_tokens, n_steps, position, logits_out, stream);
 }
 
 int mbk_decode_step_host(mbk_handle* h, int32_t token_id, int32_t position, float* logits_host, void* stream) {

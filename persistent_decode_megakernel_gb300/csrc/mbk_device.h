@@ -44,11 +44,16 @@ struct KernelParams {
 };
 
 // Changes every step.
+// One launch decodes n consecutive positions pos, pos+1, ... (teacher-forced tokens).
 struct StepParams {
-  int token;
-  int pos;
-  unsigned tag;   // step sequence number (never 0): the tag carried by every word written this step
-  float* logits;  // device fp32 [V]
+  int token;                 // the token when tokens is null (n == 1)
+  int pos;                   // position of the launch's first step
+  unsigned tag;              // tag of the first step (never 0); step i writes its words with tag + i
+  float* logits;             // device fp32 [n][V]
+  const int* tokens;         // device [n], or null
+  int n;                     // steps in this launch
+  unsigned long long* sync;  // step counter: every CTA adds 1 after each step (null when n == 1)
+  unsigned long long sync_base;  // its value when the launch starts
 };
 
 }  // namespace mbk

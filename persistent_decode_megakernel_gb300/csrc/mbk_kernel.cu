@@ -1144,8 +1144,32 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
 // ------------------------------------------------------------------ producer warp
 // Walks the CTA's chunk list (32 descriptors per coalesced load, the next batch loaded while the
 // current one is issued) and fills the ring.  Lane 0 issues; the other lanes only help load.
-__device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl, unsigned char* ring, uint32_t c0,
-                                        uint32_t c1, int lane) {
+// Producer of a multi-step launch, before the first K/V copy of step `step` >= 1: waits until every CTA
+// has finished the previous step (so the cache rows it appended are visible), then orders those
+// generic-proxy writes before this warp's bulk copies.  Bounded; false if the wait gave up.
+__device__ __noinline__ bool wait_prev_step(const unsigned long long* sync, unsigned long long target, int step,
+                                            const KernelParams* P, Ctl* ctl) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(sync) : "memory");
+    if (v >= target) break;
+    if (*(volatile unsigned*)P->status != 0u || global_ns() - t0 > 4 * P->timeout_ns) {
+      if (atomicCAS(&P->status[0], 0u, (unsigned)DS_TIMEOUT) == 0u) {
+        P->status[1] = blockIdx.x;
+        P->status[3] = 0xD000u | (unsigned)step;
+      }
+      *(volatile unsigned*)&ctl->prod_quit = 1u;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+__device__ __forceinline__ void produce(const KernelParams& P, const StepParams& S, Ctl* ctl, unsigned char* ring,
+                                        uint32_t c0, uint32_t c1, int lane) {
   const uint64_t policy = evict_first_policy();
   const unsigned ns = (unsigned)P.num_stages;
   unsigned stage = 0, uses = 0;  // ring slot and how many times the ring has wrapped
@@ -1208,6 +1232,10 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
       ++uses;
     }
   };
+  for (int step = 0; step < S.n && !quit; ++step) {
+  const int pos = S.pos + step;
+  bool synced = step == 0;  // the cache rows of earlier steps are visible to this step's copies
+  lm_prefetched = false;
   Chunk next{};
   if (c0 + lane < c1) next = P.chunks[c0 + lane];
   for (uint32_t base = c0; base < c1 && !quit; base += 32) {
@@ -1222,7 +1250,12 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
       int q = 0;
       if (lane == 0) {
         if (!lm_prefetched && lm0 != 0xFFFFFFFFu && base + (uint32_t)j + kLmPrefetchLead >= lm0) prefetch_lm_head();
-        if (rows == kAttnChunk) {
+        if (rows == kAttnChunk && !synced) {
+          synced = true;
+          if (!wait_prev_step(S.sync, S.sync_base + (unsigned long long)step * gridDim.x, step, &P, ctl)) q = 1;
+        }
+        if (q) {
+        } else if (rows == kAttnChunk) {
           const int layer = (int)(src >> 48), kvh = (int)((src >> 32) & 0xFFFF), sp = (int)(unsigned)src;
           const int a = sp * P.split_len;
           if (a <= pos) {
@@ -1269,6 +1302,7 @@ __device__ __forceinline__ void produce(const KernelParams& P, int pos, Ctl* ctl
       quit = __shfl_sync(0xffffffffu, q, 0) != 0;
     }
   }
+  }
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -1280,7 +1314,7 @@ __device__ __forceinline__ void stage_tasks(const Task* src, Task* dst, int n, i
   for (int i = tid; i < n16; i += nt) d4[i] = s4[i];
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const StepParams S) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const __grid_constant__ StepParams S) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
   if (threadIdx.x == 0) {
@@ -1318,17 +1352,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   unsigned char* ring = smem + P.off_ring;
   const int warp = threadIdx.x / 32;
   if (warp == 0) {
-    produce(ctl->params, S.pos, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31);
+    produce(ctl->params, S, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31);
     return;
   }
   Ctx c;
   c.P = &ctl->params;
   c.ctl = ctl;
   c.ring = ring;
-  c.logits = S.logits;
-  c.tag = S.tag;
-  c.pos = S.pos;
-  c.token = S.token;
+
   c.ns = (unsigned)P.num_stages;
   c.stage = 0;
   c.phase = 0;
@@ -1338,6 +1369,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   float* sv = reinterpret_cast<float*>(smem + P.off_sv);
   float* res = reinterpret_cast<float*>(smem + P.off_res);
   float* add = reinterpret_cast<float*>(smem + P.off_resid);
+#pragma unroll 1
+  for (int step = 0; step < S.n; ++step) {
+  c.tag = S.tag + (unsigned)step;
+  c.pos = S.pos + step;
+  c.token = S.tokens != nullptr ? S.tokens[step] : S.token;
+  c.logits = S.logits + (size_t)step * P.V;
+  if (step > 0) {
+    // every compute warp is past the previous step's last task: this step's RoPE row, and the first
+    // window of task records again if the CTA has more than one
+    for (int i = c.ctid; i < P.d / 2; i += kCT) ctl->rope[i] = P.rope[(size_t)c.pos * (P.d / 2) + i];
+    if (t1 - t0 > (uint32_t)kTaskWindow) stage_tasks(P.tasks + t0, tasks, kTaskWindow, c.ctid, kCT);
+    compute_sync();
+  }
 #pragma unroll 1
   for (uint32_t ti = t0; ti < t1; ++ti) {
     const uint32_t k = ti - t0;
@@ -1356,6 +1400,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       task_gemv(c, t, sv, res, add);
     compute_sync();  // the next task reuses the shared vectors
     trace_mark(c, 2);
+  }
+  // this CTA is done with the step: publish it (with the cache rows its tasks appended) to the
+  // producers that copy those rows in the next step
+  if (S.sync != nullptr && c.ctid == 0) {
+    __threadfence();
+    atomicAdd(S.sync, 1ull);
+  }
   }
 }
 

@@ -215,6 +215,10 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
   sp.pos = position;
   sp.tag = 1u;
   sp.logits = logits_out;
+  sp.tokens = nullptr;
+  sp.n = 1;
+  sp.sync = nullptr;
+  sp.sync_base = 0;
   KernelParams kp = D.kp;
   void* args[] = {&kp, &sp};
   cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(), dim3(D.plan.num_ctas), dim3(kThreads), args,

@@ -27,7 +27,7 @@ MBK_ERR_STATE = -6
 
 EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
-            "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static")
+            "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -84,6 +84,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_create.restype = ctypes.c_int
         lib.mbk_decode_step.argtypes = [vp, i32, i32, vp, vp]
         lib.mbk_decode_step.restype = ctypes.c_int
+        lib.mbk_decode_steps.argtypes = [vp, vp, i32, i32, vp, vp]
+        lib.mbk_decode_steps.restype = ctypes.c_int
         lib.mbk_decode_step_host.argtypes = [vp, i32, i32, vp, vp]
         lib.mbk_decode_step_host.restype = ctypes.c_int
         lib.mbk_kv_fill.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, vp]
@@ -144,6 +146,14 @@ def mbk_create(cfg: MbkConfig, weights: MbkWeights, kv_cache_ptr: int, device: i
 def mbk_decode_step(h, token_id: int, position: int, logits_ptr: int, stream_ptr: int) -> int:
     return load_library().mbk_decode_step(h, int(token_id), int(position), ctypes.c_void_p(logits_ptr),
                                           ctypes.c_void_p(stream_ptr))
+
+
+def mbk_decode_steps(h, tokens, position: int, logits_ptr: int, stream_ptr: int) -> int:
+    """tokens: a sequence of token ids (copied into a host int32 array here)."""
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    return load_library().mbk_decode_steps(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), int(position),
+                                           ctypes.c_void_p(logits_ptr), ctypes.c_void_p(stream_ptr))
 
 
 def mbk_decode_step_host(h, token_id: int, position: int, logits_host_ptr: int, stream_ptr: int) -> int:
@@ -261,6 +271,14 @@ class Decoder:
         out = self.logits if logits is None else logits
         stream = self.torch.cuda.current_stream(self.device).cuda_stream
         _check(mbk_decode_step(self.handle, token, pos, out.data_ptr(), stream), "mbk_decode_step")
+        return out
+
+    def steps(self, tokens, pos0: int, logits=None):
+        """Teacher-forced decode of len(tokens) positions from pos0 in one launch; logits [n, vocab]."""
+        n = len(tokens)
+        out = self.torch.empty((n, self.shape.vocab), dtype=self.torch.float32, device=self.device) if logits is None else logits
+        stream = self.torch.cuda.current_stream(self.device).cuda_stream
+        _check(mbk_decode_steps(self.handle, tokens, pos0, out.data_ptr(), stream), "mbk_decode_steps")
         return out
 
     def status(self) -> int:

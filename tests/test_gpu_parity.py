@@ -187,3 +187,47 @@ def test_wait_timeout_is_reported_and_sticky(monkeypatch):
     d.close()
     rep = run_parity(wl, steps=4)
     rep.check()
+
+
+@pytest.mark.parametrize("shape,n", [("tiny", 24), ("smollm-135m", 12), ("ragged-split", 10)])
+def test_multi_step_call_matches_single_steps(shape, n):
+    """mbk_decode_steps decodes n teacher-forced positions in one launch; its logits and cache rows
+    must equal those of n single-step calls bit for bit (same kernel, same order of operations).
+    The split-context shape also checks that each step's K/V copies see the rows the step before
+    appended inside the same launch."""
+    from persistent_decode_megakernel_gb300.mbk import Decoder
+    if shape == "ragged-split":  # several context splits; steps cross the split boundary at 1024
+        s = workloads.scaled_down(workloads.SHAPES["smollm-135m-long"], n_layers=3, vocab=4096, kv_capacity=1500,
+                                  steps=n, pos0=1020, prefill=1020)
+        wl = workloads.generate(s, seed=3)
+    else:
+        wl = workloads.generate(shape, seed=0)
+    s = wl.shape
+    a = Decoder(wl)  # prefilled caches (if any) are loaded at construction
+    b = Decoder(wl)
+    toks = [int(x) for x in wl.tokens[:n]]
+    singles = torch.stack([a.step(toks[i], s.pos0 + i).clone() for i in range(n)])
+    multi = b.steps(toks, s.pos0)
+    torch.cuda.synchronize()
+    assert a.status() == 0 and b.status() == 0
+    assert torch.equal(singles, multi)
+    assert torch.equal(a.kv, b.kv)
+    a.close()
+    b.close()
+
+
+def test_multi_step_call_rejects_bad_arguments():
+    from persistent_decode_megakernel_gb300 import mbk
+    wl = workloads.generate("tiny", seed=0)
+    d = mbk.Decoder(wl)
+    out = torch.empty((4, wl.shape.vocab), dtype=torch.float32, device=d.device)
+    stream = torch.cuda.current_stream().cuda_stream
+    C, V = wl.shape.kv_capacity, wl.shape.vocab
+    assert mbk.mbk_decode_steps(d.handle, [], 0, out.data_ptr(), stream) == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_decode_steps(d.handle, [1, 2, 3, 4], C - 3, out.data_ptr(), stream) == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_decode_steps(d.handle, [1, V, 3, 4], 0, out.data_ptr(), stream) == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_decode_steps(d.handle, [1, 2, 3, 4], -1, out.data_ptr(), stream) == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_decode_steps(d.handle, [1, 2, 3, 4], C - 4, out.data_ptr(), stream) == mbk.MBK_OK
+    torch.cuda.synchronize()
+    assert d.status() == 0
+    d.close()
