@@ -715,7 +715,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   float* kc = sq + O;                         // [d]     current K (raw)
   float* vc = kc + d;                         // [d]     current V (raw)
   uint16_t* cur = reinterpret_cast<uint16_t*>(vc + d);  // [2][d] bf16: the rotated K, V row appended
-  float* pw = vc + 2 * d;                     // [items][d + 2]  per-item o, m, l
+  float* pw = vc + 2 * d;                     // [items][d + 4]  per-item o, m, l (16-byte aligned items)
   const float2* cs = c.ctl->rope;             // this step's cos/sin (loaded at kernel start)
 
   // 1. the packed queries and (owner) the current K/V row, in one poll: they land in sq|kc|vc
@@ -857,7 +857,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
         a3 = fmaf(pj, bf16_hi(v23), a3);
       }
     }
-    float* pi = pw + it * (d + 2);
+    float* pi = pw + it * (d + 4);
     pi[2 * c.lane] = a0;
     pi[2 * c.lane + 1] = a1;
     if (d > 64) {
@@ -872,15 +872,87 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   stages_release(c, (unsigned)nst);
   compute_sync();
 
+  const int istride = g * (d + 4);  // items of one head are g apart
+  if (wo) {
+    // 3'. (fused) output rows of this KV head's columns of Wo.  Each lane owns the 8-element groups
+    // v = lane (+32) of o and merges them itself from the items (o = sum_b o_b 2^(m_b - M) /
+    // sum_b l_b 2^(m_b - M), M = max_b m_b): no merge pass and no barrier before the dot products.
+    const int nvec = O >> 3;  // <= 64 for fused plans
+    float ov[2][8];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int v = c.lane + 32 * k;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ov[k][j] = 0.f;
+      if (v < nvec) {
+        const int e0 = v << 3, h = e0 >> dshift, tt = e0 & (d - 1);
+        const float* ph = pw + h * (d + 4);
+        float M = -INFINITY;
+        for (int q = 0; q < nblk; ++q) M = fmaxf(M, ph[q * istride + d]);
+        float den = 0.f;
+#pragma unroll 1
+        for (int q = 0; q < nblk; ++q) {
+          const float* pq = ph + q * istride;
+          const float f = exp2f(pq[d] - M);
+          den = fmaf(pq[d + 1], f, den);
+          const float4 o0 = *reinterpret_cast<const float4*>(pq + tt);
+          const float4 o1 = *reinterpret_cast<const float4*>(pq + tt + 4);
+          ov[k][0] = fmaf(o0.x, f, ov[k][0]);
+          ov[k][1] = fmaf(o0.y, f, ov[k][1]);
+          ov[k][2] = fmaf(o0.z, f, ov[k][2]);
+          ov[k][3] = fmaf(o0.w, f, ov[k][3]);
+          ov[k][4] = fmaf(o1.x, f, ov[k][4]);
+          ov[k][5] = fmaf(o1.y, f, ov[k][5]);
+          ov[k][6] = fmaf(o1.z, f, ov[k][6]);
+          ov[k][7] = fmaf(o1.w, f, ov[k][7]);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ov[k][j] = ov[k][j] / den;
+      }
+    }
+    const size_t row_bytes = (size_t)O * 2;
+    unsigned long long* out = P.words + t.out_off;
+    int rbase = 0;
+#pragma unroll 1
+    for (uint32_t k0 = 1; k0 < t.nchunks; k0 += kGemvBatch) {
+      const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
+      const BatchRows b = batch_wait(c, nb);
+#pragma unroll 1
+      for (int q = c.warp; q < b.total; q += kComputeWarps) {
+        const uint4* row = b.row(q, row_bytes);
+        float a = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int v = c.lane + 32 * k;
+          if (v < nvec) {
+            const uint4 w = row[v];
+            a = fmaf(bf16_lo(w.x), ov[k][0], a);
+            a = fmaf(bf16_hi(w.x), ov[k][1], a);
+            a = fmaf(bf16_lo(w.y), ov[k][2], a);
+            a = fmaf(bf16_hi(w.y), ov[k][3], a);
+            a = fmaf(bf16_lo(w.z), ov[k][4], a);
+            a = fmaf(bf16_hi(w.z), ov[k][5], a);
+            a = fmaf(bf16_lo(w.w), ov[k][6], a);
+            a = fmaf(bf16_hi(w.w), ov[k][7], a);
+          }
+        }
+        a = warp_sum(a);
+        if (c.lane == 0) st_word(out + rbase + q, c.tag, a);
+      }
+      stages_release(c, (unsigned)nb);
+      rbase += b.total;
+    }
+    return;
+  }
+
   // 3. merge the blocks of each head: o = sum_b o_b 2^(m_b - M) / sum_b l_b 2^(m_b - M)
   const int hq0 = kvh * g;  // first query head of the task
   unsigned long long* out_o = layer_words(P, l) + P.act.att + ((size_t)sp * P.nq + hq0) * d;
   unsigned long long* out_ml = layer_words(P, l) + P.act.att + (size_t)P.nsplit * P.nq * d + ((size_t)sp * P.nq + hq0) * 2;
-  const int istride = g * (d + 2);  // items of one head are g apart
 #pragma unroll 1
   for (int e = c.ctid; e < O; e += kCT) {
     const int h = e >> dshift, tt = e & (d - 1);
-    const float* ph = pw + h * (d + 2);
+    const float* ph = pw + h * (d + 4);
     float M = -INFINITY;
     for (int q = 0; q < nblk; ++q) M = fmaxf(M, ph[q * istride + d]);
     float num = 0.f, den = 0.f;
@@ -890,36 +962,11 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
       num = fmaf(ph[q * istride + tt], f, num);
       den = fmaf(ph[q * istride + d + 1], f, den);
     }
-    if (wo) {
-      res[xpos(e, O)] = num / den;  // this head group's o, input of its Wo columns
-    } else {
-      st_word(out_o + e, c.tag, num / den);
-      if (tt == 0) {
-        st_word(out_ml + 2 * h, c.tag, M);
-        st_word(out_ml + 2 * h + 1, c.tag, den);
-      }
+    st_word(out_o + e, c.tag, num / den);
+    if (tt == 0) {
+      st_word(out_ml + 2 * h, c.tag, M);
+      st_word(out_ml + 2 * h + 1, c.tag, den);
     }
-  }
-  if (!wo) return;
-  // 4. (fused) output rows of this KV head's columns of Wo: partial sums, one word per row
-  compute_sync();
-  const int nvec = O >> 3;
-  const float4* xlo = reinterpret_cast<const float4*>(res);
-  const float4* xhi = reinterpret_cast<const float4*>(res + (O >> 1));
-  const size_t row_bytes = (size_t)O * 2;
-  unsigned long long* out = P.words + t.out_off;
-  int rbase = 0;
-#pragma unroll 1
-  for (uint32_t k0 = 1; k0 < t.nchunks; k0 += kGemvBatch) {
-    const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
-    const BatchRows b = batch_wait(c, nb);
-#pragma unroll 1
-    for (int q = c.warp; q < b.total; q += kComputeWarps) {
-      const float a = warp_sum(dot_row(c, b.row(q, row_bytes), xlo, xhi, nvec));
-      if (c.lane == 0) st_word(out + rbase + q, c.tag, a);
-    }
-    stages_release(c, (unsigned)nb);
-    rbase += b.total;
   }
 }
 

@@ -213,7 +213,8 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
 
   // the O projection fused into the attention tasks: one context split and few KV heads (its
   // consumers sum n_kv + 1 vectors)
-  p.fused_attn = p.nsplit == 1 && s.nkv <= kMaxFusedKvHeads && opt.fuse_attention != 0;
+  p.fused_attn = p.nsplit == 1 && s.nkv <= kMaxFusedKvHeads && (s.nq / s.nkv) * s.d <= kMaxFusedGroupWidth &&
+                 opt.fuse_attention != 0;
 
   // activation words
   ActLayout a{};
@@ -232,7 +233,7 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   // attention: rotated queries, current K/V (raw, then the bf16 row appended) and the partial
   // output (o, m, l) of every (32-position block, query head) item of a split
   const int attn_items = (p.split_len + 31) / 32 * g;
-  int attn_floats = O + 3 * s.d + attn_items * (s.d + 2);
+  int attn_floats = O + 3 * s.d + attn_items * (s.d + 4);
   p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
   p.sv_floats = (p.sv_floats + 31) / 32 * 32;
 
