@@ -574,16 +574,17 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
   compute_sync();
 }
 
+constexpr int kDotRound = 2;  // 16-byte vectors per lane per round of a row dot product
 // Loads of one round are issued unconditionally (an index past the row end is clamped to the row
 // start and its weights zeroed), so they are all in flight before the first FMA.
 __device__ __forceinline__ float dot_row(const Ctx& c, const uint4* row, const float4* xlo, const float4* xhi, int nvec) {
   unsigned long long a0 = 0ull, a1 = 0ull;
 #pragma unroll 1
-  for (int v0 = c.lane; v0 < nvec; v0 += 128) {
-    uint4 w[4];
-    float4 p[4], q[4];
+  for (int v0 = c.lane; v0 < nvec; v0 += 32 * kDotRound) {
+    uint4 w[kDotRound];
+    float4 p[kDotRound], q[kDotRound];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
+    for (int it = 0; it < kDotRound; ++it) {
       const int v = v0 + 32 * it;
       const int vi = v < nvec ? v : v0;
       w[it] = row[vi];
@@ -592,7 +593,7 @@ __device__ __forceinline__ float dot_row(const Ctx& c, const uint4* row, const f
       if (v >= nvec) w[it] = make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
+    for (int it = 0; it < kDotRound; ++it) {
       a0 = ffma2(bf2(w[it].x), pack2(__float_as_uint(p[it].x), __float_as_uint(p[it].y)), a0);
       a1 = ffma2(bf2(w[it].y), pack2(__float_as_uint(p[it].z), __float_as_uint(p[it].w)), a1);
       a0 = ffma2(bf2(w[it].z), pack2(__float_as_uint(q[it].x), __float_as_uint(q[it].y)), a0);
