@@ -302,7 +302,8 @@ def run_ours(args, shape_name):
                        "vs_baseline_note": "pages' H200 MIG 60-SM number, context only"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": round(algo), "kernel_avg_us": round(kernel_avg_ms * 1e3, 3),
+                         "algorithmic_bytes_per_step": round(algo), "kernel_avg_us_per_step": round(kernel_avg_ms * 1e3, 3),
+                         "per": "decode step (a launch of n steps moves n times the bytes in n times the time)",
                          "kernel": "mbk::decode_kernel"},
             "e2e": {"value": round(e2e_steps * world / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": s.vocab * 4},
