@@ -907,8 +907,9 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
           ov[k][6] = fmaf(o1.z, f, ov[k][6]);
           ov[k][7] = fmaf(o1.w, f, ov[k][7]);
         }
+        const float inv = 1.f / den;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ov[k][j] = ov[k][j] / den;
+        for (int j = 0; j < 8; ++j) ov[k][j] *= inv;
       }
     }
     const size_t row_bytes = (size_t)O * 2;
