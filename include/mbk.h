@@ -120,6 +120,20 @@ int mbk_decode_step(mbk_handle *h, int32_t token_id, int32_t position, float *lo
 int mbk_decode_steps(mbk_handle *h, const int32_t *tokens, int32_t n_steps, int32_t position, float *logits_out,
                      void *stream);
 
+/* Greedy decoding of n_steps tokens in ONE launch: step 0 decodes first_token at `position`, and
+ * step i >= 1 decodes, at position + i, the argmax of step i - 1's logits (the lowest index among
+ * equal values).  tokens_out: DEVICE int32[n_steps]; tokens_out[i] is the argmax of step i's logits,
+ * so tokens_out[n_steps - 1] is the token that would come next.  logits_out: DEVICE buffer of
+ * n_steps * vocab floats, or NULL when only the tokens are wanted.  The argmax is taken on the
+ * device at the end of each step (every LM-head task adds its largest logit by a 64-bit atomic
+ * max), and the next step's embedding waits for it, so no host round trip separates the steps.
+ * The pages list multi-step decoding under "Next" (MegaBake website); the feedback of the argmax
+ * is the plain greedy reading.  Errors: MBK_ERR_INVALID_ARG if tokens_out is NULL, n_steps < 1,
+ * first_token is not in [0, vocab) or [position, position + n_steps) is not inside
+ * [0, kv_capacity); MBK_ERR_STATE if a diagnostic injection is armed; a sticky device error. */
+int mbk_decode_greedy(mbk_handle *h, int32_t first_token, int32_t n_steps, int32_t position, int32_t *tokens_out,
+                      float *logits_out, void *stream);
+
 /* As mbk_decode_step, then copies the logits into the HOST buffer logits_host (vocab floats;
  * pinned memory makes the copy asynchronous) and synchronises `stream` before returning. */
 int mbk_decode_step_host(mbk_handle *h, int32_t token_id, int32_t position, float *logits_host, void *stream);

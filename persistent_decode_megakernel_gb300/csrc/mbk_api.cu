@@ -15,7 +15,7 @@
 #include "mbk_sched.h"
 
 namespace mbk {
-const void* decode_kernel_ptr();
+const void* decode_kernel_ptr(bool greedy);
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
 cudaError_t launch_kv_fill(uint16_t* kv_layer, const float* k_raw, const float* v_raw, const float2* rope, int nkv, int C,
                            int d, int p0, int n, cudaStream_t st);
@@ -44,6 +44,9 @@ struct mbk_handle {
   int32_t* d_tokens = nullptr;    // [kv_capacity] token ids of a multi-step call
   unsigned long long* d_sync = nullptr;  // inter-step counter of multi-step launches
   unsigned long long sync_count = 0;     // its value after the last launch
+  unsigned long long* d_amax = nullptr;  // [kv_capacity] greedy decoding: argmax key of each step
+  unsigned* d_amax_done = nullptr;       // [kv_capacity] ... and the LM-head tasks that contributed
+  unsigned long long* d_tokword = nullptr;  // ... and the argmax as a tagged word for the next step
   unsigned long long* d_trace = nullptr;
   unsigned long long* d_inject = nullptr;
   bool inject_armed = false;
@@ -54,6 +57,12 @@ struct mbk_handle {
 namespace {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int lm_task_count(const Plan& p) {
+  int n = 0;
+  for (const Task& t : p.tasks) n += t.type == T_LMHEAD ? 1 : 0;
+  return n;
+}
 
 PlanShape shape_of(const mbk_config& c) {
   PlanShape s;
@@ -94,6 +103,9 @@ void free_all(mbk_handle* h) {
   cudaFree(h->d_logits_tmp);
   cudaFree(h->d_tokens);
   cudaFree(h->d_sync);
+  cudaFree(h->d_amax);
+  cudaFree(h->d_amax_done);
+  cudaFree(h->d_tokword);
   cudaFree(h->d_trace);
   cudaFree(h->d_inject);
   if (h->h_status) cudaFreeHost(h->h_status);
@@ -215,15 +227,17 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   const Plan& p = h->plan;
   h->grid = p.num_ctas;
 
-  const void* kfn = decode_kernel_ptr();
-  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess) {
-    delete h;
-    return MBK_ERR_CUDA;
-  }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, p.smem_bytes) != cudaSuccess || per_sm < 1) {
-    delete h;
-    return MBK_ERR_UNSUPPORTED;
+  for (bool greedy : {false, true}) {  // the teacher-forced and the greedy instantiation
+    const void* kfn = decode_kernel_ptr(greedy);
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess) {
+      delete h;
+      return MBK_ERR_CUDA;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, p.smem_bytes) != cudaSuccess || per_sm < 1) {
+      delete h;
+      return MBK_ERR_UNSUPPORTED;
+    }
   }
 
   int rc = MBK_OK;
@@ -243,6 +257,8 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
       ck(cudaMalloc(&h->d_words, sizeof(unsigned long long) * p.act_words)) &&
       ck(cudaMalloc(&h->d_status, 16)) && ck(cudaMalloc(&h->d_logits_tmp, sizeof(float) * s.V)) &&
       ck(cudaMalloc(&h->d_tokens, sizeof(int32_t) * s.C)) && ck(cudaMalloc(&h->d_sync, 8)) &&
+      ck(cudaMalloc(&h->d_amax, sizeof(unsigned long long) * s.C)) && ck(cudaMalloc(&h->d_amax_done, sizeof(unsigned) * s.C)) &&
+      ck(cudaMalloc(&h->d_tokword, 8)) && ck(cudaMemset(h->d_tokword, 0, 8)) &&
       ck(cudaMemset(h->d_sync, 0, 8)) &&
       ck(cudaHostAlloc(&h->h_status, 16, cudaHostAllocMapped))) {
     ck(cudaMemcpy(h->d_tasks, p.tasks.data(), sizeof(Task) * p.tasks.size(), cudaMemcpyHostToDevice));
@@ -302,21 +318,36 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   kp.host_status = h_status_dev;
   kp.timeout_ns = (unsigned long long)env_int("MBK_WAIT_TIMEOUT_MS", 1000) * 1000000ull;
   kp.poll_backoff_ns = (unsigned)std::max(0, env_int("MBK_POLL_BACKOFF_NS", 0));
+  kp.lm_tasks = lm_task_count(p);
   *out = h;
   return MBK_OK;
 }
 
 namespace {
 // One launch of n consecutive steps from pos0 (tokens on the device, or `token` when n == 1).
-int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, int32_t pos0, float* logits, void* stream) {
+int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, int32_t pos0, float* logits, void* stream,
+                 int32_t* greedy_out = nullptr) {
   StepParams sp;
+  sp.greedy = greedy_out != nullptr;
+  sp.amax = h->d_amax;
+  sp.amax_done = h->d_amax_done;
+  sp.out_tokens = greedy_out;
+  sp.tokword = h->d_tokword;
+  if (sp.greedy) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(h->d_amax, 0, sizeof(unsigned long long) * (size_t)n, st) != cudaSuccess ||
+        cudaMemsetAsync(h->d_amax_done, 0, sizeof(unsigned) * (size_t)n, st) != cudaSuccess)
+      return MBK_ERR_CUDA;
+  }
   sp.token = token;
   sp.pos = pos0;
   // tags tag+1 .. tag+n; tag 0 marks never-written words, so a range that would wrap restarts at 1
   if (h->tag + (unsigned)n < h->tag || h->tag + (unsigned)n == 0u) h->tag = 0;
   sp.tag = h->tag + 1u;
   h->tag += (unsigned)n;
-  sp.logits = logits;
+  // greedy decoding without caller logits: every step's logits go to one internal [V] buffer
+  sp.logits = logits != nullptr ? logits : h->d_logits_tmp;
+  sp.logits_step = logits != nullptr ? h->cfg.vocab : 0;
   sp.tokens = d_tokens;
   sp.n = n;
   sp.sync = n > 1 ? h->d_sync : nullptr;
@@ -328,7 +359,7 @@ int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, i
     h->inject_armed = false;
   }
   void* args[] = {&kp, &sp};
-  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(), dim3(h->grid), dim3(kThreads), args,
+  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(sp.greedy != 0), dim3(h->grid), dim3(kThreads), args,
                                               (size_t)h->plan.smem_bytes, (cudaStream_t)stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;
@@ -359,6 +390,18 @@ int mbk_decode_steps(mbk_handle* h, const int32_t* tokens, int32_t n_steps, int3
   h->last_token = tokens[n_steps - 1];
   if (n_steps == 1) return launch_steps(h, tokens[0], nullptr, 1, position, logits_out, stream);
   return launch_steps(h, 0, h->d_tokens, n_steps, position, logits_out, stream);
+}
+
+int mbk_decode_greedy(mbk_handle* h, int32_t first_token, int32_t n_steps, int32_t position, int32_t* tokens_out,
+                      float* logits_out, void* stream) {
+  if (!h || !tokens_out || n_steps < 1) return MBK_ERR_INVALID_ARG;
+  if (first_token < 0 || first_token >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
+  if (position < 0 || n_steps > h->cfg.kv_capacity || position > h->cfg.kv_capacity - n_steps) return MBK_ERR_INVALID_ARG;
+  if (h->inject_armed) return MBK_ERR_STATE;  // injection is defined for single teacher-forced steps only
+  if (int st = sticky_status(h)) return st;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  h->last_token = first_token;
+  return launch_steps(h, first_token, nullptr, n_steps, position, logits_out, stream, tokens_out);
 }
 
 int mbk_decode_step_host(mbk_handle* h, int32_t token_id, int32_t position, float* logits_host, void* stream) {

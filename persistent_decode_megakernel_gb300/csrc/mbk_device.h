@@ -41,6 +41,7 @@ struct KernelParams {
   unsigned long long* trace;    // null, or 4 globaltimer stamps per task (begin, ready, end, first stage)
   const unsigned long long* inject;  // null, or words [L][H]: row l replaces the input of layer l >= 1
   unsigned poll_backoff_ns;     // sleep between polls of a word that is not ready yet (0: none)
+  int lm_tasks;                 // LM-head tasks of a step (greedy decoding: contributions to its argmax)
 };
 
 // Changes every step.
@@ -49,11 +50,21 @@ struct StepParams {
   int token;                 // the token when tokens is null (n == 1)
   int pos;                   // position of the launch's first step
   unsigned tag;              // tag of the first step (never 0); step i writes its words with tag + i
-  float* logits;             // device fp32 [n][V]
+  float* logits;             // device fp32 [n][V] (or one [V] buffer every step overwrites)
+  int logits_step;           // floats between the logits of consecutive steps: V, or 0
   const int* tokens;         // device [n], or null
   int n;                     // steps in this launch
   unsigned long long* sync;  // step counter: every CTA adds 1 after each step (null when n == 1)
   unsigned long long sync_base;  // its value when the launch starts
+  // greedy decoding (greedy != 0): the token of step i + 1 is the argmax of step i's logits (lowest
+  // index among equal values); tokens[] is unused.  amax[i] collects the packed (value, index) key of
+  // step i by atomic max, amax_done[i] counts the LM-head tasks that contributed (both zeroed by the
+  // host), and out_tokens[i] receives the argmax of step i (written by the CTA that completes it).
+  int greedy;
+  unsigned long long* amax;
+  unsigned* amax_done;
+  int* out_tokens;
+  unsigned long long* tokword;  // the argmax of step i as a word tagged tag + i + 1 (read by step i + 1)
 };
 
 }  // namespace mbk

@@ -116,8 +116,9 @@ struct Ctl {
   unsigned abort;       // set once this CTA gave up a wait: later activation waits return at once
   unsigned prod_quit;   // the producer stopped early (its consumers stopped taking stages)
   unsigned skip;        // an earlier step failed: this launch does nothing
-  unsigned pad;
+  int gtoken;           // greedy decoding: this step's token (polled by thread 0)
   float red[32];        // block reduction scratch
+  unsigned long long amax[kComputeWarps + 1];  // greedy decoding: per-warp argmax keys of the LM head
   float2 rope[64];      // cos/sin of this step's position, i < head_dim / 2
   const uint16_t* gain[2 * kMaxLayers + 1];  // attn_norm[l] at 2l, mlp_norm[l] at 2l+1, final at 2L
   const uint16_t* bias[3 * kMaxLayers];      // bq, bk, bv of layer l at 3l..3l+2
@@ -1041,6 +1042,55 @@ __device__ __forceinline__ void emit_row(Ctx& c, int type, unsigned long long* o
   st_word(out + r, c.tag, v);
 }
 
+// Greedy decoding, end of step `step` (every compute thread, after the block barrier that ends the
+// step's last task).  The largest logit of the CTA's LM-head tasks (the lowest row among equal
+// values) joins the step's argmax by one 64-bit atomic max of its key (ordered value bits, then
+// ~row: keys of different values order like the values), and the tasks are counted.  The CTA whose
+// count completes the step reads the argmax, reports it and publishes it as a tagged word with the
+// next step's tag; every CTA polls that word like any other input at the start of the next step.
+// Nothing here waits.
+__device__ __noinline__ void greedy_boundary(const KernelParams* P, const StepParams* S, Ctl* ctl, int step,
+                                            uint32_t t0, uint32_t t1) {
+  const int ctid = (int)threadIdx.x - 32, lane = (int)threadIdx.x & 31;
+  const float* logits = S->logits + (size_t)step * S->logits_step;
+  unsigned long long key = 0ull;
+  unsigned ntask = 0;
+  for (uint32_t ti = t1; ti > t0; --ti) {  // the LM-head tasks close the CTA's list
+    const Task* t = P->tasks + (ti - 1);
+    if (t->type != T_LMHEAD) break;
+    ++ntask;
+    const unsigned row0 = t->row0, nrows = t->nrows;
+    for (unsigned i = (unsigned)ctid; i < nrows; i += kCT) {
+      const unsigned u = __float_as_uint(logits[row0 + i]);
+      const unsigned ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+      const unsigned long long k = ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (row0 + i));
+      key = k > key ? k : key;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long k2 = __shfl_xor_sync(0xffffffffu, key, o);
+    key = k2 > key ? k2 : key;
+  }
+  if (lane == 0) ctl->amax[ctid >> 5] = key;
+  compute_sync();
+  if (ctid == 0 && ntask > 0) {
+    unsigned long long best = 0ull;
+    for (int w = 0; w < kComputeWarps; ++w) best = ctl->amax[w] > best ? ctl->amax[w] : best;
+    atomicMax(S->amax + step, best);
+    __threadfence();
+    const unsigned before = atomicAdd(S->amax_done + step, ntask);
+    if (before + ntask == (unsigned)P->lm_tasks) {  // the last contribution of the step
+      __threadfence();
+      const unsigned long long k = atomicOr(S->amax + step, 0ull);
+      const unsigned idx = 0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull);
+      const int tok = k != 0ull && idx < (unsigned)P->V ? (int)idx : 0;
+      S->out_tokens[step] = tok;
+      st_word(S->tokword, S->tag + (unsigned)step + 1u, __int_as_float(tok));
+    }
+  }
+}
+
 // A projection task (QKV, O, gate/up, down, LM head): one code path for every type.  The critical
 // path after the inputs arrive is one block barrier, the row's dot products and the output store:
 // weight stages are checked before the inputs are polled, and the norm scale (a reduction of the
@@ -1363,6 +1413,9 @@ __device__ __forceinline__ void stage_tasks(const Task* src, Task* dst, int n, i
   for (int i = tid; i < n16; i += nt) d4[i] = s4[i];
 }
 
+// kGreedy: greedy decoding (the argmax of each step's logits is the next step's token).  A separate
+// instantiation, so that the teacher-forced kernel carries none of its state in registers.
+template <bool kGreedy>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const __grid_constant__ StepParams S) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
@@ -1418,18 +1471,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   float* sv = reinterpret_cast<float*>(smem + P.off_sv);
   float* res = reinterpret_cast<float*>(smem + P.off_res);
   float* add = reinterpret_cast<float*>(smem + P.off_resid);
+  constexpr bool greedy = kGreedy;
+  c.task_index = t0;
 #pragma unroll 1
   for (int step = 0; step < S.n; ++step) {
   c.tag = S.tag + (unsigned)step;
   c.pos = S.pos + step;
-  c.token = S.tokens != nullptr ? S.tokens[step] : S.token;
-  c.logits = S.logits + (size_t)step * P.V;
+  c.token = (S.tokens != nullptr && !greedy) ? S.tokens[step] : S.token;
+  c.logits = S.logits + (size_t)step * S.logits_step;
   if (step > 0) {
     // every compute warp is past the previous step's last task: this step's RoPE row, and the first
-    // window of task records again if the CTA has more than one
+    // window of task records again if the CTA has more than one; greedy: the previous step's argmax
     for (int i = c.ctid; i < P.d / 2; i += kCT) ctl->rope[i] = P.rope[(size_t)c.pos * (P.d / 2) + i];
     if (t1 - t0 > (uint32_t)kTaskWindow) stage_tasks(P.tasks + t0, tasks, kTaskWindow, c.ctid, kCT);
+    if constexpr (greedy) {
+      // the previous step's argmax: this CTA's part (the call sits here rather than at the end of
+      // the step's loop, where it made the compiler spill registers of the task loop), then the
+      // token itself, published with this step's tag
+      greedy_boundary(c.P, &S, ctl, step - 1, t0, t1);
+      InVec v{};
+      v.src = S.tokword;
+      v.n = v.n1 = 1;
+      v.dst = reinterpret_cast<float*>(&ctl->gtoken);
+      poll_vec(c, v, 0xA00000u);
+    }
     compute_sync();
+    if constexpr (greedy) c.token = ctl->gtoken;
   }
 #pragma unroll 1
   for (uint32_t ti = t0; ti < t1; ++ti) {
@@ -1457,6 +1524,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     atomicAdd(S.sync, 1ull);
   }
   }
+  if constexpr (greedy) greedy_boundary(c.P, &S, ctl, S.n - 1, t0, t1);  // the last step's argmax
+
 }
 
 // ------------------------------------------------------------------ RoPE table and cache fill
@@ -1500,7 +1569,9 @@ __global__ void kv_fill_kernel(uint16_t* kv_layer, const float* k_raw, const flo
 
 // Launch helpers used by the C ABI (mbk_api.cu).
 namespace mbk {
-const void* decode_kernel_ptr() { return reinterpret_cast<const void*>(&decode_kernel); }
+const void* decode_kernel_ptr(bool greedy) {
+  return greedy ? reinterpret_cast<const void*>(&decode_kernel<true>) : reinterpret_cast<const void*>(&decode_kernel<false>);
+}
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st) {
   rope_table_kernel<<<264, 256, 0, st>>>(out, C, d, theta);
   return cudaGetLastError();

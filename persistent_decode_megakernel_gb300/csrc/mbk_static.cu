@@ -21,7 +21,7 @@
 #include "mbk_sched.h"
 
 namespace mbk {
-const void* decode_kernel_ptr();
+const void* decode_kernel_ptr(bool greedy);
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
 }  // namespace mbk
 
@@ -101,7 +101,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     cudaDeviceGetAttribute(&D.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (!coop) return MBK_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(decode_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize, D.smem_optin) != cudaSuccess)
+    if (cudaFuncSetAttribute(decode_kernel_ptr(false), cudaFuncAttributeMaxDynamicSharedMemorySize, D.smem_optin) != cudaSuccess)
       return MBK_ERR_CUDA;
     D.base = static_cast<unsigned char*>(p);
     D.num_sms = prop.multiProcessorCount;
@@ -201,6 +201,9 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     kp.trace = nullptr;
     kp.inject = nullptr;
     kp.poll_backoff_ns = 0;
+    int lm = 0;
+    for (const Task& t : plan.tasks) lm += t.type == T_LMHEAD ? 1 : 0;
+    kp.lm_tasks = lm;
     D.plan = plan;
     D.resident_key = key;
   }
@@ -215,13 +218,19 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
   sp.pos = position;
   sp.tag = 1u;
   sp.logits = logits_out;
+  sp.logits_step = 0;
   sp.tokens = nullptr;
   sp.n = 1;
   sp.sync = nullptr;
   sp.sync_base = 0;
+  sp.greedy = 0;
+  sp.amax = nullptr;
+  sp.amax_done = nullptr;
+  sp.out_tokens = nullptr;
+  sp.tokword = nullptr;
   KernelParams kp = D.kp;
   void* args[] = {&kp, &sp};
-  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(), dim3(D.plan.num_ctas), dim3(kThreads), args,
+  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(false), dim3(D.plan.num_ctas), dim3(kThreads), args,
                                               (size_t)D.plan.smem_bytes, st);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;

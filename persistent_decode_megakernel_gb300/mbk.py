@@ -27,7 +27,8 @@ MBK_ERR_STATE = -6
 
 EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
-            "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps")
+            "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps",
+            "mbk_decode_greedy")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -86,6 +87,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_decode_step.restype = ctypes.c_int
         lib.mbk_decode_steps.argtypes = [vp, vp, i32, i32, vp, vp]
         lib.mbk_decode_steps.restype = ctypes.c_int
+        lib.mbk_decode_greedy.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        lib.mbk_decode_greedy.restype = ctypes.c_int
         lib.mbk_decode_step_host.argtypes = [vp, i32, i32, vp, vp]
         lib.mbk_decode_step_host.restype = ctypes.c_int
         lib.mbk_kv_fill.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, vp]
@@ -154,6 +157,14 @@ def mbk_decode_steps(h, tokens, position: int, logits_ptr: int, stream_ptr: int)
     arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     return load_library().mbk_decode_steps(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), int(position),
                                            ctypes.c_void_p(logits_ptr), ctypes.c_void_p(stream_ptr))
+
+
+def mbk_decode_greedy(h, first_token: int, n_steps: int, position: int, tokens_out_ptr: int, logits_ptr: int,
+                      stream_ptr: int) -> int:
+    """tokens_out_ptr: device int32[n_steps]; logits_ptr: device float[n_steps][vocab], or 0 for none."""
+    return load_library().mbk_decode_greedy(h, int(first_token), int(n_steps), int(position),
+                                            ctypes.c_void_p(tokens_out_ptr), ctypes.c_void_p(logits_ptr or None),
+                                            ctypes.c_void_p(stream_ptr))
 
 
 def mbk_decode_step_host(h, token_id: int, position: int, logits_host_ptr: int, stream_ptr: int) -> int:
@@ -280,6 +291,18 @@ class Decoder:
         stream = self.torch.cuda.current_stream(self.device).cuda_stream
         _check(mbk_decode_steps(self.handle, tokens, pos0, out.data_ptr(), stream), "mbk_decode_steps")
         return out
+
+    def greedy(self, first_token: int, n: int, pos0: int, logits=None, want_logits: bool = True):
+        """Greedy decode of n steps from first_token at pos0 in one launch.  Returns (tokens, logits):
+        tokens[i] (device int32) is the argmax of step i's logits; logits [n, vocab] or None."""
+        toks = self.torch.empty(n, dtype=self.torch.int32, device=self.device)
+        out = logits
+        if out is None and want_logits:
+            out = self.torch.empty((n, self.shape.vocab), dtype=self.torch.float32, device=self.device)
+        stream = self.torch.cuda.current_stream(self.device).cuda_stream
+        _check(mbk_decode_greedy(self.handle, first_token, n, pos0, toks.data_ptr(), out.data_ptr() if out is not None else 0,
+                                 stream), "mbk_decode_greedy")
+        return toks, out
 
     def status(self) -> int:
         return mbk_get_status(self.handle)
