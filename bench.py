@@ -252,6 +252,23 @@ def run_ours(args, shape_name):
         torch.cuda.synchronize()
         single_tps = n1 / (a1.elapsed_time(b1) * 1e-3)
 
+    # greedy decoding over the same positions (mbk_decode_greedy: each step's argmax is the next
+    # token, inside one launch per run of positions; tokens only, no logits), for reference
+    greedy_tps = None
+    if spc > 1:
+        for _ in range(2):
+            dec.greedy(toks[0], spc, s.pos0, want_logits=False)
+        torch.cuda.synchronize()
+        ng = max(1, min(ncalls, 8))
+        a1, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a1.record(stream)
+        for _ in range(ng):
+            dec.greedy(toks[0], spc, s.pos0, want_logits=False)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        assert dec.status() == 0, "device-side wait timed out during greedy decoding"
+        greedy_tps = ng * spc / (a1.elapsed_time(b1) * 1e-3)
+
     # end to end through the C ABI with host buffers: token ids from the host, every step's logits
     # back to pinned host memory, the stream synchronised after each call
     host = torch.empty((spc, s.vocab), dtype=torch.float32, pin_memory=True)
@@ -299,6 +316,7 @@ def run_ours(args, shape_name):
                        "l2": "inputs larger than L2 (weights stream evict-first)",
                        "steps_per_call": spc,
                        "single_step_tokens_per_s": round(single_tps, 2) if single_tps else None,
+                       "greedy_tokens_per_s": round(greedy_tps, 2) if greedy_tps else None,
                        "vs_baseline_note": "pages' H200 MIG 60-SM number, context only"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
