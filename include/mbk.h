@@ -98,12 +98,32 @@ typedef struct {
  * Every device pointer must be 16-byte aligned.  On success *out receives the handle. */
 int mbk_create(const mbk_config *cfg, const mbk_weights *weights, void *kv_cache, int device, mbk_handle **out);
 
+/* As mbk_create, with a PAGED KV cache: kv_pool is a device bf16 pool of num_pages pages, each
+ * [n_layers][2][n_kv_heads][page_size][head_dim] (a page holds page_size consecutive positions of
+ * every layer and head).  Which page holds positions q*page_size .. (q+1)*page_size - 1 is set with
+ * mbk_set_page_table; until then no position is mapped.  The decode step itself is unchanged: the
+ * weight producer copies cached rows page by page and the appended row goes to its page.  The pages
+ * list a paged KV cache under "Next" (megabake/megabake README, "Current status"); the layout is
+ * this library's.  Errors: as mbk_create, and MBK_ERR_INVALID_ARG unless page_size is a power of
+ * two in [32, kv_capacity], num_pages >= 1 and kv_capacity / page_size (rounded up) <= 256. */
+int mbk_create_paged(const mbk_config *cfg, const mbk_weights *weights, void *kv_pool, int32_t num_pages,
+                     int32_t page_size, int device, mbk_handle **out);
+
+/* Paged handles: pages[q] (HOST array of n_pages distinct entries in [0, num_pages)) is the pool
+ * page of logical page q; positions [0, min(kv_capacity, n_pages * page_size)) are then mapped and
+ * may be decoded or filled.  The table is copied on `stream` before the call returns; a call that
+ * changes it must be ordered after the steps that use the old one.  Errors: MBK_ERR_INVALID_ARG for
+ * a contiguous handle, n_pages < 1 or above kv_capacity / page_size (rounded up), an entry out of
+ * range or repeated. */
+int mbk_set_page_table(mbk_handle *h, const int32_t *pages, int32_t n_pages, void *stream);
+
 /* One decode step: embeds token_id, writes K/V at `position` for every layer, attends over
  * cache rows [0, position] and writes fp32 logits[vocab] to the DEVICE buffer logits_out.
  * Cache rows below `position` are the caller's responsibility (earlier steps or mbk_kv_fill).
  * stream: a cudaStream_t (NULL = legacy default stream).  Asynchronous: returns after the launch.
  * Errors: MBK_ERR_INVALID_ARG if token_id is not in [0, vocab) or position not in
- * [0, kv_capacity) or logits_out is NULL; a sticky device error from an earlier step. */
+ * [0, kv_capacity) (for a paged cache: not mapped) or logits_out is NULL; a sticky device error
+ * from an earlier step. */
 int mbk_decode_step(mbk_handle *h, int32_t token_id, int32_t position, float *logits_out, void *stream);
 
 /* n_steps consecutive decode steps in ONE launch: token tokens[i] (a HOST array of n_steps ids,

@@ -17,8 +17,8 @@
 namespace mbk {
 const void* decode_kernel_ptr(bool greedy);
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
-cudaError_t launch_kv_fill(uint16_t* kv_layer, const float* k_raw, const float* v_raw, const float2* rope, int nkv, int C,
-                           int d, int p0, int n, cudaStream_t st);
+cudaError_t launch_kv_fill(const KernelParams& kp, int layer, const float* k_raw, const float* v_raw, int p0, int n,
+                           cudaStream_t st);
 }  // namespace mbk
 
 using namespace mbk;
@@ -47,6 +47,11 @@ struct mbk_handle {
   unsigned long long* d_amax = nullptr;  // [kv_capacity] greedy decoding: argmax key of each step
   unsigned* d_amax_done = nullptr;       // [kv_capacity] ... and the LM-head tasks that contributed
   unsigned long long* d_tokword = nullptr;  // ... and the argmax as a tagged word for the next step
+  // paged KV cache (mbk_create_paged): pool size, page size and the device page table
+  bool paged = false;
+  int num_pages = 0, page_size = 0, max_pages = 0;
+  int32_t* d_page_table = nullptr;
+  int mapped = 0;  // positions [0, mapped) have cache rows: kv_capacity, or what the page table covers
   unsigned long long* d_trace = nullptr;
   unsigned long long* d_inject = nullptr;
   bool inject_armed = false;
@@ -106,6 +111,7 @@ void free_all(mbk_handle* h) {
   cudaFree(h->d_amax);
   cudaFree(h->d_amax_done);
   cudaFree(h->d_tokword);
+  cudaFree(h->d_page_table);
   cudaFree(h->d_trace);
   cudaFree(h->d_inject);
   if (h->h_status) cudaFreeHost(h->h_status);
@@ -158,7 +164,50 @@ int mbk_plan_check(const mbk_config* cfg, int num_sms, mbk_plan_info* info) {
   return MBK_OK;
 }
 
+namespace {
+// The KV-cache layout of a handle: contiguous (num_pages == 0) or a pool of num_pages pages.
+struct KvLayout {
+  int num_pages = 0, page_size = 0;
+};
+int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache, KvLayout kvl, int device,
+                mbk_handle** out);
+}  // namespace
+
 int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache, int device, mbk_handle** out) {
+  return create_impl(cfg, weights, kv_cache, KvLayout{}, device, out);
+}
+
+int mbk_create_paged(const mbk_config* cfg, const mbk_weights* weights, void* kv_pool, int32_t num_pages,
+                     int32_t page_size, int device, mbk_handle** out) {
+  if (!out) return MBK_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (config_check(cfg) != MBK_OK || num_pages < 1 || page_size < 32 || (page_size & (page_size - 1)) != 0 ||
+      page_size > cfg->kv_capacity || (cfg->kv_capacity + page_size - 1) / page_size > kMaxPages)
+    return MBK_ERR_INVALID_ARG;
+  KvLayout kvl;
+  kvl.num_pages = num_pages;
+  kvl.page_size = page_size;
+  return create_impl(cfg, weights, kv_pool, kvl, device, out);
+}
+
+int mbk_set_page_table(mbk_handle* h, const int32_t* pages, int32_t n_pages, void* stream) {
+  if (!h || !pages || !h->paged || n_pages < 1 || n_pages > h->max_pages) return MBK_ERR_INVALID_ARG;
+  std::vector<char> used(h->num_pages, 0);
+  for (int32_t i = 0; i < n_pages; ++i) {
+    if (pages[i] < 0 || pages[i] >= h->num_pages || used[pages[i]]) return MBK_ERR_INVALID_ARG;
+    used[pages[i]] = 1;
+  }
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  if (cudaMemcpyAsync(h->d_page_table, pages, sizeof(int32_t) * (size_t)n_pages, cudaMemcpyHostToDevice,
+                      (cudaStream_t)stream) != cudaSuccess)
+    return MBK_ERR_CUDA;
+  h->mapped = std::min(h->cfg.kv_capacity, n_pages * h->page_size);
+  return MBK_OK;
+}
+
+namespace {
+int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache, KvLayout kvl, int device,
+                mbk_handle** out) {
   if (!out) return MBK_ERR_INVALID_ARG;
   *out = nullptr;
   if (config_check(cfg) != MBK_OK || !weights || !weights->embed || !weights->final_norm || !weights->layers || !kv_cache)
@@ -200,6 +249,11 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   if (!h) return MBK_ERR_NOMEM;
   h->device = device;
   h->cfg = *cfg;
+  h->paged = kvl.num_pages > 0;
+  h->num_pages = kvl.num_pages;
+  h->page_size = kvl.page_size;
+  h->max_pages = h->paged ? (cfg->kv_capacity + kvl.page_size - 1) / kvl.page_size : 0;
+  h->mapped = h->paged ? 0 : cfg->kv_capacity;
   PlanOptions opt;
   opt.smem_limit = smem_optin;
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
@@ -259,6 +313,8 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
       ck(cudaMalloc(&h->d_tokens, sizeof(int32_t) * s.C)) && ck(cudaMalloc(&h->d_sync, 8)) &&
       ck(cudaMalloc(&h->d_amax, sizeof(unsigned long long) * s.C)) && ck(cudaMalloc(&h->d_amax_done, sizeof(unsigned) * s.C)) &&
       ck(cudaMalloc(&h->d_tokword, 8)) && ck(cudaMemset(h->d_tokword, 0, 8)) &&
+      (!h->paged || (ck(cudaMalloc(&h->d_page_table, sizeof(int32_t) * h->max_pages)) &&
+                     ck(cudaMemset(h->d_page_table, 0, sizeof(int32_t) * h->max_pages)))) &&
       ck(cudaMemset(h->d_sync, 0, 8)) &&
       ck(cudaHostAlloc(&h->h_status, 16, cudaHostAllocMapped))) {
     ck(cudaMemcpy(h->d_tasks, p.tasks.data(), sizeof(Task) * p.tasks.size(), cudaMemcpyHostToDevice));
@@ -319,9 +375,15 @@ int mbk_create(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache
   kp.timeout_ns = (unsigned long long)env_int("MBK_WAIT_TIMEOUT_MS", 1000) * 1000000ull;
   kp.poll_backoff_ns = (unsigned)std::max(0, env_int("MBK_POLL_BACKOFF_NS", 0));
   kp.lm_tasks = lm_task_count(p);
+  kp.page_table = h->paged ? h->d_page_table : nullptr;
+  kp.page_size = h->paged ? h->page_size : s.C;
+  kp.page_shift = 0;
+  while (h->paged && (1 << kp.page_shift) < h->page_size) ++kp.page_shift;
+  kp.page_elems = h->paged ? (unsigned long long)s.L * 2 * s.nkv * h->page_size * s.d : 0ull;
   *out = h;
   return MBK_OK;
 }
+}  // namespace
 
 namespace {
 // One launch of n consecutive steps from pos0 (tokens on the device, or `token` when n == 1).
@@ -368,7 +430,7 @@ int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, i
 
 int mbk_decode_step(mbk_handle* h, int32_t token_id, int32_t position, float* logits_out, void* stream) {
   if (!h || !logits_out) return MBK_ERR_INVALID_ARG;
-  if (token_id < 0 || token_id >= h->cfg.vocab || position < 0 || position >= h->cfg.kv_capacity) return MBK_ERR_INVALID_ARG;
+  if (token_id < 0 || token_id >= h->cfg.vocab || position < 0 || position >= h->mapped) return MBK_ERR_INVALID_ARG;
   if (int st = sticky_status(h)) return st;
   if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
   h->last_token = token_id;
@@ -378,7 +440,7 @@ int mbk_decode_step(mbk_handle* h, int32_t token_id, int32_t position, float* lo
 int mbk_decode_steps(mbk_handle* h, const int32_t* tokens, int32_t n_steps, int32_t position, float* logits_out,
                      void* stream) {
   if (!h || !tokens || !logits_out || n_steps < 1) return MBK_ERR_INVALID_ARG;
-  if (position < 0 || n_steps > h->cfg.kv_capacity || position > h->cfg.kv_capacity - n_steps) return MBK_ERR_INVALID_ARG;
+  if (position < 0 || n_steps > h->mapped || position > h->mapped - n_steps) return MBK_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n_steps; ++i)
     if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
   if (h->inject_armed) return MBK_ERR_STATE;  // injection is defined for single steps only
@@ -396,7 +458,7 @@ int mbk_decode_greedy(mbk_handle* h, int32_t first_token, int32_t n_steps, int32
                       float* logits_out, void* stream) {
   if (!h || !tokens_out || n_steps < 1) return MBK_ERR_INVALID_ARG;
   if (first_token < 0 || first_token >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
-  if (position < 0 || n_steps > h->cfg.kv_capacity || position > h->cfg.kv_capacity - n_steps) return MBK_ERR_INVALID_ARG;
+  if (position < 0 || n_steps > h->mapped || position > h->mapped - n_steps) return MBK_ERR_INVALID_ARG;
   if (h->inject_armed) return MBK_ERR_STATE;  // injection is defined for single teacher-forced steps only
   if (int st = sticky_status(h)) return st;
   if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
@@ -418,13 +480,11 @@ int mbk_decode_step_host(mbk_handle* h, int32_t token_id, int32_t position, floa
 int mbk_kv_fill(mbk_handle* h, int layer, const float* k_raw, const float* v_raw, int32_t p0, int32_t n, void* stream) {
   if (!h || !k_raw || !v_raw) return MBK_ERR_INVALID_ARG;
   const mbk_config& c = h->cfg;
-  if (layer < 0 || layer >= c.n_layers || p0 < 0 || n < 0 || (int64_t)p0 + n > c.kv_capacity) return MBK_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= c.n_layers || p0 < 0 || n < 0 || (int64_t)p0 + n > h->mapped) return MBK_ERR_INVALID_ARG;
   if (int st = sticky_status(h)) return st;
   if (n == 0) return MBK_OK;
   if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
-  uint16_t* kv_layer = h->kp.kv + (size_t)layer * 2 * c.n_kv_heads * c.kv_capacity * c.head_dim;
-  cudaError_t e = launch_kv_fill(kv_layer, k_raw, v_raw, h->d_rope, c.n_kv_heads, c.kv_capacity, c.head_dim, p0, n,
-                                 (cudaStream_t)stream);
+  cudaError_t e = launch_kv_fill(h->kp, layer, k_raw, v_raw, p0, n, (cudaStream_t)stream);
   return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;
 }
 

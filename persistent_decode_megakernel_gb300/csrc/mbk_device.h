@@ -32,7 +32,7 @@ struct KernelParams {
   const uint16_t* embed;
   const uint16_t* final_norm;
   const LayerW* layers;
-  uint16_t* kv;                 // [L][2][nkv][C][d]
+  uint16_t* kv;                 // the KV cache (layout below)
   const float2* rope;           // [C][d/2] (cos, sin)
   unsigned long long* words;    // activation exchange words [L * act.per_layer]
   unsigned* status;             // device status [4]: code, cta, task, detail
@@ -42,6 +42,13 @@ struct KernelParams {
   const unsigned long long* inject;  // null, or words [L][H]: row l replaces the input of layer l >= 1
   unsigned poll_backoff_ns;     // sleep between polls of a word that is not ready yet (0: none)
   int lm_tasks;                 // LM-head tasks of a step (greedy decoding: contributions to its argmax)
+  // KV-cache layout.  Contiguous (page_table null): [L][2][nkv][C][d], page_size = C.  Paged: a pool
+  // of pages, each [L][2][nkv][page_size][d]; page_table[q] is the page that holds positions
+  // q * page_size ..; page_size is a power of two (page_shift its log2) and the table has at most
+  // kMaxPages entries (copied into shared memory at kernel start).
+  const int32_t* page_table;
+  int page_size, page_shift;
+  unsigned long long page_elems;  // bf16 elements of one page: L * 2 * nkv * page_size * d
 };
 
 // Changes every step.

@@ -124,6 +124,7 @@ struct Ctl {
   const uint16_t* bias[3 * kMaxLayers];      // bq, bk, bv of layer l at 3l..3l+2
   KernelParams params;  // the launch parameters, copied here: reads through a pointer into the
                         // parameter window are slow, shared-memory reads are not
+  int32_t pages[kMaxPages];  // paged KV cache: the page table
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block too large");
 
@@ -144,6 +145,17 @@ __device__ __noinline__ void record_failure(unsigned* status, unsigned* host_sta
     }
   }
   *(volatile unsigned*)abort_flag = 1u;
+}
+
+// Element offset of KV-cache row `p` of (layer, kv = 0 for K / 1 for V, KV head h), contiguous or paged.
+__device__ __forceinline__ size_t kv_off(const KernelParams& P, const Ctl* ctl, int layer, int kv, int h, int p) {
+  size_t page = 0;
+  int r = p;
+  if (P.page_table != nullptr) {
+    page = (size_t)(unsigned)ctl->pages[p >> P.page_shift];
+    r = p & (P.page_size - 1);
+  }
+  return page * P.page_elems + ((((size_t)layer * 2 + kv) * P.nkv + h) * P.page_size + r) * P.d;
 }
 
 // ------------------------------------------------------------------ per-CTA context (registers)
@@ -765,8 +777,8 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
     cur[d + i] = __bfloat16_as_ushort(v0);
     cur[d + i + half] = __bfloat16_as_ushort(v1);
     if (!aborted(c) && (!wo || (t.flags & TF_KV_APPEND))) {  // one task per head appends the row
-      __nv_bfloat16* Kc = reinterpret_cast<__nv_bfloat16*>(P.kv) + ((((size_t)l * 2 + 0) * P.nkv + kvh) * P.C + pos) * d;
-      __nv_bfloat16* Vc = reinterpret_cast<__nv_bfloat16*>(P.kv) + ((((size_t)l * 2 + 1) * P.nkv + kvh) * P.C + pos) * d;
+      __nv_bfloat16* Kc = reinterpret_cast<__nv_bfloat16*>(P.kv) + kv_off(P, c.ctl, l, 0, kvh, pos);
+      __nv_bfloat16* Vc = reinterpret_cast<__nv_bfloat16*>(P.kv) + kv_off(P, c.ctl, l, 1, kvh, pos);
       Kc[i] = k0;
       Kc[i + half] = k1;
       Vc[i] = v0;
@@ -1359,9 +1371,6 @@ __device__ __forceinline__ void produce(const KernelParams& P, const StepParams&
           const int a = sp * P.split_len;
           if (a <= pos) {
             const int b = min(a + P.split_len, pos);
-            const size_t head_off = (((size_t)layer * 2) * P.nkv + kvh) * P.C * P.d;
-            const uint16_t* K = P.kv + head_off;
-            const uint16_t* V = P.kv + head_off + (size_t)P.nkv * P.C * P.d;
             for (int jj = a; jj < b; jj += P.rows_per_stage) {
               const int n = min(P.rows_per_stage, b - jj);
               const unsigned nb = (unsigned)(n * P.d * 2);
@@ -1370,8 +1379,17 @@ __device__ __forceinline__ void produce(const KernelParams& P, const StepParams&
                 q = 1;
                 break;
               }
-              bulk_load(dst, K + (size_t)jj * P.d, nb, &ctl->full[stage], policy);
-              bulk_load(dst + (size_t)P.rows_per_stage * P.d * 2, V + (size_t)jj * P.d, nb, &ctl->full[stage], policy);
+              // K rows then V rows; a paged cache gives one copy pair per run of rows inside a page
+              for (int r0 = 0; r0 < n;) {
+                const int p = jj + r0;
+                const int run = P.page_table != nullptr ? min(n - r0, P.page_size - (p & (P.page_size - 1))) : n - r0;
+                const unsigned rb = (unsigned)(run * P.d * 2);
+                unsigned char* dk = dst + (size_t)r0 * P.d * 2;
+                bulk_load(dk, P.kv + kv_off(P, ctl, layer, 0, kvh, p), rb, &ctl->full[stage], policy);
+                bulk_load(dk + (size_t)P.rows_per_stage * P.d * 2, P.kv + kv_off(P, ctl, layer, 1, kvh, p), rb,
+                          &ctl->full[stage], policy);
+                r0 += run;
+              }
               advance();
             }
           }
@@ -1439,6 +1457,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     ctl->bias[3 * i + 2] = P.layers[i].w[LW_BV];
   }
   if (threadIdx.x == 0) ctl->gain[2 * P.L] = P.final_norm;
+  if (P.page_table != nullptr)  // the page table (at most kMaxPages entries: checked by the host)
+    for (int i = threadIdx.x; i < (P.C + P.page_size - 1) / P.page_size; i += blockDim.x) ctl->pages[i] = P.page_table[i];
   // this CTA's task records, staged in shared memory kTaskWindow at a time (one window covers a
   // CTA's whole step for the usual shapes)
   const uint32_t t0 = P.task_off[blockIdx.x], t1 = P.task_off[blockIdx.x + 1];
@@ -1543,8 +1563,9 @@ __global__ void rope_table_kernel(float2* out, int C, int d, double theta) {
 }
 
 // Rows [p0, p0+n) of one layer from pre-RoPE K and V: K rotated like a decode step, both -> bf16.
-__global__ void kv_fill_kernel(uint16_t* kv_layer, const float* k_raw, const float* v_raw, const float2* rope, int nkv,
-                               int C, int d, int p0, int n) {
+__global__ void kv_fill_kernel(uint16_t* kv, int layer, const float* k_raw, const float* v_raw, const float2* rope, int nkv,
+                               int d, int p0, int n, const int32_t* table, int page_size, int page_shift,
+                               unsigned long long page_elems) {
   const int half = d / 2;
   const size_t total = (size_t)nkv * n * half;
   for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
@@ -1556,8 +1577,11 @@ __global__ void kv_fill_kernel(uint16_t* kv_layer, const float* k_raw, const flo
     const float* vr = v_raw + ((size_t)h * n + j) * d;
     const float2 r = rope[(size_t)p * half + i];
     const float x0 = kr[i], x1 = kr[i + half];
-    __nv_bfloat16* K = reinterpret_cast<__nv_bfloat16*>(kv_layer) + ((size_t)h * C + p) * d;
-    __nv_bfloat16* V = reinterpret_cast<__nv_bfloat16*>(kv_layer) + ((size_t)(nkv + h) * C + p) * d;
+    const size_t page = table != nullptr ? (size_t)(unsigned)table[p >> page_shift] : 0;
+    const int row = table != nullptr ? (p & (page_size - 1)) : p;
+    const size_t kbase = page * page_elems + ((((size_t)layer * 2) * nkv + h) * page_size + row) * d;
+    __nv_bfloat16* K = reinterpret_cast<__nv_bfloat16*>(kv) + kbase;
+    __nv_bfloat16* V = reinterpret_cast<__nv_bfloat16*>(kv) + kbase + (size_t)nkv * page_size * d;
     K[i] = __float2bfloat16_rn(x0 * r.x - x1 * r.y);
     K[i + half] = __float2bfloat16_rn(x1 * r.x + x0 * r.y);
     V[i] = __float2bfloat16_rn(vr[i]);
@@ -1576,9 +1600,10 @@ cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStrea
   rope_table_kernel<<<264, 256, 0, st>>>(out, C, d, theta);
   return cudaGetLastError();
 }
-cudaError_t launch_kv_fill(uint16_t* kv_layer, const float* k_raw, const float* v_raw, const float2* rope, int nkv, int C,
-                           int d, int p0, int n, cudaStream_t st) {
-  kv_fill_kernel<<<264, 256, 0, st>>>(kv_layer, k_raw, v_raw, rope, nkv, C, d, p0, n);
+cudaError_t launch_kv_fill(const KernelParams& kp, int layer, const float* k_raw, const float* v_raw, int p0, int n,
+                           cudaStream_t st) {
+  kv_fill_kernel<<<264, 256, 0, st>>>(kp.kv, layer, k_raw, v_raw, kp.rope, kp.nkv, kp.d, p0, n, kp.page_table, kp.page_size,
+                                      kp.page_shift, kp.page_elems);
   return cudaGetLastError();
 }
 }  // namespace mbk

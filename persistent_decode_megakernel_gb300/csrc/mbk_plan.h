@@ -112,7 +112,8 @@ constexpr int kMaxTaskChunks = 256;
 constexpr int kGemvBatch = 4;          // ring stages a GEMV consumes together
 constexpr int kGemvXVec = 4;           // 16-byte input vectors a GEMV lane keeps in registers
 static_assert(kGemvXVec % 2 == 0, "the GEMV loads its weights in pairs of vectors");
-constexpr int kCtlBytes = 4352;        // shared-memory control block (barriers, flags, tables, parameters)
+constexpr int kCtlBytes = 5376;        // shared-memory control block (barriers, flags, tables, parameters)
+constexpr int kMaxPages = 256;         // logical pages of a paged KV cache (its table lives in the control block)
 constexpr int kMaxLayers = 64;
 constexpr int kTaskWindow = 160;      // task records staged in shared memory at a time
 constexpr int kMaxFusedKvHeads = 4;   // the O projection is fused into attention for at most this many KV heads

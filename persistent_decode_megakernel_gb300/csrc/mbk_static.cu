@@ -204,6 +204,10 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     int lm = 0;
     for (const Task& t : plan.tasks) lm += t.type == T_LMHEAD ? 1 : 0;
     kp.lm_tasks = lm;
+    kp.page_table = nullptr;  // contiguous cache
+    kp.page_size = s.C;
+    kp.page_shift = 0;
+    kp.page_elems = 0;
     D.plan = plan;
     D.resident_key = key;
   }

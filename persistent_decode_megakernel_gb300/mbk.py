@@ -28,7 +28,7 @@ MBK_ERR_STATE = -6
 EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
             "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps",
-            "mbk_decode_greedy")
+            "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -89,6 +89,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_decode_steps.restype = ctypes.c_int
         lib.mbk_decode_greedy.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         lib.mbk_decode_greedy.restype = ctypes.c_int
+        lib.mbk_create_paged.argtypes = [ctypes.POINTER(MbkConfig), ctypes.POINTER(MbkWeights), vp, i32, i32, ctypes.c_int,
+                                         ctypes.POINTER(vp)]
+        lib.mbk_create_paged.restype = ctypes.c_int
+        lib.mbk_set_page_table.argtypes = [vp, vp, i32, vp]
+        lib.mbk_set_page_table.restype = ctypes.c_int
         lib.mbk_decode_step_host.argtypes = [vp, i32, i32, vp, vp]
         lib.mbk_decode_step_host.restype = ctypes.c_int
         lib.mbk_kv_fill.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, vp]
@@ -157,6 +162,23 @@ def mbk_decode_steps(h, tokens, position: int, logits_ptr: int, stream_ptr: int)
     arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     return load_library().mbk_decode_steps(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), int(position),
                                            ctypes.c_void_p(logits_ptr), ctypes.c_void_p(stream_ptr))
+
+
+def mbk_create_paged(cfg: MbkConfig, weights: MbkWeights, kv_pool_ptr: int, num_pages: int, page_size: int,
+                     device: int) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(load_library().mbk_create_paged(ctypes.byref(cfg), ctypes.byref(weights), ctypes.c_void_p(kv_pool_ptr),
+                                           int(num_pages), int(page_size), int(device), ctypes.byref(h)),
+           "mbk_create_paged")
+    return h
+
+
+def mbk_set_page_table(h, pages, stream_ptr: int) -> int:
+    """pages: a sequence of pool page indices (copied into a host int32 array here)."""
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(pages, dtype=np.int32))
+    return load_library().mbk_set_page_table(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size),
+                                             ctypes.c_void_p(stream_ptr))
 
 
 def mbk_decode_greedy(h, first_token: int, n_steps: int, position: int, tokens_out_ptr: int, logits_ptr: int,
@@ -243,7 +265,9 @@ class Decoder:
     step() launches one decode step into a device logits tensor on the current torch stream.
     """
 
-    def __init__(self, wl, device: int = 0):
+    def __init__(self, wl, device: int = 0, paged=None):
+        """paged: None for a contiguous cache, or (num_pages, page_size, pages): a pool of num_pages
+        pages and the page table pages[q] for logical page q."""
         import torch
         self.torch = torch
         s = wl.shape
@@ -253,7 +277,13 @@ class Decoder:
         self.embed = wl.embed.to(dev)
         self.final_norm = wl.final_norm.to(dev)
         self.layers = [{k: (None if v is None else v.to(dev)) for k, v in w.items()} for w in wl.layers]
-        self.kv = torch.zeros((s.n_layers, 2, s.n_kv_heads, s.kv_capacity, s.head_dim), dtype=torch.bfloat16, device=dev)
+        self.paged = paged
+        if paged is None:
+            self.kv = torch.zeros((s.n_layers, 2, s.n_kv_heads, s.kv_capacity, s.head_dim), dtype=torch.bfloat16, device=dev)
+        else:
+            num_pages, page_size, _ = paged
+            self.pool = torch.zeros((num_pages, s.n_layers, 2, s.n_kv_heads, page_size, s.head_dim), dtype=torch.bfloat16,
+                                    device=dev)
         arr = (MbkLayerWeights * s.n_layers)()
         for i, w in enumerate(self.layers):
             for k in LAYER_FIELDS:
@@ -262,10 +292,36 @@ class Decoder:
         self._layer_arr = arr
         self.weights = MbkWeights(self.embed.data_ptr(), self.final_norm.data_ptr(), arr)
         self.cfg = config_from_shape(s)
-        self.handle = mbk_create(self.cfg, self.weights, self.kv.data_ptr(), device)
+        if paged is None:
+            self.handle = mbk_create(self.cfg, self.weights, self.kv.data_ptr(), device)
+        else:
+            self.handle = mbk_create_paged(self.cfg, self.weights, self.pool.data_ptr(), paged[0], paged[1], device)
+            self.set_pages(paged[2])
         self.logits = torch.empty(s.vocab, dtype=torch.float32, device=dev)
         if s.prefill:
             self.fill(wl.k_raw, wl.v_raw, 0)
+
+    def set_pages(self, pages) -> None:
+        stream = self.torch.cuda.current_stream(self.device).cuda_stream
+        _check(mbk_set_page_table(self.handle, pages, stream), "mbk_set_page_table")
+        self.pages = list(pages)
+
+    def logical_kv(self):
+        """The cache in the contiguous layout [L][2][nkv][C][d] (paged: gathered through the page table;
+        unmapped positions read as zero)."""
+        if self.paged is None:
+            return self.kv
+        torch = self.torch
+        s = self.shape
+        ps = self.paged[1]
+        out = torch.zeros((s.n_layers, 2, s.n_kv_heads, s.kv_capacity, s.head_dim), dtype=torch.bfloat16, device=self.device)
+        for q, page in enumerate(self.pages):
+            a = q * ps
+            b = min(s.kv_capacity, a + ps)
+            if a >= b:
+                break
+            out[:, :, :, a:b] = self.pool[page, :, :, :, : b - a]
+        return out
 
     def fill(self, k_raw, v_raw, p0: int) -> None:
         """Load cache rows p0.. of every layer from pre-RoPE K and V (fp32 [L][nkv][n][d])."""
