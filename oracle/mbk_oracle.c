@@ -74,6 +74,72 @@ void orc_gemv(const uint16_t *W, const float *x, const uint16_t *b, int rows, in
   }
 }
 
+/* E4M3 value of a code, from the format's definition. */
+float orc_fp8_to_f32(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);           /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexp(1.0 + m / 8.0, e - 7);    /* normal */
+  return (float)((c & 0x80) ? -v : v);
+}
+
+/* Nearest code to f (ties to the even code), saturating at 448: the non-negative finite codes
+ * 0x00..0x7E are increasing in value, so the nearest is found between the two codes that
+ * bracket |f|. */
+uint8_t orc_fp8_from_f32(float f) {
+  if (isnan(f)) return 0x7F;
+  const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  const double a = fabs((double)f);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  int lo = 0, hi = 0x7E; /* largest code with value <= a */
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if ((double)orc_fp8_to_f32((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+  }
+  const double vlo = orc_fp8_to_f32((uint8_t)lo), vhi = orc_fp8_to_f32((uint8_t)(lo + 1));
+  int c;
+  if (a - vlo < vhi - a) c = lo;
+  else if (a - vlo > vhi - a) c = lo + 1;
+  else c = (lo % 2 == 0) ? lo : lo + 1;
+  return (uint8_t)(sign | c);
+}
+
+void orc_quantize_fp8(const uint16_t *W, int rows, int cols, uint8_t *q, float *s) {
+  for (int r = 0; r < rows; ++r) {
+    const uint16_t *w = W + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int k = 0; k < cols; ++k) {
+      const float a = fabsf(orc_bf16_to_f32(w[k]));
+      if (a > amax) amax = a;
+    }
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    s[r] = sc;
+    for (int k = 0; k < cols; ++k) q[(size_t)r * cols + k] = orc_fp8_from_f32(orc_bf16_to_f32(w[k]) / sc);
+  }
+}
+
+void orc_gemv_fp8(const uint8_t *Q, const float *s, const float *x, const uint16_t *b, int rows, int cols, float *y,
+                  int nthreads) {
+  int nt = threads_for(nthreads);
+  (void)nt;
+  float lut[256];
+  for (int c = 0; c < 256; ++c) lut[c] = orc_fp8_to_f32((uint8_t)c);
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nt) schedule(static)
+#endif
+  for (int r = 0; r < rows; ++r) {
+    const uint8_t *w = Q + (size_t)r * cols;
+    double acc = 0.0;
+    for (int k = 0; k < cols; ++k) acc += (double)lut[w[k]] * (double)x[k];
+    acc *= (double)s[r];
+    if (b) acc += (double)orc_bf16_to_f32(b[r]);
+    y[r] = (float)acc;
+  }
+}
+
 /* RoPE (article, "How a model gets in": the rope region).  Rotate-half pairing as in
  * Hugging Face Llama: element i pairs with element i + d/2, frequency theta^(-2i/d). */
 void orc_rope(float *v, int n_heads, int d, int pos, double theta) {
@@ -170,8 +236,34 @@ static int config_ok(const orc_config *c) {
 /* One decode step, in the order the article's section "What a megakernel is, and why small
  * models want one" lists the ops, with the embedding at the start and the final norm and
  * tied vocabulary projection at the end (README, "Current status"). */
+/* A projection of the step: on the bf16 weight, or on its FP8 copy when there is one. */
+static void project(const uint16_t *W, const orc_fp8_layer *f8, int slot, const float *x, const uint16_t *b, int rows,
+                    int cols, float *y, int nthreads) {
+  if (f8)
+    orc_gemv_fp8(f8->q[slot], f8->s[slot], x, b, rows, cols, y, nthreads);
+  else
+    orc_gemv(W, x, b, rows, cols, y, nthreads);
+}
+
+static int decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                       const orc_fp8_weights *fp8, uint16_t *kv_cache, int token, int pos, float *logits, float *taps,
+                       int nthreads);
+
 int orc_decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
                     uint16_t *kv_cache, int token, int pos, float *logits, float *taps, int nthreads) {
+  return decode_step(cfg, embed, final_norm, layers, NULL, kv_cache, token, pos, logits, taps, nthreads);
+}
+
+int orc_decode_step_fp8(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                        const orc_fp8_weights *fp8, uint16_t *kv_cache, int token, int pos, float *logits, float *taps,
+                        int nthreads) {
+  if (!fp8 || !fp8->layers || !fp8->lm_q || !fp8->lm_s) return -1;
+  return decode_step(cfg, embed, final_norm, layers, fp8, kv_cache, token, pos, logits, taps, nthreads);
+}
+
+static int decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                       const orc_fp8_weights *fp8, uint16_t *kv_cache, int token, int pos, float *logits, float *taps,
+                       int nthreads) {
   if (!cfg || !embed || !layers || !kv_cache || !logits || !config_ok(cfg)) return -1;
   if (token < 0 || token >= cfg->vocab || pos < 0 || pos >= cfg->kv_capacity) return -1;
   const int L = cfg->n_layers, H = cfg->hidden, I = cfg->intermediate;
@@ -195,14 +287,15 @@ int orc_decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t
 
   for (int l = 0; l < L; ++l) {
     const orc_layer *w = &layers[l];
+    const orc_fp8_layer *f8 = fp8 ? &fp8->layers[l] : NULL;
     uint16_t *Kc = kv_cache + (size_t)l * 2 * nkv * cap * d;
     uint16_t *Vc = Kc + (size_t)nkv * cap * d;
 
     /* attention sublayer */
     orc_rmsnorm(x, w->attn_norm, H, cfg->rms_eps, xn);
-    orc_gemv(w->wq, xn, cfg->qkv_bias ? w->bq : NULL, nq * d, H, q, nthreads);
-    orc_gemv(w->wk, xn, cfg->qkv_bias ? w->bk : NULL, nkv * d, H, k, nthreads);
-    orc_gemv(w->wv, xn, cfg->qkv_bias ? w->bv : NULL, nkv * d, H, v, nthreads);
+    project(w->wq, f8, 0, xn, cfg->qkv_bias ? w->bq : NULL, nq * d, H, q, nthreads);
+    project(w->wk, f8, 1, xn, cfg->qkv_bias ? w->bk : NULL, nkv * d, H, k, nthreads);
+    project(w->wv, f8, 2, xn, cfg->qkv_bias ? w->bv : NULL, nkv * d, H, v, nthreads);
     orc_rope(q, nq, d, pos, cfg->rope_theta);
     orc_rope(k, nkv, d, pos, cfg->rope_theta);
     for (int h = 0; h < nkv; ++h)
@@ -211,23 +304,26 @@ int orc_decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t
         Vc[((size_t)h * cap + pos) * d + t] = orc_f32_to_bf16(v[(size_t)h * d + t]);
       }
     orc_attention(q, Kc, Vc, nq, nkv, d, cap, pos + 1, o, nthreads);
-    orc_gemv(w->wo, o, NULL, H, nq * d, y, nthreads);
+    project(w->wo, f8, 3, o, NULL, H, nq * d, y, nthreads);
     for (int i = 0; i < H; ++i) x[i] = (float)((double)x[i] + (double)y[i]);
     if (taps) memcpy(taps + (size_t)(2 * l + 1) * H, x, sizeof(float) * H);
 
     /* MLP sublayer */
     orc_rmsnorm(x, w->mlp_norm, H, cfg->rms_eps, xn);
-    orc_gemv(w->w_gate, xn, NULL, I, H, g, nthreads);
-    orc_gemv(w->w_up, xn, NULL, I, H, u, nthreads);
+    project(w->w_gate, f8, 4, xn, NULL, I, H, g, nthreads);
+    project(w->w_up, f8, 5, xn, NULL, I, H, u, nthreads);
     orc_silu_mul(g, u, I, hbuf);
-    orc_gemv(w->w_down, hbuf, NULL, H, I, y, nthreads);
+    project(w->w_down, f8, 6, hbuf, NULL, H, I, y, nthreads);
     for (int i = 0; i < H; ++i) x[i] = (float)((double)x[i] + (double)y[i]);
     if (taps) memcpy(taps + (size_t)(2 * l + 2) * H, x, sizeof(float) * H);
   }
 
   /* final norm, then the tied vocabulary projection (the embedding matrix) */
   orc_rmsnorm(x, final_norm, H, cfg->rms_eps, xn);
-  orc_gemv(embed, xn, NULL, cfg->vocab, H, logits, nthreads);
+  if (fp8)
+    orc_gemv_fp8(fp8->lm_q, fp8->lm_s, xn, NULL, cfg->vocab, H, logits, nthreads);
+  else
+    orc_gemv(embed, xn, NULL, cfg->vocab, H, logits, nthreads);
 
   free(x); free(xn); free(y); free(q); free(k); free(v); free(o); free(g); free(u); free(hbuf);
   return 0;

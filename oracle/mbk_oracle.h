@@ -87,6 +87,42 @@ void orc_kv_fill(const orc_config *cfg, uint16_t *kv_layer, const float *k_raw, 
 int orc_decode_step(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
                     uint16_t *kv_cache, int token, int pos, float *logits, float *taps, int nthreads);
 
+/* ---- FP8 weights (opt-in weight format; the MegaBake website lists FP8 under "Next") ----
+ * The pages name FP8 weight streaming but fix no format; the reading taken here: OCP FP8 E4M3
+ * (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN;
+ * largest finite 448, smallest normal 2^-6, subnormals m * 2^-9) with one fp32 scale per output
+ * row.  Row r of a bf16 matrix W: amax = max_k |W[r,k]|; s = amax / 448 in fp32 (1 for an all-zero
+ * row); q[r,k] = E4M3(W[r,k] / s), the fp32 quotient rounded to the nearest code, ties to the even
+ * code, magnitudes above 448 saturating to 448.  A projection over such a row is
+ * y[r] = s * sum_k E4M3value(q[r,k]) x[k] (+ bias): the scale applies to the exact sum.
+ * Which weights: every layer's Wq, Wk, Wv, Wo, Wgate, Wup, Wdown and the LM head's copy of E; the
+ * embedding lookup, norm gains and biases stay bf16.  Parity pins: exact codes of hand-computed
+ * values, ties, saturation, the round trip of every finite code, and the row maximum mapping to 448. */
+uint8_t orc_fp8_from_f32(float f);
+float orc_fp8_to_f32(uint8_t c);
+/* q: [rows][cols] codes, s: [rows] scales. */
+void orc_quantize_fp8(const uint16_t *W, int rows, int cols, uint8_t *q, float *s);
+/* y[r] = s[r] * sum_k value(Q[r,k]) x[k] (+ b[r]), accumulated in double, stored as fp32. */
+void orc_gemv_fp8(const uint8_t *Q, const float *s, const float *x, const uint16_t *b, int rows, int cols, float *y,
+                  int nthreads);
+
+/* The FP8 copies of one layer's projections, in the order Wq, Wk, Wv, Wo, Wgate, Wup, Wdown. */
+typedef struct {
+  const uint8_t *q[7];
+  const float *s[7];
+} orc_fp8_layer;
+typedef struct {
+  const orc_fp8_layer *layers;  /* [L] */
+  const uint8_t *lm_q;          /* [V][H]: the LM head's copy of E */
+  const float *lm_s;            /* [V] */
+} orc_fp8_weights;
+
+/* orc_decode_step with every projection and the LM head on FP8 weights (the embedding row, the
+ * norms and the biases still come from the bf16 tensors). */
+int orc_decode_step_fp8(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                        const orc_fp8_weights *fp8, uint16_t *kv_cache, int token, int pos, float *logits, float *taps,
+                        int nthreads);
+
 /* Number of OpenMP threads the oracle would use for nthreads <= 0 (1 without OpenMP). */
 int orc_max_threads(void);
 

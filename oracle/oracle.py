@@ -55,6 +55,18 @@ class _Layer(ctypes.Structure):
                                   "w_gate", "w_up", "w_down")]
 
 
+class _Fp8Layer(ctypes.Structure):
+    _fields_ = [("q", _P * 7), ("s", _P * 7)]
+
+
+class _Fp8Weights(ctypes.Structure):
+    _fields_ = [("layers", ctypes.POINTER(_Fp8Layer)), ("lm_q", _P), ("lm_s", _P)]
+
+
+# the projections of a layer in the order of the FP8 tables
+FP8_SLOTS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
 def bind(lib):
     """Declare the argument types of the oracle's exported functions on a loaded CDLL."""
     f = ctypes.c_float
@@ -72,7 +84,27 @@ def bind(lib):
                                     ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int]
     lib.orc_decode_step.restype = ctypes.c_int
     lib.orc_max_threads.restype = ctypes.c_int
+    lib.orc_fp8_from_f32.argtypes = [f]
+    lib.orc_fp8_from_f32.restype = ctypes.c_uint8
+    lib.orc_fp8_to_f32.argtypes = [ctypes.c_uint8]
+    lib.orc_fp8_to_f32.restype = f
+    lib.orc_quantize_fp8.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P]
+    lib.orc_gemv_fp8.argtypes = [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int]
+    lib.orc_decode_step_fp8.argtypes = [ctypes.POINTER(_Config), _P, _P, ctypes.POINTER(_Layer),
+                                        ctypes.POINTER(_Fp8Weights), _P, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int]
+    lib.orc_decode_step_fp8.restype = ctypes.c_int
     return lib
+
+
+def quantize_fp8(w_bits: np.ndarray, lib=None):
+    """FP8 (E4M3) codes and per-row fp32 scales of a bf16 matrix given as uint16 bit patterns [rows, cols]."""
+    lib = oracle_lib() if lib is None else lib
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    sc = np.empty(rows, dtype=np.float32)
+    lib.orc_quantize_fp8(w.ctypes.data, rows, cols, q.ctypes.data, sc.ctypes.data)
+    return q, sc
 
 
 def oracle_lib():
@@ -103,7 +135,8 @@ class OracleDecoder:
     Holds its own bf16 KV cache [L][2][nkv][cap][d] (uint16 bit patterns).
     """
 
-    def __init__(self, wl, nthreads: int = 0, lib=None):
+    def __init__(self, wl, nthreads: int = 0, lib=None, fp8: bool = False):
+        """fp8: every projection and the LM head on FP8 (E4M3, per-row scale) copies of the weights."""
         self.lib = oracle_lib() if lib is None else lib
         s = wl.shape
         self.shape = s
@@ -124,6 +157,18 @@ class OracleDecoder:
                     self._keep.append(a)
                     setattr(arr[i], k, a.ctypes.data)
         self.layers = arr
+        self.fp8 = None
+        if fp8:
+            f8 = (_Fp8Layer * s.n_layers)()
+            for i, w in enumerate(wl.layers):
+                for j, k in enumerate(FP8_SLOTS):
+                    q, sc = quantize_fp8(bf16_bits(w[k]), self.lib)
+                    self._keep += [q, sc]
+                    f8[i].q[j] = q.ctypes.data
+                    f8[i].s[j] = sc.ctypes.data
+            lq, ls = quantize_fp8(self.embed, self.lib)
+            self._keep += [lq, ls, f8]
+            self.fp8 = _Fp8Weights(f8, lq.ctypes.data, ls.ctypes.data)
         self.kv = np.zeros((s.n_layers, 2, s.n_kv_heads, s.kv_capacity, s.head_dim), dtype=np.uint16)
         if s.prefill:
             self.fill(wl.k_raw, wl.v_raw, 0)
@@ -141,9 +186,14 @@ class OracleDecoder:
         s = self.shape
         logits = np.empty(s.vocab, dtype=np.float32)
         tap = np.empty((2 * s.n_layers + 1, s.hidden), dtype=np.float32) if taps else None
-        rc = self.lib.orc_decode_step(ctypes.byref(self.cfg), self.embed.ctypes.data, self.final_norm.ctypes.data,
-                                      self.layers, self.kv.ctypes.data, int(token), int(pos), logits.ctypes.data,
-                                      _ptr(tap), self.nthreads)
+        if self.fp8 is None:
+            rc = self.lib.orc_decode_step(ctypes.byref(self.cfg), self.embed.ctypes.data, self.final_norm.ctypes.data,
+                                          self.layers, self.kv.ctypes.data, int(token), int(pos), logits.ctypes.data,
+                                          _ptr(tap), self.nthreads)
+        else:
+            rc = self.lib.orc_decode_step_fp8(ctypes.byref(self.cfg), self.embed.ctypes.data, self.final_norm.ctypes.data,
+                                              self.layers, ctypes.byref(self.fp8), self.kv.ctypes.data, int(token), int(pos),
+                                              logits.ctypes.data, _ptr(tap), self.nthreads)
         if rc != 0:
             raise ValueError(f"oracle rejected token={token} pos={pos}")
         return (logits, tap) if taps else logits
