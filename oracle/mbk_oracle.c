@@ -135,7 +135,7 @@ void orc_gemv_fp8(const uint8_t *Q, const float *s, const float *x, const uint16
     double acc = 0.0;
     for (int k = 0; k < cols; ++k) acc += (double)lut[w[k]] * (double)x[k];
     acc *= (double)s[r];
-    if (b) acc += (double)orc_bf16_to_f32(b[r]);
+    if (b != NULL) acc += (double)orc_bf16_to_f32(b[r]);  /* the bias is not quantized */
     y[r] = (float)acc;
   }
 }
