@@ -89,7 +89,14 @@ float orc_fp8_to_f32(uint8_t c) {
 /* Nearest code to f (ties to the even code), saturating at 448: the non-negative finite codes
  * 0x00..0x7E are increasing in value, so the nearest is found between the two codes that
  * bracket |f|. */
+static double fp8_value[0x7F]; /* the non-negative finite codes' values (filled once) */
+static int fp8_value_ready = 0;
+
 uint8_t orc_fp8_from_f32(float f) {
+  if (!fp8_value_ready) {
+    for (int c = 0; c < 0x7F; ++c) fp8_value[c] = orc_fp8_to_f32((uint8_t)c);
+    fp8_value_ready = 1;
+  }
   if (isnan(f)) return 0x7F;
   const uint8_t sign = signbit(f) ? 0x80 : 0x00;
   const double a = fabs((double)f);
@@ -97,9 +104,9 @@ uint8_t orc_fp8_from_f32(float f) {
   int lo = 0, hi = 0x7E; /* largest code with value <= a */
   while (lo < hi) {
     const int mid = (lo + hi + 1) / 2;
-    if ((double)orc_fp8_to_f32((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+    if (fp8_value[mid] <= a) lo = mid; else hi = mid - 1;
   }
-  const double vlo = orc_fp8_to_f32((uint8_t)lo), vhi = orc_fp8_to_f32((uint8_t)(lo + 1));
+  const double vlo = fp8_value[lo], vhi = fp8_value[lo + 1];
   int c;
   if (a - vlo < vhi - a) c = lo;
   else if (a - vlo > vhi - a) c = lo + 1;
