@@ -78,7 +78,17 @@ typedef struct {
   double rms_eps;
   double rope_theta;
   int qkv_bias;      /* 1: bq, bk, bv are used (Qwen2); 0: ignored */
+  int weight_format; /* MBK_WEIGHTS_BF16 (0): stream the bf16 weights as given.  MBK_WEIGHTS_FP8 (1): at
+                      * create the library quantizes every projection (Wq, Wk, Wv, Wo, Wgate, Wup, Wdown)
+                      * and the LM head's copy of the embedding to FP8 E4M3 with one fp32 scale per
+                      * output row (scale = row max |w| / 448; codes = w / scale rounded to nearest
+                      * even, saturating), owns those copies and streams them: about half the bytes
+                      * per token.  The embedding lookup, norm gains and biases stay bf16.  The MegaBake
+                      * website lists FP8 under "Next"; the format is this library's reading.  Needs
+                      * hidden and intermediate to be multiples of 16. */
 } mbk_config;
+
+enum { MBK_WEIGHTS_BF16 = 0, MBK_WEIGHTS_FP8 = 1 };
 
 /* Device pointers of one layer's bf16 tensors ([out][in] for matrices, [n] for vectors).
  * bq/bk/bv may be NULL when qkv_bias == 0. */
@@ -108,6 +118,12 @@ int mbk_create(const mbk_config *cfg, const mbk_weights *weights, void *kv_cache
  * two in [32, kv_capacity], num_pages >= 1 and kv_capacity / page_size (rounded up) <= 256. */
 int mbk_create_paged(const mbk_config *cfg, const mbk_weights *weights, void *kv_pool, int32_t num_pages,
                      int32_t page_size, int device, mbk_handle **out);
+
+/* FP8 copies of a bf16 matrix, exactly as mbk_create makes them for MBK_WEIGHTS_FP8: w (device bf16
+ * [rows][cols], cols even) -> q (device [rows][cols] E4M3 codes) and s (device fp32 [rows] scales).
+ * Asynchronous on `stream`.  Errors: MBK_ERR_INVALID_ARG for a NULL pointer, rows < 1 or an odd
+ * or non-positive cols. */
+int mbk_quantize_fp8(const void *w, int32_t rows, int32_t cols, void *q, float *s, void *stream);
 
 /* Paged handles: pages[q] (HOST array of n_pages distinct entries in [0, num_pages)) is the pool
  * page of logical page q; positions [0, min(kv_capacity, n_pages * page_size)) are then mapped and

@@ -15,7 +15,8 @@
 #include "mbk_sched.h"
 
 namespace mbk {
-const void* decode_kernel_ptr(bool greedy);
+const void* decode_kernel_ptr(bool greedy, bool fp8);
+cudaError_t launch_quantize_fp8(const uint16_t* w, int rows, int cols, uint8_t* q, float* s, cudaStream_t st);
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
 cudaError_t launch_kv_fill(const KernelParams& kp, int layer, const float* k_raw, const float* v_raw, int p0, int n,
                            cudaStream_t st);
@@ -51,6 +52,9 @@ struct mbk_handle {
   bool paged = false;
   int num_pages = 0, page_size = 0, max_pages = 0;
   int32_t* d_page_table = nullptr;
+  // FP8 weights (MBK_WEIGHTS_FP8): the library's E4M3 copies and their per-row scales
+  uint8_t* d_fp8 = nullptr;
+  float* d_wscale = nullptr;
   int mapped = 0;  // positions [0, mapped) have cache rows: kv_capacity, or what the page table covers
   unsigned long long* d_trace = nullptr;
   unsigned long long* d_inject = nullptr;
@@ -80,6 +84,7 @@ PlanShape shape_of(const mbk_config& c) {
   s.V = c.vocab;
   s.C = c.kv_capacity;
   s.qkv_bias = c.qkv_bias ? 1 : 0;
+  s.wb = c.weight_format == MBK_WEIGHTS_FP8 ? 1 : 2;
   return s;
 }
 
@@ -92,6 +97,7 @@ int env_int(const char* name, int dflt) {
 int config_check(const mbk_config* cfg) {
   if (!cfg) return MBK_ERR_INVALID_ARG;
   if (!(cfg->rms_eps >= 0.0) || !(cfg->rope_theta > 0.0) || !std::isfinite(cfg->rope_theta)) return MBK_ERR_INVALID_ARG;
+  if (cfg->weight_format != MBK_WEIGHTS_BF16 && cfg->weight_format != MBK_WEIGHTS_FP8) return MBK_ERR_INVALID_ARG;
   if (!validate_shape(shape_of(*cfg)).empty()) return MBK_ERR_INVALID_ARG;
   return MBK_OK;
 }
@@ -112,6 +118,8 @@ void free_all(mbk_handle* h) {
   cudaFree(h->d_amax_done);
   cudaFree(h->d_tokword);
   cudaFree(h->d_page_table);
+  cudaFree(h->d_fp8);
+  cudaFree(h->d_wscale);
   cudaFree(h->d_trace);
   cudaFree(h->d_inject);
   if (h->h_status) cudaFreeHost(h->h_status);
@@ -190,6 +198,12 @@ int mbk_create_paged(const mbk_config* cfg, const mbk_weights* weights, void* kv
   return create_impl(cfg, weights, kv_pool, kvl, device, out);
 }
 
+int mbk_quantize_fp8(const void* w, int32_t rows, int32_t cols, void* q, float* s, void* stream) {
+  if (!w || !q || !s || rows < 1 || cols < 2 || (cols & 1)) return MBK_ERR_INVALID_ARG;
+  return launch_quantize_fp8(reinterpret_cast<const uint16_t*>(w), rows, cols, reinterpret_cast<uint8_t*>(q), s,
+                             (cudaStream_t)stream) == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;
+}
+
 int mbk_set_page_table(mbk_handle* h, const int32_t* pages, int32_t n_pages, void* stream) {
   if (!h || !pages || !h->paged || n_pages < 1 || n_pages > h->max_pages) return MBK_ERR_INVALID_ARG;
   std::vector<char> used(h->num_pages, 0);
@@ -254,12 +268,56 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   h->page_size = kvl.page_size;
   h->max_pages = h->paged ? (cfg->kv_capacity + kvl.page_size - 1) / kvl.page_size : 0;
   h->mapped = h->paged ? 0 : cfg->kv_capacity;
+  // FP8 weights: the library's E4M3 copies (each matrix 256-byte aligned) and their row scales, per
+  // layer [q|k|v rows][Wo rows][gate rows][up rows][Wd rows], then the LM head's V rows
+  int wscale_layer = 0;
+  if (s.wb == 1) {
+    const int qd = s.nq * s.d, kvd = s.nkv * s.d;
+    const int slot_of[7] = {W_Q, W_K, W_V, W_O, W_GATE, W_UP, W_DOWN};
+    const int rows_of[7] = {qd, kvd, kvd, s.H, s.I, s.I, s.H};
+    const int cols_of[7] = {s.H, s.H, s.H, qd, s.H, s.H, s.I};
+    int soff[7];
+    for (int m = 0, o = 0; m < 7; ++m) {
+      soff[m] = o;
+      o += rows_of[m];
+      wscale_layer = o;
+    }
+    auto align = [](size_t b) { return (b + 255) / 256 * 256; };
+    size_t bytes = 0;
+    std::vector<size_t> off((size_t)s.L * 7);
+    for (int l = 0; l < s.L; ++l)
+      for (int m = 0; m < 7; ++m) {
+        off[(size_t)l * 7 + m] = bytes;
+        bytes += align((size_t)rows_of[m] * cols_of[m]);
+      }
+    const size_t lm_off = bytes;
+    bytes += align((size_t)s.V * s.H);
+    bool ok = cudaMalloc(&h->d_fp8, bytes) == cudaSuccess &&
+              cudaMalloc(&h->d_wscale, sizeof(float) * ((size_t)wscale_layer * s.L + s.V)) == cudaSuccess;
+    for (int l = 0; ok && l < s.L; ++l)
+      for (int m = 0; ok && m < 7; ++m) {
+        uint8_t* q = h->d_fp8 + off[(size_t)l * 7 + m];
+        ok = launch_quantize_fp8(reinterpret_cast<const uint16_t*>(wa.layers[l][slot_of[m]]), rows_of[m], cols_of[m], q,
+                                 h->d_wscale + (size_t)l * wscale_layer + soff[m], 0) == cudaSuccess;
+        wa.layers[l][slot_of[m]] = (uint64_t)(uintptr_t)q;
+      }
+    if (ok)
+      ok = launch_quantize_fp8(reinterpret_cast<const uint16_t*>(wa.embed), s.V, s.H, h->d_fp8 + lm_off,
+                               h->d_wscale + (size_t)wscale_layer * s.L, 0) == cudaSuccess;
+    wa.lm_head = (uint64_t)(uintptr_t)(h->d_fp8 + lm_off);
+    if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
+      free_all(h);
+      delete h;
+      return MBK_ERR_CUDA;
+    }
+  }
   PlanOptions opt;
   opt.smem_limit = smem_optin;
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
   opt.fuse_attention = env_int("MBK_FUSE_ATTENTION", -1);
   std::string err = build_plan(s, wa, prop.multiProcessorCount, opt, &h->plan);
   if (!err.empty()) {
+    free_all(h);
     delete h;
     return MBK_ERR_UNSUPPORTED;
   }
@@ -282,13 +340,15 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   h->grid = p.num_ctas;
 
   for (bool greedy : {false, true}) {  // the teacher-forced and the greedy instantiation
-    const void* kfn = decode_kernel_ptr(greedy);
+    const void* kfn = decode_kernel_ptr(greedy, s.wb == 1);
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess) {
+      free_all(h);
       delete h;
       return MBK_ERR_CUDA;
     }
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, kThreads, p.smem_bytes) != cudaSuccess || per_sm < 1) {
+      free_all(h);
       delete h;
       return MBK_ERR_UNSUPPORTED;
     }
@@ -380,6 +440,9 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   kp.page_shift = 0;
   while (h->paged && (1 << kp.page_shift) < h->page_size) ++kp.page_shift;
   kp.page_elems = h->paged ? (unsigned long long)s.L * 2 * s.nkv * h->page_size * s.d : 0ull;
+  kp.wbytes = s.wb;
+  kp.wscale_layer = wscale_layer;
+  kp.wscale = h->d_wscale;
   *out = h;
   return MBK_OK;
 }
@@ -421,7 +484,8 @@ int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, i
     h->inject_armed = false;
   }
   void* args[] = {&kp, &sp};
-  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(sp.greedy != 0), dim3(h->grid), dim3(kThreads), args,
+  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(sp.greedy != 0, h->kp.wbytes == 1), dim3(h->grid),
+                                              dim3(kThreads), args,
                                               (size_t)h->plan.smem_bytes, (cudaStream_t)stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;

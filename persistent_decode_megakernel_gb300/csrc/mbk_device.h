@@ -49,6 +49,12 @@ struct KernelParams {
   const int32_t* page_table;
   int page_size, page_shift;
   unsigned long long page_elems;  // bf16 elements of one page: L * 2 * nkv * page_size * d
+  // Streamed projection weights: bf16 (wbytes 2, wscale null) or FP8 E4M3 copies (wbytes 1) with one
+  // fp32 scale per output row: per layer [q|k|v rows][Wo rows][gate rows][up rows][Wd rows]
+  // (wscale_layer floats), then the LM head's V rows.
+  int wbytes;
+  int wscale_layer;
+  const float* wscale;
 };
 
 // Changes every step.

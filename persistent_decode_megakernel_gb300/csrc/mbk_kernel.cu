@@ -485,9 +485,39 @@ __device__ __forceinline__ float sum2(unsigned long long v) {
 }
 // bf16 pair in one 32-bit word -> fp32x2 {element 2i, element 2i+1}
 __device__ __forceinline__ unsigned long long bf2(uint32_t w) { return pack2(w << 16, w & 0xffff0000u); }
+// Two FP8 E4M3 weights (low byte first) as a packed fp32 pair: E4M3 -> f16 is exact (one
+// instruction for both), then f16 -> f32.  (Re-basing the f16 bits as fp32 with integer operations
+// instead of the two conversions measured slower.)
+__device__ __forceinline__ unsigned long long f8x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(two & 0xffffu)));
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(h2));
+  return pack2(__float_as_uint(lo), __float_as_uint(hi));
+}
+// A weight "vector": 8 consecutive weights of a row, 16 bytes of bf16 or (F8) 8 bytes of E4M3 codes
+// (held in .x and .y).  wpair<F8>(w, j) gives weights 2j and 2j + 1 as a packed fp32 pair.
+template <bool F8>
+__device__ __forceinline__ uint4 wload(const unsigned char* row, int v) {
+  if constexpr (F8) {
+    const uint2 w = reinterpret_cast<const uint2*>(row)[v];
+    return make_uint4(w.x, w.y, 0u, 0u);
+  } else {
+    return reinterpret_cast<const uint4*>(row)[v];
+  }
+}
+template <bool F8>
+__device__ __forceinline__ unsigned long long wpair(const uint4& w, int j) {
+  if constexpr (F8)
+    return f8x2(j == 0 ? w.x : j == 1 ? (w.x >> 16) : j == 2 ? w.y : (w.y >> 16));
+  else
+    return bf2(j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w);
+}
 
+template <bool F8>
 __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const float* x, float* res, float scale) {
-  const int nvec = in >> 3;  // 16-byte vectors per row
+  const int nvec = in >> 3;  // 8-weight vectors per row
   const int gpr = (int)t.gpr, gshift = 31 - __clz(gpr);
   // warp = rw * gpr + slice; warps beyond the last whole group (rw >= rpp) take no rows
   const int slice = c.warp & (gpr - 1), rw = c.warp >> gshift, rpp = kComputeWarps >> gshift;
@@ -510,7 +540,7 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
     xp[k][2] = pack2(__float_as_uint(q.x), __float_as_uint(q.y));
     xp[k][3] = pack2(__float_as_uint(q.z), __float_as_uint(q.w));
   }
-  const size_t row_bytes = (size_t)in * 2;
+  const size_t row_bytes = (size_t)in * (F8 ? 1 : 2);
   int rbase = 0;
   for (uint32_t k0 = 0; k0 < t.nchunks; k0 += kGemvBatch) {
     const int nb = (int)min((uint32_t)kGemvBatch, t.nchunks - k0);
@@ -523,7 +553,7 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
     const int n2 = nb > 2 ? (int)stage_rows_at(c, 2) : 0;
     const int n3 = nb > 3 ? (int)stage_rows_at(c, 3) : 0;
     const int total = n0 + n1 + n2 + n3;
-    auto row_of = [&](int r) -> const uint4* {
+    auto row_of = [&](int r) -> const unsigned char* {
       const unsigned char* base = s0;
       if (r >= n0) {
         r -= n0;
@@ -537,12 +567,12 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
           }
         }
       }
-      return reinterpret_cast<const uint4*>(base + (size_t)r * row_bytes);
+      return base + (size_t)r * row_bytes;
     };
     // four rows per iteration (independent accumulator chains); the loop bound is uniform across
     // the warp (shuffles below)
     for (int ra = rstart; ra < total; ra += 4 * rpp) {
-      const uint4* R[4];
+      const unsigned char* R[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) R[i] = row_of(ra + i * rpp < total ? ra + i * rpp : ra);
       unsigned long long acc[4][2];
@@ -554,17 +584,17 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
         const int vi = v < v1 ? v : 0;  // clamped index; its x registers are zero
         uint4 w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = R[i][vi];
+        for (int i = 0; i < 4; ++i) w[i] = wload<F8>(R[i], vi);
         if (v >= v1) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          acc[i][0] = ffma2(bf2(w[i].x), xp[k][0], acc[i][0]);
-          acc[i][1] = ffma2(bf2(w[i].y), xp[k][1], acc[i][1]);
-          acc[i][0] = ffma2(bf2(w[i].z), xp[k][2], acc[i][0]);
-          acc[i][1] = ffma2(bf2(w[i].w), xp[k][3], acc[i][1]);
+          acc[i][0] = ffma2(wpair<F8>(w[i], 0), xp[k][0], acc[i][0]);
+          acc[i][1] = ffma2(wpair<F8>(w[i], 1), xp[k][1], acc[i][1]);
+          acc[i][0] = ffma2(wpair<F8>(w[i], 2), xp[k][2], acc[i][0]);
+          acc[i][1] = ffma2(wpair<F8>(w[i], 3), xp[k][3], acc[i][1]);
         }
       }
       float sm[4];
@@ -590,7 +620,8 @@ __device__ __forceinline__ void gemv_xreg(Ctx& c, const Task& t, int in, const f
 constexpr int kDotRound = 2;  // 16-byte vectors per lane per round of a row dot product
 // Loads of one round are issued unconditionally (an index past the row end is clamped to the row
 // start and its weights zeroed), so they are all in flight before the first FMA.
-__device__ __forceinline__ float dot_row(const Ctx& c, const uint4* row, const float4* xlo, const float4* xhi, int nvec) {
+template <bool F8>
+__device__ __forceinline__ float dot_row(const Ctx& c, const unsigned char* row, const float4* xlo, const float4* xhi, int nvec) {
   unsigned long long a0 = 0ull, a1 = 0ull;
 #pragma unroll 1
   for (int v0 = c.lane; v0 < nvec; v0 += 32 * kDotRound) {
@@ -600,23 +631,24 @@ __device__ __forceinline__ float dot_row(const Ctx& c, const uint4* row, const f
     for (int it = 0; it < kDotRound; ++it) {
       const int v = v0 + 32 * it;
       const int vi = v < nvec ? v : v0;
-      w[it] = row[vi];
+      w[it] = wload<F8>(row, vi);
       p[it] = xlo[vi];
       q[it] = xhi[vi];
       if (v >= nvec) w[it] = make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int it = 0; it < kDotRound; ++it) {
-      a0 = ffma2(bf2(w[it].x), pack2(__float_as_uint(p[it].x), __float_as_uint(p[it].y)), a0);
-      a1 = ffma2(bf2(w[it].y), pack2(__float_as_uint(p[it].z), __float_as_uint(p[it].w)), a1);
-      a0 = ffma2(bf2(w[it].z), pack2(__float_as_uint(q[it].x), __float_as_uint(q[it].y)), a0);
-      a1 = ffma2(bf2(w[it].w), pack2(__float_as_uint(q[it].z), __float_as_uint(q[it].w)), a1);
+      a0 = ffma2(wpair<F8>(w[it], 0), pack2(__float_as_uint(p[it].x), __float_as_uint(p[it].y)), a0);
+      a1 = ffma2(wpair<F8>(w[it], 1), pack2(__float_as_uint(p[it].z), __float_as_uint(p[it].w)), a1);
+      a0 = ffma2(wpair<F8>(w[it], 2), pack2(__float_as_uint(q[it].x), __float_as_uint(q[it].y)), a0);
+      a1 = ffma2(wpair<F8>(w[it], 3), pack2(__float_as_uint(q[it].z), __float_as_uint(q[it].w)), a1);
     }
   }
   return sum2(a0) + sum2(a1);
 }
 // Two rows against the same x (gate and up rows): the x vectors are loaded once for both.
-__device__ __forceinline__ void dot_row2(const Ctx& c, const uint4* ra, const uint4* rb, const float4* xlo,
+template <bool F8>
+__device__ __forceinline__ void dot_row2(const Ctx& c, const unsigned char* ra, const unsigned char* rb, const float4* xlo,
                                          const float4* xhi, int nvec, float& sa, float& sb) {
   unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
 #pragma unroll 1
@@ -627,8 +659,8 @@ __device__ __forceinline__ void dot_row2(const Ctx& c, const uint4* ra, const ui
     for (int it = 0; it < 2; ++it) {
       const int v = v0 + 32 * it;
       const int vi = v < nvec ? v : v0;
-      wa[it] = ra[vi];
-      wb[it] = rb[vi];
+      wa[it] = wload<F8>(ra, vi);
+      wb[it] = wload<F8>(rb, vi);
       p[it] = xlo[vi];
       q[it] = xhi[vi];
       if (v >= nvec) wa[it] = wb[it] = make_uint4(0u, 0u, 0u, 0u);
@@ -639,14 +671,14 @@ __device__ __forceinline__ void dot_row2(const Ctx& c, const uint4* ra, const ui
       const unsigned long long x1 = pack2(__float_as_uint(p[it].z), __float_as_uint(p[it].w));
       const unsigned long long x2 = pack2(__float_as_uint(q[it].x), __float_as_uint(q[it].y));
       const unsigned long long x3 = pack2(__float_as_uint(q[it].z), __float_as_uint(q[it].w));
-      a0 = ffma2(bf2(wa[it].x), x0, a0);
-      a1 = ffma2(bf2(wa[it].y), x1, a1);
-      a0 = ffma2(bf2(wa[it].z), x2, a0);
-      a1 = ffma2(bf2(wa[it].w), x3, a1);
-      b0 = ffma2(bf2(wb[it].x), x0, b0);
-      b1 = ffma2(bf2(wb[it].y), x1, b1);
-      b0 = ffma2(bf2(wb[it].z), x2, b0);
-      b1 = ffma2(bf2(wb[it].w), x3, b1);
+      a0 = ffma2(wpair<F8>(wa[it], 0), x0, a0);
+      a1 = ffma2(wpair<F8>(wa[it], 1), x1, a1);
+      a0 = ffma2(wpair<F8>(wa[it], 2), x2, a0);
+      a1 = ffma2(wpair<F8>(wa[it], 3), x3, a1);
+      b0 = ffma2(wpair<F8>(wb[it], 0), x0, b0);
+      b1 = ffma2(wpair<F8>(wb[it], 1), x1, b1);
+      b0 = ffma2(wpair<F8>(wb[it], 2), x2, b0);
+      b1 = ffma2(wpair<F8>(wb[it], 3), x3, b1);
     }
   }
   sa = sum2(a0) + sum2(a1);
@@ -657,7 +689,7 @@ struct BatchRows {
   const unsigned char* s[kGemvBatch];
   int n[kGemvBatch];
   int total;
-  __device__ __forceinline__ const uint4* row(int r, size_t row_bytes) const {
+  __device__ __forceinline__ const unsigned char* row(int r, size_t row_bytes) const {
     const unsigned char* base = s[0];
     if (r >= n[0]) {
       r -= n[0];
@@ -671,7 +703,7 @@ struct BatchRows {
         }
       }
     }
-    return reinterpret_cast<const uint4*>(base + (size_t)r * row_bytes);
+    return base + (size_t)r * row_bytes;
   }
 };
 __device__ __forceinline__ BatchRows batch_wait(Ctx& c, int nb) {
@@ -707,6 +739,7 @@ __device__ __forceinline__ float res_row(const float* res, int i, int gpr) {
 // lane owning output elements.  One barrier later the blocks of each head are merged by their
 // log-sum-exp weights.  Writes per query head o (normalised over this split) and (m, l); scores
 // are kept in base-2 units (scaled by log2 e), so m is too.
+template <bool F8>
 __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, float* res) {
   const KernelParams& P = *c.P;
   const bool wo = (t.flags & TF_WO) != 0;  // fused O projection: KV head in aux, output rows row0..
@@ -925,8 +958,10 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
         for (int j = 0; j < 8; ++j) ov[k][j] *= inv;
       }
     }
-    const size_t row_bytes = (size_t)O * 2;
+    const size_t row_bytes = (size_t)O * (F8 ? 1 : 2);
     unsigned long long* out = P.words + t.out_off;
+    // FP8: the scales of Wo's rows (one per full row, shared by every KV head's segment)
+    const float* rsc = F8 ? P.wscale + (size_t)l * P.wscale_layer + (P.nq + 2 * P.nkv) * d + t.row0 : nullptr;
     int rbase = 0;
 #pragma unroll 1
     for (uint32_t k0 = 1; k0 < t.nchunks; k0 += kGemvBatch) {
@@ -934,24 +969,35 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
       const BatchRows b = batch_wait(c, nb);
 #pragma unroll 1
       for (int q = c.warp; q < b.total; q += kComputeWarps) {
-        const uint4* row = b.row(q, row_bytes);
+        const unsigned char* row = b.row(q, row_bytes);
         float a = 0.f;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int v = c.lane + 32 * k;
           if (v < nvec) {
-            const uint4 w = row[v];
-            a = fmaf(bf16_lo(w.x), ov[k][0], a);
-            a = fmaf(bf16_hi(w.x), ov[k][1], a);
-            a = fmaf(bf16_lo(w.y), ov[k][2], a);
-            a = fmaf(bf16_hi(w.y), ov[k][3], a);
-            a = fmaf(bf16_lo(w.z), ov[k][4], a);
-            a = fmaf(bf16_hi(w.z), ov[k][5], a);
-            a = fmaf(bf16_lo(w.w), ov[k][6], a);
-            a = fmaf(bf16_hi(w.w), ov[k][7], a);
+            if constexpr (F8) {
+              const uint4 w = wload<true>(row, v);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const unsigned long long wp = wpair<true>(w, j);
+                a = fmaf(__uint_as_float((uint32_t)wp), ov[k][2 * j], a);
+                a = fmaf(__uint_as_float((uint32_t)(wp >> 32)), ov[k][2 * j + 1], a);
+              }
+            } else {
+              const uint4 w = reinterpret_cast<const uint4*>(row)[v];
+              a = fmaf(bf16_lo(w.x), ov[k][0], a);
+              a = fmaf(bf16_hi(w.x), ov[k][1], a);
+              a = fmaf(bf16_lo(w.y), ov[k][2], a);
+              a = fmaf(bf16_hi(w.y), ov[k][3], a);
+              a = fmaf(bf16_lo(w.z), ov[k][4], a);
+              a = fmaf(bf16_hi(w.z), ov[k][5], a);
+              a = fmaf(bf16_lo(w.w), ov[k][6], a);
+              a = fmaf(bf16_hi(w.w), ov[k][7], a);
+            }
           }
         }
         a = warp_sum(a);
+        if constexpr (F8) a *= rsc[rbase + q];
         if (c.lane == 0) st_word(out + rbase + q, c.tag, a);
       }
       stages_release(c, (unsigned)nb);
@@ -1107,6 +1153,7 @@ __device__ __noinline__ void greedy_boundary(const KernelParams* P, const StepPa
 // path after the inputs arrive is one block barrier, the row's dot products and the output store:
 // weight stages are checked before the inputs are polled, and the norm scale (a reduction of the
 // per-warp sums of squares) is computed by every warp alongside its dot products.
+template <bool F8>
 __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, float* res, float* add) {
   const KernelParams& P = *c.P;
   const int l = t.layer, type = t.type, n = (int)t.nrows;
@@ -1211,12 +1258,23 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
   // 3. the projection and its outputs
   float* logits = c.logits + t.row0;
   const bool pairs = (f & TF_PAIRS) != 0;
+  // FP8: the per-row weight scales of the task's rows (gate/up: gate rows, then up rows I further on)
+  const float* rsc = nullptr;
+  if constexpr (F8) {
+    const int qkv = (P.nq + 2 * P.nkv) * P.d;
+    const size_t base = type == T_LMHEAD ? (size_t)P.L * P.wscale_layer
+                                         : (size_t)l * P.wscale_layer + (type == T_QKV ? 0
+                                                                         : type == T_OPROJ ? qkv
+                                                                         : type == T_GATEUP ? qkv + P.H
+                                                                                            : qkv + P.H + 2 * P.I);
+    rsc = P.wscale + base + t.row0;
+  }
   if (direct) {
     // one warp per row (gate/up: per row pair); lane 0 writes the output as soon as its row is done
     const int nvec = in >> 3;
     const float4* xlo = reinterpret_cast<const float4*>(sv);
     const float4* xhi = reinterpret_cast<const float4*>(sv + (in >> 1));
-    const size_t row_bytes = (size_t)in * 2;
+    const size_t row_bytes = (size_t)in * (F8 ? 1 : 2);
     int rbase = 0;
 #pragma unroll 1
     for (uint32_t k0 = 0; k0 < t.nchunks; k0 += kGemvBatch) {
@@ -1227,16 +1285,20 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
       for (int q = c.warp; q < rows; q += kComputeWarps) {
         float a, u = 0.f;
         if (pairs) {
-          dot_row2(c, b.row(q, row_bytes), b.row(n + q, row_bytes), xlo, xhi, nvec, a, u);
+          dot_row2<F8>(c, b.row(q, row_bytes), b.row(n + q, row_bytes), xlo, xhi, nvec, a, u);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             a += __shfl_xor_sync(0xffffffffu, a, o);
             u += __shfl_xor_sync(0xffffffffu, u, o);
           }
         } else {
-          a = warp_sum(dot_row(c, b.row(q, row_bytes), xlo, xhi, nvec));
+          a = warp_sum(dot_row<F8>(c, b.row(q, row_bytes), xlo, xhi, nvec));
         }
         if (scale == 0.f) scale = norm_scale();
+        if constexpr (F8) {
+          a *= rsc[rbase + q];
+          if (pairs) u *= rsc[P.I + q];
+        }
         if (c.lane == 0) emit_row(c, type, out, rbase + q, a * scale, u * scale, add, logits);
       }
       stages_release(c, (unsigned)nb);
@@ -1244,11 +1306,17 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
     }
   } else {
     // warps share rows: partial sums in res, summed in a fixed order after the barrier
-    gemv_xreg(c, t, in, sv, res, norm_scale());
+    gemv_xreg<F8>(c, t, in, sv, res, norm_scale());
     const int gpr = (int)t.gpr;
 #pragma unroll 1
-    for (int i = c.ctid; i < n; i += kCT)
-      emit_row(c, type, out, i, res_row(res, i, gpr), pairs ? res_row(res, n + i, gpr) : 0.f, add, logits);
+    for (int i = c.ctid; i < n; i += kCT) {
+      float a = res_row(res, i, gpr), u = pairs ? res_row(res, n + i, gpr) : 0.f;
+      if constexpr (F8) {
+        a *= rsc[i];
+        if (pairs) u *= rsc[P.I + i];
+      }
+      emit_row(c, type, out, i, a, u, add, logits);
+    }
   }
 }
 
@@ -1396,7 +1464,7 @@ __device__ __forceinline__ void produce(const KernelParams& P, const StepParams&
         } else if (rows & kStridedRows) {
           // one KV head's columns of Wo: a segment per output row, packed back to back
           const unsigned n = rows & ~kStridedRows, seg = bytes / n;
-          const size_t stride = (size_t)P.nq * P.d * 2;
+          const size_t stride = (size_t)P.nq * P.d * P.wbytes;
           unsigned char* dst = acquire(bytes, n);
           if (!dst) {
             q = 1;
@@ -1433,7 +1501,7 @@ __device__ __forceinline__ void stage_tasks(const Task* src, Task* dst, int n, i
 
 // kGreedy: greedy decoding (the argmax of each step's logits is the next step's token).  A separate
 // instantiation, so that the teacher-forced kernel carries none of its state in registers.
-template <bool kGreedy>
+template <bool kGreedy, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const __grid_constant__ StepParams S) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
@@ -1531,9 +1599,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (P.trace != nullptr && c.ctid == 0) P.trace[(size_t)ti * 4 + 3] = 0;
     trace_mark(c, 0);
     if (t.type == T_ATTN)
-      task_attn(c, t, sv, res);
+      task_attn<kF8>(c, t, sv, res);
     else
-      task_gemv(c, t, sv, res, add);
+      task_gemv<kF8>(c, t, sv, res, add);
     compute_sync();  // the next task reuses the shared vectors
     trace_mark(c, 2);
   }
@@ -1593,8 +1661,43 @@ __global__ void kv_fill_kernel(uint16_t* kv, int layer, const float* k_raw, cons
 
 // Launch helpers used by the C ABI (mbk_api.cu).
 namespace mbk {
-const void* decode_kernel_ptr(bool greedy) {
-  return greedy ? reinterpret_cast<const void*>(&decode_kernel<true>) : reinterpret_cast<const void*>(&decode_kernel<false>);
+const void* decode_kernel_ptr(bool greedy, bool fp8) {
+  if (fp8)
+    return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, true>)
+                  : reinterpret_cast<const void*>(&decode_kernel<false, true>);
+  return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, false>)
+                : reinterpret_cast<const void*>(&decode_kernel<false, false>);
+}
+
+// FP8 copies of a bf16 matrix [rows][cols] (cols even): per row the scale amax / 448 (1 for an
+// all-zero row) and the E4M3 codes of w / scale (nearest, ties to even, saturating at 448).  One
+// block per row at a time.
+__global__ void quantize_fp8_kernel(const uint16_t* w, int rows, int cols, uint8_t* q, float* s) {
+  __shared__ float red[32];
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint16_t* wr = w + (size_t)r * cols;
+    float amax = 0.f;
+    for (int k = threadIdx.x; k < cols; k += blockDim.x) amax = fmaxf(amax, fabsf(bf16_to_f32(wr[k])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (threadIdx.x == 0) s[r] = sc;
+    for (int k = 2 * threadIdx.x; k < cols; k += 2 * blockDim.x) {
+      const float lo = __fdiv_rn(bf16_to_f32(wr[k]), sc), hi = __fdiv_rn(bf16_to_f32(wr[k + 1]), sc);
+      unsigned short two;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(hi), "f"(lo));  // lo -> the low byte
+      *reinterpret_cast<unsigned short*>(q + (size_t)r * cols + k) = two;
+    }
+    __syncthreads();  // red[] is reused by the next row
+  }
+}
+cudaError_t launch_quantize_fp8(const uint16_t* w, int rows, int cols, uint8_t* q, float* s, cudaStream_t st) {
+  quantize_fp8_kernel<<<rows < 2048 ? rows : 2048, 256, 0, st>>>(w, rows, cols, q, s);
+  return cudaGetLastError();
 }
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st) {
   rope_table_kernel<<<264, 256, 0, st>>>(out, C, d, theta);

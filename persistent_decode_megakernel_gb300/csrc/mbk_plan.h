@@ -124,6 +124,7 @@ constexpr unsigned kLmPrefetchLead = 24;           // ... issued this many chunk
 struct PlanShape {
   int L, H, I, nq, nkv, d, V, C;
   int qkv_bias;
+  int wb = 2;  // bytes of a streamed projection weight: 2 (bf16) or 1 (FP8 E4M3 with per-row scales)
 };
 
 }  // namespace mbk

@@ -89,8 +89,10 @@ std::string validate_shape(const PlanShape& s) {
   if (s.nq / s.nkv > 16) return "at most 16 query heads per KV head";
   if (s.H % 8 || s.I % 8) return "hidden and intermediate must be multiples of 8";
   int max_in = std::max(std::max(s.H, s.I), s.nq * s.d);
-  if (max_in * 2 > kStageBytes) {
-    snprintf(buf, sizeof buf, "a weight row of %d bf16 exceeds one %d-byte stage", max_in, kStageBytes);
+  if (s.wb != 1 && s.wb != 2) return "weights must be bf16 or FP8";
+  if (s.wb == 1 && (s.H % 16 || s.I % 16)) return "FP8 weights need hidden and intermediate sizes that are multiples of 16";
+  if (max_in * s.wb > kStageBytes) {
+    snprintf(buf, sizeof buf, "a weight row of %d elements exceeds one %d-byte stage", max_in, kStageBytes);
     return buf;
   }
   if (s.H > kMaxTaskRows) return "hidden larger than the per-task result capacity";
@@ -276,12 +278,13 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       for (const Seg& sg : segs_for(r0, r1)) add_chunks(cta_chunks[cta], sg);
       t.nchunks = (uint32_t)(cta_chunks[cta].size() - t.chunk0);
       for (uint32_t c = t.chunk0; c < t.chunk0 + t.nchunks; ++c) cta_bytes[cta] += cta_chunks[cta][c].bytes;
-      gemv_layout(cta_chunks[cta], t, row_bytes / 2, res_per_row);
+      gemv_layout(cta_chunks[cta], t, row_bytes / s.wb, res_per_row);
       cta_tasks[cta].push_back(t);
     }
   };
 
-  const int hb = s.H * 2;
+  const int hb = s.H * s.wb;  // bytes of a weight row over the hidden size
+  const uint64_t lm_base = w.lm_head ? w.lm_head : w.embed;
   for (int l = 0; l < s.L; ++l) {
     const auto& W = w.layers[l];
     gemv_op(T_QKV, l, qd + 2 * kvd, 1, hb, [&](int r0, int r1) {
@@ -298,7 +301,7 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       // attention with the O projection: per KV head, its columns of Wo split by output rows over
       // the CTAs; each task recomputes the head's attention (every task of a head rounds the
       // appended K/V row identically; the first one writes it to the cache)
-      const int seg = g * s.d * 2;                        // bytes of one row's segment
+      const int seg = g * s.d * s.wb;                     // bytes of one row's segment
       const int rpc = kStageBytes / seg;                  // segments per stage
       const int per_head = std::max(1, std::min(s.H, std::min(max_tasks, num_ctas) / s.nkv));
       for (int kvh = 0; kvh < s.nkv; ++kvh) {
@@ -323,7 +326,7 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
           for (int r = r0; r < r1; r += rpc) {
             const int n = std::min(rpc, r1 - r);
             Chunk ch;
-            ch.src = W[W_O] + (uint64_t)r * qd * 2 + (uint64_t)kvh * seg;
+            ch.src = W[W_O] + (uint64_t)r * qd * s.wb + (uint64_t)kvh * seg;
             ch.bytes = (uint32_t)(n * seg);
             ch.rows = (uint32_t)n | kStridedRows;
             cta_chunks[cta].push_back(ch);
@@ -359,14 +362,14 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       }
     }
     if (!p.fused_attn)
-      gemv_op(T_OPROJ, l, s.H, 1, qd * 2, [&](int r0, int r1) {
-        return std::vector<Seg>{Seg{W[W_O], qd * 2, r0, r1 - r0}};
+      gemv_op(T_OPROJ, l, s.H, 1, qd * s.wb, [&](int r0, int r1) {
+        return std::vector<Seg>{Seg{W[W_O], qd * s.wb, r0, r1 - r0}};
       });
     gemv_op(T_GATEUP, l, s.I, 2, hb, [&](int r0, int r1) {
       return std::vector<Seg>{Seg{W[W_GATE], hb, r0, r1 - r0}, Seg{W[W_UP], hb, r0, r1 - r0}};
     });
-    gemv_op(T_DOWN, l, s.H, 1, s.I * 2, [&](int r0, int r1) {
-      return std::vector<Seg>{Seg{W[W_DOWN], s.I * 2, r0, r1 - r0}};
+    gemv_op(T_DOWN, l, s.H, 1, s.I * s.wb, [&](int r0, int r1) {
+      return std::vector<Seg>{Seg{W[W_DOWN], s.I * s.wb, r0, r1 - r0}};
     });
   }
   {
@@ -386,7 +389,7 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
       t.row0 = (uint32_t)r0;
       t.nrows = (uint32_t)(r1 - r0);
       t.chunk0 = (uint32_t)cta_chunks[cta].size();
-      add_chunks(cta_chunks[cta], Seg{w.embed, hb, r0, r1 - r0});
+      add_chunks(cta_chunks[cta], Seg{lm_base, hb, r0, r1 - r0});
       t.nchunks = (uint32_t)(cta_chunks[cta].size() - t.chunk0);
       for (uint32_t c = t.chunk0; c < t.chunk0 + t.nchunks; ++c) cta_bytes[cta] += cta_chunks[cta][c].bytes;
       gemv_layout(cta_chunks[cta], t, s.H, 1);
@@ -439,26 +442,28 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
   const int qd = s.nq * s.d, kvd = s.nkv * s.d;
   // tensor extents (base -> bytes) for bounds checks
   std::map<uint64_t, uint64_t> extent;
-  extent[w.embed] = (uint64_t)s.V * s.H * 2;
+  const uint64_t wb = (uint64_t)s.wb;
+  const uint64_t lm_base = w.lm_head ? w.lm_head : w.embed;
+  extent[lm_base] = (uint64_t)s.V * s.H * wb;
   for (int l = 0; l < s.L; ++l) {
     const auto& W = w.layers[l];
-    extent[W[W_Q]] = (uint64_t)qd * s.H * 2;
-    extent[W[W_K]] = (uint64_t)kvd * s.H * 2;
-    extent[W[W_V]] = (uint64_t)kvd * s.H * 2;
-    extent[W[W_O]] = (uint64_t)s.H * qd * 2;
-    extent[W[W_GATE]] = (uint64_t)s.I * s.H * 2;
-    extent[W[W_UP]] = (uint64_t)s.I * s.H * 2;
-    extent[W[W_DOWN]] = (uint64_t)s.H * s.I * 2;
+    extent[W[W_Q]] = (uint64_t)qd * s.H * wb;
+    extent[W[W_K]] = (uint64_t)kvd * s.H * wb;
+    extent[W[W_V]] = (uint64_t)kvd * s.H * wb;
+    extent[W[W_O]] = (uint64_t)s.H * qd * wb;
+    extent[W[W_GATE]] = (uint64_t)s.I * s.H * wb;
+    extent[W[W_UP]] = (uint64_t)s.I * s.H * wb;
+    extent[W[W_DOWN]] = (uint64_t)s.H * s.I * wb;
   }
   std::map<uint64_t, std::vector<int>> covered;  // tensor base -> per-row count
   auto row_bytes_of = [&](uint64_t base) -> int {
-    if (base == w.embed) return s.H * 2;
+    if (base == lm_base) return s.H * s.wb;
     for (int l = 0; l < s.L; ++l) {
       const auto& W = w.layers[l];
-      if (base == W[W_O]) return qd * 2;
-      if (base == W[W_DOWN]) return s.I * 2;
+      if (base == W[W_O]) return qd * s.wb;
+      if (base == W[W_DOWN]) return s.I * s.wb;
     }
-    return s.H * 2;
+    return s.H * s.wb;
   };
   for (auto& e : extent) covered[e.first].assign(e.second / row_bytes_of(e.first), 0);
   // fused plans stream Wo as per-KV-head segments of each row: (row, head) -> count
@@ -509,13 +514,13 @@ std::string check_plan(const PlanShape& s, const WeightAddrs& w, const Plan& p) 
             (uint32_t)ph.src != 0u)
           return "bad attention placeholder";
         const uint64_t wo = w.layers[t.layer][W_O];
-        const uint32_t seg = (uint32_t)((s.nq / s.nkv) * s.d * 2);
+        const uint32_t seg = (uint32_t)((s.nq / s.nkv) * s.d * s.wb);
         uint32_t r = t.row0;
         for (uint32_t k = t.chunk0 + 1; k < t.chunk0 + t.nchunks; ++k) {
           const Chunk& ch = p.chunks[k];
           const uint32_t n = ch.rows & ~kStridedRows;
           if (!(ch.rows & kStridedRows) || n == 0 || ch.bytes != n * seg || ch.bytes > (uint32_t)kStageBytes || ch.src % 16 ||
-              seg % 16 || ch.src != wo + (uint64_t)r * qd * 2 + (uint64_t)t.aux * seg)
+              seg % 16 || ch.src != wo + (uint64_t)r * qd * s.wb + (uint64_t)t.aux * seg)
             return "bad Wo segment chunk";
           for (uint32_t q = 0; q < n; ++q) covered_wo[wo][(size_t)(r + q) * s.nkv + t.aux] += 1;
           r += n;

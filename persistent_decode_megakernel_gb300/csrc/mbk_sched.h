@@ -14,6 +14,7 @@ namespace mbk {
 enum WeightSlot { W_ATTN_NORM, W_Q, W_K, W_V, W_BQ, W_BK, W_BV, W_O, W_MLP_NORM, W_GATE, W_UP, W_DOWN, W_NSLOTS };
 struct WeightAddrs {
   uint64_t embed = 0, final_norm = 0;
+  uint64_t lm_head = 0;  // rows the LM head streams: the embedding (bf16) or its FP8 copy; 0 = embed
   std::vector<std::array<uint64_t, W_NSLOTS>> layers;
 };
 

@@ -21,7 +21,7 @@
 #include "mbk_sched.h"
 
 namespace mbk {
-const void* decode_kernel_ptr(bool greedy);
+const void* decode_kernel_ptr(bool greedy, bool fp8);
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
 }  // namespace mbk
 
@@ -83,6 +83,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
   s.V = cfg->vocab;
   s.C = cfg->kv_capacity;
   s.qkv_bias = cfg->qkv_bias ? 1 : 0;
+  if (cfg->weight_format != MBK_WEIGHTS_BF16) return MBK_ERR_INVALID_ARG;  // this entry streams the bf16 weights
   if (!validate_shape(s).empty() || !(cfg->rms_eps >= 0.0) || !(cfg->rope_theta > 0.0)) return MBK_ERR_INVALID_ARG;
   if (((uintptr_t)weights->embed | (uintptr_t)kv_cache) & 15u) return MBK_ERR_INVALID_ARG;
 
@@ -101,7 +102,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     cudaDeviceGetAttribute(&D.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (!coop) return MBK_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(decode_kernel_ptr(false), cudaFuncAttributeMaxDynamicSharedMemorySize, D.smem_optin) != cudaSuccess)
+    if (cudaFuncSetAttribute(decode_kernel_ptr(false, false), cudaFuncAttributeMaxDynamicSharedMemorySize, D.smem_optin) != cudaSuccess)
       return MBK_ERR_CUDA;
     D.base = static_cast<unsigned char*>(p);
     D.num_sms = prop.multiProcessorCount;
@@ -208,6 +209,9 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     kp.page_size = s.C;
     kp.page_shift = 0;
     kp.page_elems = 0;
+    kp.wbytes = 2;  // bf16 weights as given
+    kp.wscale_layer = 0;
+    kp.wscale = nullptr;
     D.plan = plan;
     D.resident_key = key;
   }
@@ -234,7 +238,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
   sp.tokword = nullptr;
   KernelParams kp = D.kp;
   void* args[] = {&kp, &sp};
-  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(false), dim3(D.plan.num_ctas), dim3(kThreads), args,
+  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(false, false), dim3(D.plan.num_ctas), dim3(kThreads), args,
                                               (size_t)D.plan.smem_bytes, st);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;

@@ -28,7 +28,7 @@ MBK_ERR_STATE = -6
 EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
             "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps",
-            "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table")
+            "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -42,7 +42,10 @@ class MbkConfig(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("intermediate", ctypes.c_int),
                 ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("vocab", ctypes.c_int), ("kv_capacity", ctypes.c_int), ("rms_eps", ctypes.c_double),
-                ("rope_theta", ctypes.c_double), ("qkv_bias", ctypes.c_int)]
+                ("rope_theta", ctypes.c_double), ("qkv_bias", ctypes.c_int), ("weight_format", ctypes.c_int)]
+
+
+MBK_WEIGHTS_BF16, MBK_WEIGHTS_FP8 = 0, 1
 
 
 LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")
@@ -94,6 +97,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_create_paged.restype = ctypes.c_int
         lib.mbk_set_page_table.argtypes = [vp, vp, i32, vp]
         lib.mbk_set_page_table.restype = ctypes.c_int
+        lib.mbk_quantize_fp8.argtypes = [vp, i32, i32, vp, vp, vp]
+        lib.mbk_quantize_fp8.restype = ctypes.c_int
         lib.mbk_decode_step_host.argtypes = [vp, i32, i32, vp, vp]
         lib.mbk_decode_step_host.restype = ctypes.c_int
         lib.mbk_kv_fill.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, vp]
@@ -132,10 +137,10 @@ def mbk_error_string(code: int) -> str:
     return load_library().mbk_error_string(int(code)).decode()
 
 
-def config_from_shape(shape) -> MbkConfig:
+def config_from_shape(shape, weight_format: int = 0) -> MbkConfig:
     return MbkConfig(shape.n_layers, shape.hidden, shape.intermediate, shape.n_heads, shape.n_kv_heads,
                      shape.head_dim, shape.vocab, shape.kv_capacity, float(shape.rms_eps), float(shape.rope_theta),
-                     int(shape.qkv_bias))
+                     int(shape.qkv_bias), int(weight_format))
 
 
 def mbk_plan_check(cfg: MbkConfig, num_sms: int) -> MbkPlanInfo:
@@ -171,6 +176,11 @@ def mbk_create_paged(cfg: MbkConfig, weights: MbkWeights, kv_pool_ptr: int, num_
                                            int(num_pages), int(page_size), int(device), ctypes.byref(h)),
            "mbk_create_paged")
     return h
+
+
+def mbk_quantize_fp8(w_ptr: int, rows: int, cols: int, q_ptr: int, s_ptr: int, stream_ptr: int) -> int:
+    return load_library().mbk_quantize_fp8(ctypes.c_void_p(w_ptr), int(rows), int(cols), ctypes.c_void_p(q_ptr),
+                                           ctypes.c_void_p(s_ptr), ctypes.c_void_p(stream_ptr))
 
 
 def mbk_set_page_table(h, pages, stream_ptr: int) -> int:
@@ -265,9 +275,10 @@ class Decoder:
     step() launches one decode step into a device logits tensor on the current torch stream.
     """
 
-    def __init__(self, wl, device: int = 0, paged=None):
+    def __init__(self, wl, device: int = 0, paged=None, fp8: bool = False):
         """paged: None for a contiguous cache, or (num_pages, page_size, pages): a pool of num_pages
-        pages and the page table pages[q] for logical page q."""
+        pages and the page table pages[q] for logical page q.  fp8: stream FP8 copies of the weights
+        (MBK_WEIGHTS_FP8)."""
         import torch
         self.torch = torch
         s = wl.shape
@@ -291,7 +302,7 @@ class Decoder:
                 setattr(arr[i], k, None if t is None else t.data_ptr())
         self._layer_arr = arr
         self.weights = MbkWeights(self.embed.data_ptr(), self.final_norm.data_ptr(), arr)
-        self.cfg = config_from_shape(s)
+        self.cfg = config_from_shape(s, MBK_WEIGHTS_FP8 if fp8 else MBK_WEIGHTS_BF16)
         if paged is None:
             self.handle = mbk_create(self.cfg, self.weights, self.kv.data_ptr(), device)
         else:

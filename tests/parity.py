@@ -112,7 +112,7 @@ def _rows_to_gpu(dec, orc_kv: np.ndarray, rows: slice) -> None:
     dec.kv[:, :, :, rows] = src.to(dec.device)
 
 
-def run_parity(wl, device: int = 0, steps: int | None = None, mode: str = "sync") -> ParityReport:
+def run_parity(wl, device: int = 0, steps: int | None = None, mode: str = "sync", fp8: bool = False) -> ParityReport:
     """mode "sync": every GPU step starts from the oracle's state (the oracle's cache rows below the
     step's position are copied into the GPU cache first), so each step's logits and its newly
     written cache row are compared from identical inputs -- teacher forcing of the token AND of
@@ -123,8 +123,8 @@ def run_parity(wl, device: int = 0, steps: int | None = None, mode: str = "sync"
 
     s = wl.shape
     n = s.steps if steps is None else steps
-    dec = Decoder(wl, device=device)
-    orc = OracleDecoder(wl)
+    dec = Decoder(wl, device=device, fp8=fp8)  # fp8: both sides on the FP8 copies of the weights
+    orc = OracleDecoder(wl, fp8=fp8)
     prefill = KvCompare(0, 0, 0.0)
     if s.prefill:
         torch.cuda.synchronize()

@@ -21,7 +21,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "mbk.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mbk_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mbk_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_abi():
