@@ -33,16 +33,21 @@ PAGES_TOKS = {"smollm-135m": 912.0, "qwen2-0.5b": 759.0, "smollm-1.7b": 419.0}  
 METRIC = "batch-1 decode tokens/s and achieved HBM GB/s as fraction of GB300 roofline"
 
 
-def algorithmic_bytes(shape, positions) -> float:
+def algorithmic_bytes(shape, positions, fp8: bool = False) -> float:
     """Bytes a decode step must move, averaged over `positions`: every weight once (tied E as the LM
-    head), the norm gains, the token's embedding row, K/V rows 0..p read once, one K/V row written."""
+    head), the norm gains, the token's embedding row, K/V rows 0..p read once, one K/V row written.
+    fp8: the projections and the LM head as one byte per weight plus a 4-byte scale per row."""
     s = shape
     H, I, d = s.hidden, s.intermediate, s.head_dim
     qd, kvd = s.n_heads * d, s.n_kv_heads * d
-    per_layer = (qd * H + 2 * kvd * H + H * qd + 3 * H * I + 2 * H) * 2
+    wb = 1 if fp8 else 2
+    proj = qd * H + 2 * kvd * H + H * qd + 3 * H * I
+    per_layer = proj * wb + 2 * H * 2
+    if fp8:
+        per_layer += (qd + 2 * kvd + H + 2 * I + H) * 4
     if s.qkv_bias:
         per_layer += (qd + 2 * kvd) * 2
-    fixed = s.n_layers * per_layer + s.vocab * H * 2 + H * 2 + H * 2
+    fixed = s.n_layers * per_layer + s.vocab * H * wb + (s.vocab * 4 if fp8 else 0) + H * 2 + H * 2
     kv_row = s.n_layers * 2 * kvd * 2
     kv = statistics.fmean([(p + 1) * kv_row + kv_row for p in positions])
     return fixed + kv
@@ -188,7 +193,8 @@ def run_ours(args, shape_name):
     build.build()
     wl = workloads.generate(shape_name, seed=0)
     s = wl.shape
-    dec = mbk.Decoder(wl, device=local)
+    fp8 = getattr(args, "weights", "bf16") == "fp8"
+    dec = mbk.Decoder(wl, device=local, fp8=fp8)
     stream = torch.cuda.current_stream()
     # one call decodes `spc` consecutive teacher-forced positions (mbk_decode_steps; 1 = mbk_decode_step)
     spc = args.steps_per_call if args.steps_per_call > 0 else s.steps
@@ -292,7 +298,7 @@ def run_ours(args, shape_name):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, torch.device("cuda", local))
 
     positions = [poss[warm + i] for i in range(steps)]
-    algo = algorithmic_bytes(s, positions)
+    algo = algorithmic_bytes(s, positions, fp8)
     peak, peak_kind = load_peaks()
     achieved = algo / (kernel_avg_ms * 1e-3) / 1e9
     tps = steps * world / (total_ms * 1e-3)
@@ -303,13 +309,13 @@ def run_ours(args, shape_name):
         ctps, cn, cores = time_oracle(wl, budget, s.steps)
         cpu = {"value": round(ctps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{cn} teacher-forced decode steps of the same workload (time-bounded to {budget:.0f} s)"}
-    traffic = profiled_traffic(shape_name)
+    traffic = profiled_traffic(shape_name) if not fp8 else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s", "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": round(tps / PAGES_TOKS[shape_name], 3) if shape_name in PAGES_TOKS else None,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": "fp8-e4m3 weights, f32 math" if fp8 else "bf16", "data": "synthetic",
             "config": {"workload": f"{shape_name} batch-1 teacher-forced decode, random-init weights",
                        "positions": f"{s.pos0}..{s.pos0 + s.steps - 1} cycling", "kv_capacity": s.kv_capacity,
                        "parallelism": "replicas" if world > 1 else "single-gpu",
@@ -317,7 +323,8 @@ def run_ours(args, shape_name):
                        "steps_per_call": spc,
                        "single_step_tokens_per_s": round(single_tps, 2) if single_tps else None,
                        "greedy_tokens_per_s": round(greedy_tps, 2) if greedy_tps else None,
-                       "vs_baseline_note": "pages' H200 MIG 60-SM number, context only"},
+                       "vs_baseline_note": "pages' H200 MIG 60-SM number, context only",
+                       "weights": "fp8 (E4M3, per-row fp32 scales, quantized by the library)" if fp8 else "bf16"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_step": round(algo), "kernel_avg_us_per_step": round(kernel_avg_ms * 1e3, 3),
@@ -368,6 +375,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="smollm-135m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
+                    help="fp8: stream the library's FP8 (E4M3, per-row scale) copies of the weights")
     ap.add_argument("--steps-per-call", type=int, default=0,
                     help="teacher-forced steps per launch (default: the workload's positions; 1 = one launch per step)")
     args = ap.parse_args()
