@@ -93,3 +93,42 @@ def test_create_rejects_null_arguments_before_touching_a_gpu(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         mbk.load_library(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("name", list(workloads.SHAPES))
+def test_fp8_plan_streams_one_byte_per_weight(lib, name):
+    """MBK_WEIGHTS_FP8: the same schedule over E4M3 copies -- every weight byte once, at one byte a weight."""
+    s = workloads.SHAPES[name]
+    bf = mbk.mbk_plan_check(mbk.config_from_shape(s), 152)
+    f8 = mbk.mbk_plan_check(mbk.config_from_shape(s, mbk.MBK_WEIGHTS_FP8), 152)
+    assert f8.weight_bytes * 2 == bf.weight_bytes
+    assert f8.num_tasks == bf.num_tasks
+    assert f8.num_chunks <= bf.num_chunks  # twice the rows fit a stage
+
+
+def test_fp8_needs_rows_of_whole_16_bytes(lib):
+    cfg = mbk.config_from_shape(workloads.SHAPES["tiny"], mbk.MBK_WEIGHTS_FP8)
+    cfg.intermediate = 680  # a multiple of 8 (fine for bf16) but not of 16
+    with pytest.raises(mbk.MbkError) as e:
+        mbk.mbk_plan_check(cfg, 152)
+    assert e.value.code == mbk.MBK_ERR_INVALID_ARG
+    cfg.weight_format = 7  # no such format
+    cfg.intermediate = 688
+    with pytest.raises(mbk.MbkError) as e:
+        mbk.mbk_plan_check(cfg, 152)
+    assert e.value.code == mbk.MBK_ERR_INVALID_ARG
+
+
+def test_new_entry_points_reject_bad_arguments_before_touching_a_gpu(lib):
+    cfg = mbk.config_from_shape(workloads.SHAPES["tiny"])
+    h = ctypes.c_void_p()
+    w = ctypes.c_void_p(16)
+    for pages, size in [(8, 48), (8, 16), (0, 32), (8, 256), (8, 2 * cfg.kv_capacity)]:
+        rc = lib.mbk_create_paged(ctypes.byref(cfg), None, w, pages, size, 0, ctypes.byref(h))
+        assert rc == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_set_page_table(None, None, 1, None) == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_decode_greedy(None, 0, 1, 0, None, None, None) == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_decode_steps(None, None, 1, 0, None, None) == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_quantize_fp8(None, 4, 8, w, w, None) == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_quantize_fp8(w, 4, 7, w, w, None) == mbk.MBK_ERR_INVALID_ARG  # odd row length
+    assert lib.mbk_quantize_fp8(w, 0, 8, w, w, None) == mbk.MBK_ERR_INVALID_ARG
