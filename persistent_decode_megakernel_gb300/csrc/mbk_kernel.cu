@@ -70,16 +70,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
-// L2 prefetch of a global range (no shared-memory destination), kept with the given policy.
-__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ uint64_t evict_last_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -1380,31 +1370,6 @@ __device__ __forceinline__ void produce(const KernelParams& P, const StepParams&
     mbar_expect_tx(&ctl->full[stage], bytes);
     return ring + (size_t)stage * kStageBytes;
   };
-  // A few layers before the LM head, the LM head's rows beyond what the ring will hold when it
-  // starts are prefetched into L2: HBM is mostly idle during the layers, and the LM head then
-  // refills the ring from L2 instead of waiting on HBM at the end of the step.
-  uint32_t lm0 = 0xFFFFFFFFu, lm1 = 0;
-  {
-    const uint32_t t0 = P.task_off[blockIdx.x], t1 = P.task_off[blockIdx.x + 1];
-    if (t1 > t0) {
-      const Task last = P.tasks[t1 - 1];
-      if (last.type == T_LMHEAD) {
-        lm0 = last.chunk0;
-        lm1 = last.chunk0 + last.nchunks;
-      }
-    }
-  }
-  bool lm_prefetched = false;
-  auto prefetch_lm_head = [&]() {
-    lm_prefetched = true;
-    const uint64_t keep = evict_last_policy();
-    unsigned bytes = 0;
-    for (uint32_t k = lm0 + ns; k < lm1 && bytes < kLmPrefetchBytes; ++k) {
-      const Chunk ch = P.chunks[k];
-      prefetch_l2(reinterpret_cast<const void*>(ch.src), ch.bytes, keep);
-      bytes += ch.bytes;
-    }
-  };
   auto advance = [&]() {
     if (++stage == ns) {
       stage = 0;
@@ -1414,7 +1379,6 @@ __device__ __forceinline__ void produce(const KernelParams& P, const StepParams&
   for (int step = 0; step < S.n && !quit; ++step) {
   const int pos = S.pos + step;
   bool synced = step == 0;  // the cache rows of earlier steps are visible to this step's copies
-  lm_prefetched = false;
   Chunk next{};
   if (c0 + lane < c1) next = P.chunks[c0 + lane];
   for (uint32_t base = c0; base < c1 && !quit; base += 32) {
@@ -1428,7 +1392,6 @@ __device__ __forceinline__ void produce(const KernelParams& P, const StepParams&
       const unsigned rows = __shfl_sync(0xffffffffu, mine.rows, j);
       int q = 0;
       if (lane == 0) {
-        if (!lm_prefetched && lm0 != 0xFFFFFFFFu && base + (uint32_t)j + kLmPrefetchLead >= lm0) prefetch_lm_head();
         if (rows == kAttnChunk && !synced) {
           synced = true;
           if (!wait_prev_step(S.sync, S.sync_base + (unsigned long long)step * gridDim.x, step, &P, ctl)) q = 1;

@@ -118,8 +118,6 @@ constexpr int kMaxLayers = 64;
 constexpr int kTaskWindow = 160;      // task records staged in shared memory at a time
 constexpr int kMaxFusedKvHeads = 4;   // the O projection is fused into attention for at most this many KV heads
 constexpr int kMaxFusedGroupWidth = 512;  // ... and query-head groups of at most this many elements (g * head_dim)
-constexpr unsigned kLmPrefetchBytes = 320u << 10;  // LM-head bytes per CTA prefetched into L2 during the layers
-constexpr unsigned kLmPrefetchLead = 24;           // ... issued this many chunks before the producer reaches them
 
 struct PlanShape {
   int L, H, I, nq, nkv, d, V, C;
