@@ -77,3 +77,25 @@ def test_fp8_multi_step_and_greedy_match_single_steps():
     assert tg.cpu().tolist() == [int(np.argmax(r)) for r in lg.cpu().numpy()]
     a.close()
     b.close()
+
+
+def test_fp8_with_a_paged_cache_matches_fp8_contiguous():
+    """The weight format and the cache layout are independent: FP8 on a shuffled page table gives the
+    FP8 contiguous results bit for bit (teacher-forced and greedy launches)."""
+    from persistent_decode_megakernel_gb300.mbk import Decoder
+    wl = workloads.generate("smollm-135m", seed=0)
+    s = wl.shape
+    n_logical = s.kv_capacity // 32
+    table = np.random.default_rng(5).permutation(n_logical + 2)[:n_logical].tolist()
+    a = Decoder(wl, fp8=True)
+    b = Decoder(wl, fp8=True, paged=(n_logical + 2, 32, table))
+    toks = [int(x) for x in wl.tokens[:20]]
+    assert torch.equal(a.steps(toks, 0), b.steps(toks, 0))
+    ta, la = a.greedy(toks[0], 6, 20)
+    tb, lb = b.greedy(toks[0], 6, 20)
+    torch.cuda.synchronize()
+    assert a.status() == 0 and b.status() == 0
+    assert torch.equal(ta, tb) and torch.equal(la, lb)
+    assert torch.equal(a.kv, b.logical_kv())
+    a.close()
+    b.close()
