@@ -2,13 +2,13 @@
 //
 // One cooperative launch per decode step, one CTA per SM (MegaBake article, "What a megakernel is,
 // and why small models want one": resident CTAs working through a task list and synchronising
-// through global memory).  Every CTA runs 16 warps:
+// through global memory).  Every CTA runs 12 warps:
 //   warp 0      streams the weights of its upcoming tasks into a ring of shared-memory stages with
 //               TMA bulk copies (cp.async.bulk + mbarrier transaction counts).  Weights do not depend
 //               on the token, so the stream runs ahead of the data dependencies by up to the ring's
 //               depth -- the "cross-phase prefetch of the next GEMM's weights while a CTA waits" the
 //               article lists as future work ("Checking the 5.5x").
-//   warps 1-15  execute the CTA's tasks in order.  Activations move between CTAs as 64-bit words
+//   warps 1-11  execute the CTA's tasks in order.  Activations move between CTAs as 64-bit words
 //               {tag:32 | fp32 value:32}, each written once per step by exactly one thread; a reader
 //               polls the word until its tag equals this step's tag.  A value and its readiness
 //               travel in one single-copy-atomic store, so no fence, counter or grid barrier is
