@@ -21,19 +21,21 @@
  * and k after the bias, with K cached after rotation; softmax(q.K/sqrt(d)) V with query head h
  * reading KV head h/(n_heads/n_kv_heads); silu(z) = z/(1+exp(-z)); tied LM head (logits = E.xn).
  *
- * Numerics: weights and KV cache bf16; all activations fp32 (accumulation in fp32); K and V are
- * rounded to bf16 (round to nearest even) when appended, and attention reads the rounded values.
+ * Numerics: weights and KV cache bf16 (or, with MBK_WEIGHTS_FP8, the library's E4M3 copies of the
+ * projections with one fp32 scale per row); all activations fp32 (accumulation in fp32); K and V
+ * are rounded to bf16 (round to nearest even) when appended, and attention reads the rounded values.
  *
  * Memory layouts (all row-major, C order):
  *  - weight matrices: bf16 [out][in] (Hugging Face nn.Linear layout), read in place;
  *  - embedding / LM head: bf16 [vocab][hidden];
- *  - KV cache: bf16 [n_layers][2][n_kv_heads][kv_capacity][head_dim] (index 0 = K, 1 = V);
+ *  - KV cache: bf16 [n_layers][2][n_kv_heads][kv_capacity][head_dim] (index 0 = K, 1 = V), or a
+ *    pool of pages [num_pages][n_layers][2][n_kv_heads][page_size][head_dim] (mbk_create_paged);
  *  - logits: fp32 [vocab].
  *
  * Ownership: the caller owns the weights, the KV cache and every logits buffer; they must stay
- * valid (and the weights unchanged) for the handle's lifetime.  The library copies no weights.
- * It owns its task tables, activation exchange buffers, RoPE table and status word, all freed
- * by mbk_destroy.
+ * valid (and the weights unchanged) for the handle's lifetime.  The library copies no weights,
+ * except the FP8 copies it makes for MBK_WEIGHTS_FP8.  It owns those, its task tables, activation
+ * exchange buffers, RoPE table, page table and status word, all freed by mbk_destroy.
  *
  * Threading / streams: a handle is not thread-safe.  Steps on one handle must be issued in order
  * on one stream (or on streams ordered by the caller); two steps of one handle must never run
@@ -42,7 +44,7 @@
  * Errors: every function returning int returns MBK_OK (0) or a negative MBK_ERR_* code.  Host
  * checks run before any launch and leave device state unchanged.  A device-side failure (a wait
  * that ran out of time) is recorded in a device status word; it is returned by the next
- * mbk_decode_step / mbk_kv_fill call on the handle and by mbk_get_status, and is sticky until
+ * decode or mbk_kv_fill call on the handle and by mbk_get_status, and is sticky until
  * mbk_destroy.
  */
 #ifndef MBK_H
@@ -60,7 +62,8 @@ extern "C" {
 #define MBK_ERR_CUDA (-3)         /* a CUDA runtime call failed                              */
 #define MBK_ERR_TIMEOUT (-4)      /* a device-side wait gave up (sticky)                     */
 #define MBK_ERR_NOMEM (-5)        /* device or host allocation failed                        */
-#define MBK_ERR_STATE (-6)        /* the handle is in a sticky error state                   */
+#define MBK_ERR_STATE (-6)        /* not possible in the present state: an armed injection, or no
+                                     schedule for the shape (mbk_plan_check)                    */
 
 typedef struct mbk_handle mbk_handle;
 

@@ -143,7 +143,7 @@ const char* mbk_error_string(int code) {
     case MBK_ERR_CUDA: return "CUDA runtime error";
     case MBK_ERR_TIMEOUT: return "a device-side wait timed out";
     case MBK_ERR_NOMEM: return "out of memory";
-    case MBK_ERR_STATE: return "handle is in an error state";
+    case MBK_ERR_STATE: return "not possible in the present state";
     default: return "unknown error";
   }
 }
