@@ -80,6 +80,20 @@ def test_mha_head_dim_128():
     rep.check()
 
 
+def test_mqa_sixteen_query_heads_per_kv_head():
+    """Multi-query attention at the largest group the plan accepts (16 query heads on one KV head)."""
+    shape = workloads.DecoderShape("mqa16", 2, 1024, 2048, 16, 1, 64, 2048, 96, 1e-5, 1e4, False, steps=12)
+    rep = run_parity(workloads.generate(shape, seed=10))
+    rep.check()
+
+
+def test_gqa_head_dim_128_with_the_o_projection_fused():
+    """Head dim 128 with 4 query heads per KV head: the O projection is folded into attention."""
+    shape = workloads.DecoderShape("gqa128", 2, 1024, 2048, 8, 2, 128, 2048, 96, 1e-5, 1e4, False, steps=12)
+    rep = run_parity(workloads.generate(shape, seed=11))
+    rep.check()
+
+
 @pytest.mark.parametrize("fuse", ["0", "1"])
 def test_o_projection_fused_and_separate(fuse, monkeypatch):
     """The O projection runs either inside the attention tasks (per-KV-head partial sums) or as tasks
