@@ -141,10 +141,11 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def time_oracle(wl, budget_s: float, max_steps: int):
-    """Oracle decode steps of `wl` for about budget_s seconds; returns (tokens/s, steps, threads)."""
+def time_oracle(wl, budget_s: float, max_steps: int, fp8: bool = False):
+    """Oracle decode steps of `wl` for about budget_s seconds; returns (tokens/s, steps, threads).
+    fp8: the oracle on the FP8 copies of the weights (quantized before the timed steps)."""
     from oracle import OracleDecoder
-    orc = OracleDecoder(wl)
+    orc = OracleDecoder(wl, fp8=fp8)
     s = wl.shape
     n, t0 = 0, time.perf_counter()
     while n < max_steps:
@@ -166,10 +167,11 @@ def run_reference(args, shape_name):
     budget = float(os.environ.get("MBK_REF_BUDGET_S", "60"))
     # warm-up steps (untimed), then the timed sample
     from oracle import OracleDecoder
-    warm = OracleDecoder(wl)
+    fp8 = args.weights == "fp8"
+    warm = OracleDecoder(wl, fp8=fp8)
     for i in range(min(args.warmup, 3)):
         warm.step(int(wl.tokens[i]), s.pos0 + i)
-    tps, n, cores = time_oracle(wl, budget, args.steps)
+    tps, n, cores = time_oracle(wl, budget, args.steps, fp8)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(tps, 3), "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / tps, 3), "higher_is_better": True,
@@ -306,7 +308,7 @@ def run_ours(args, shape_name):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         budget = float(os.environ.get("MBK_CPU_BUDGET_S", "15"))
-        ctps, cn, cores = time_oracle(wl, budget, s.steps)
+        ctps, cn, cores = time_oracle(wl, budget, s.steps, fp8)
         cpu = {"value": round(ctps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{cn} teacher-forced decode steps of the same workload (time-bounded to {budget:.0f} s)"}
     traffic = profiled_traffic(shape_name) if not fp8 else None
