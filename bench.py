@@ -244,6 +244,9 @@ def run_ours(args, shape_name):
     total_ms = max_over_ranks(start.elapsed_time(end), world, torch.device("cuda", local))
     kern_ms = [a.elapsed_time(b) / spc for a, b in ev]  # per decode step
     kernel_avg_ms = statistics.fmean(kern_ms)
+    ks = sorted(kern_ms)
+    spread = {"median_us": round(1e3 * ks[len(ks) // 2], 3), "p10_us": round(1e3 * ks[len(ks) // 10], 3),
+              "p90_us": round(1e3 * ks[min(len(ks) - 1, (9 * len(ks)) // 10)], 3), "launches": len(ks)}
 
     # the same workload one step per launch (mbk_decode_step), for reference
     single_tps = None
@@ -325,6 +328,7 @@ def run_ours(args, shape_name):
                        "steps_per_call": spc,
                        "single_step_tokens_per_s": round(single_tps, 2) if single_tps else None,
                        "greedy_tokens_per_s": round(greedy_tps, 2) if greedy_tps else None,
+                       "per_step_time_over_launches": spread,
                        "vs_baseline_note": "pages' H200 MIG 60-SM number, context only",
                        "weights": "fp8 (E4M3, per-row fp32 scales, quantized by the library)" if fp8 else "bf16"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
