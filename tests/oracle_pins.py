@@ -209,11 +209,12 @@ def pin_silu_mul(lib):
 
 
 # ---------------------------------------------------------------- whole decoder
-def torch_restatement(wl, n_steps, kv_init=None):
+def torch_restatement(wl, n_steps, kv_init=None, proj=None, lm=None):
     """An independent float64 restatement built from torch library routines (rms_norm, linear,
     scaled_dot_product_attention, silu).  Each op's result is rounded to fp32, K and V to bf16,
     which is the precision the oracle states.  kv_init: optional uint16 numpy cache to start
-    from.  Returns (logits list, kv cache bf16 tensor)."""
+    from.  proj / lm: optional float64 replacements of the projection weights (proj[l][key]) and of
+    the LM head matrix (FP8: the dequantized codes).  Returns (logits list, kv cache bf16 tensor)."""
     s = wl.shape
     L, H, nq, nkv, d, cap = s.n_layers, s.hidden, s.n_heads, s.n_kv_heads, s.head_dim, s.kv_capacity
     r32 = lambda t: t.float().double()  # noqa: E731
@@ -237,7 +238,8 @@ def torch_restatement(wl, n_steps, kv_init=None):
         x = E[tok].clone()
         for l in range(L):
             w = wl.layers[l]
-            lin = lambda a, key, bkey=None: r32(F.linear(a, w[key].double(),  # noqa: E731
+            wk_ = (lambda key: proj[l][key]) if proj is not None else (lambda key: w[key].double())  # noqa: E731
+            lin = lambda a, key, bkey=None: r32(F.linear(a, wk_(key),  # noqa: E731
                                                       None if (bkey is None or w[bkey] is None or not s.qkv_bias) else w[bkey].double()))
             xn = r32(F.rms_norm(x, (H,), weight=w["attn_norm"].double(), eps=s.rms_eps))
             q = lin(xn, "wq", "bq").view(nq, d)
@@ -256,7 +258,7 @@ def torch_restatement(wl, n_steps, kv_init=None):
             hh = r32(F.silu(lin(xn, "w_gate")) * lin(xn, "w_up"))
             x = r32(x + lin(hh, "w_down"))
         xn = r32(F.rms_norm(x, (H,), weight=wl.final_norm.double(), eps=s.rms_eps))
-        out.append(r32(F.linear(xn, E)).float().numpy())
+        out.append(r32(F.linear(xn, E if lm is None else lm)).float().numpy())
     return out, kv
 
 
