@@ -276,3 +276,78 @@ def pin_decoder_vs_torch(lib_unused, wl, n_steps, decoder_cls):
     b = ref_kv.view(torch.int16).numpy().astype(np.int32) & 0xFFFF
     diff = a != b
     assert diff.sum() <= max(2, a.size // 100000), f"{diff.sum()} cache entries differ"
+
+
+# ---------------------------------------------------------------- FP8 weight format
+# E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities, S.1111.111 = NaN,
+# largest finite 448; nearest code with ties to even, saturating.  Values worked out by hand.
+FP8_EXACT = [(0.0, 0x00), (1.0, 0x38), (-1.0, 0xB8), (448.0, 0x7E), (-448.0, 0xFE), (2.0 ** -6, 0x08),
+             (2.0 ** -9, 0x01), (7 * 2.0 ** -9, 0x07), (3.0, 0x44), (240.0, 0x77), (256.0, 0x78), (0.3125, 0x2A)]
+FP8_ROUNDED = [(1.0625, 0x38), (1.1875, 0x3A), (1.06, 0x38), (1.07, 0x39), (-0.3, 0xAA), (2.0 ** -10, 0x00),
+               (1.5 * 2.0 ** -9, 0x02), (464.0, 0x7E), (1.0e6, 0x7E), (-1.0e6, 0xFE)]
+
+
+def e4m3_values() -> np.ndarray:
+    """Value of each of the 256 codes, from the bit fields (independent of the oracle's decoder)."""
+    c = np.arange(256)
+    e, m = (c >> 3) & 15, c & 7
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
+    v = np.where(c & 0x80, -v, v)
+    v[(e == 15) & (m == 7)] = np.nan
+    return v
+
+
+def pin_fp8_codes(lib):
+    for value, code in FP8_EXACT + FP8_ROUNDED:
+        assert lib.orc_fp8_from_f32(value) == code, (value, code)
+    vals = e4m3_values()
+    for c in range(256):
+        if not np.isnan(vals[c]):
+            assert lib.orc_fp8_to_f32(c) == vals[c], c
+            assert lib.orc_fp8_from_f32(float(vals[c])) == c, c
+
+
+def pin_fp8_quantize_and_gemv(lib, wl):
+    """The oracle's codes and scales of real matrices against an exhaustive-search restatement, and
+    its FP8 projection against the scaled float64 sum."""
+    from oracle.oracle import bf16_bits, quantize_fp8
+    vals = e4m3_values()
+    pos = vals[:0x7F]
+    for m in (wl.layers[0]["wq"], wl.embed[:64]):
+        bits = bf16_bits(m)
+        w = (bits.astype(np.uint32) << 16).view(np.float32)
+        amax = np.abs(w).max(axis=1)
+        s = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0)).astype(np.float32)
+        x = (w / s[:, None]).astype(np.float32).astype(np.float64)
+        d = np.abs(np.minimum(np.abs(x), 448.0)[..., None] - pos)
+        best = d.min(axis=-1, keepdims=True)
+        ties = d == best
+        first = ties.argmax(axis=-1)
+        nxt = np.take_along_axis(ties, np.minimum(first + 1, 0x7E)[..., None], axis=-1)[..., 0] & (first < 0x7E)
+        want = np.where(nxt & (first % 2 == 1), first + 1, first).astype(np.uint8) | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+        q, sc = quantize_fp8(bits, lib)
+        assert np.array_equal(sc.view(np.uint32), s.view(np.uint32))
+        assert np.array_equal(q, want)
+        xin = np.random.default_rng(3).standard_normal(q.shape[1]).astype(F32)
+        y = np.empty(q.shape[0], dtype=F32)
+        lib.orc_gemv_fp8(_p(q), _p(sc), _p(xin), None, q.shape[0], q.shape[1], _p(y), 1)
+        ref = (vals[q] @ xin.astype(np.float64)) * sc.astype(np.float64)
+        assert np.allclose(y, ref.astype(F32), rtol=1e-6, atol=1e-12)
+
+
+def pin_fp8_decoder_vs_torch(lib, wl, n_steps, decoder_cls):
+    """The FP8 decode step equals the torch restatement run on the dequantized weights."""
+    from oracle.oracle import FP8_SLOTS, bf16_bits, quantize_fp8
+    vals = e4m3_values()
+
+    def deq(t):
+        q, s = quantize_fp8(bf16_bits(t), lib)
+        return torch.from_numpy(vals[q] * s.astype(np.float64)[:, None])
+
+    proj = [{k: deq(w[k]) for k in FP8_SLOTS} for w in wl.layers]
+    ref, _ = torch_restatement(wl, n_steps, proj=proj, lm=deq(wl.embed))
+    dec = decoder_cls(wl)
+    for i in range(n_steps):
+        got = dec.step(int(wl.tokens[i]), wl.shape.pos0 + i).astype(np.float64)
+        rel = float(np.linalg.norm(got - ref[i]) / np.linalg.norm(ref[i]))
+        assert rel < 1e-5, f"step {i}: rel L2 {rel}"

@@ -119,69 +119,15 @@ def test_fp8_decoder_stays_near_the_bf16_decoder():
         assert 1e-4 < rel < 0.1, rel
 
 
-# ---- the FP8 decode step against the torch restatement on dequantized weights ----
-def _e4m3_values() -> np.ndarray:
-    """Value of each of the 256 codes, from the bit fields (independent of the oracle's decoder)."""
-    c = np.arange(256)
-    e, m, sgn = (c >> 3) & 15, c & 7, np.where(c & 0x80, -1.0, 1.0)
-    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
-    v = sgn * v
-    v[(e == 15) & (m == 7)] = np.nan
-    return v
-
-
-def _quantize_numpy(w_bits: np.ndarray):
-    """Per-row scale amax/448 (fp32) and nearest codes with ties to even, saturating: a numpy
-    restatement by exhaustive search over the 127 non-negative finite codes."""
-    w = (w_bits.astype(np.uint32) << 16).view(np.float32)
-    amax = np.abs(w).max(axis=1)
-    s = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0)).astype(np.float32)
-    x = (w / s[:, None]).astype(np.float32).astype(np.float64)
-    mag = np.minimum(np.abs(x), 448.0)
-    pos = _e4m3_values()[:0x7F]
-    q = np.empty(x.shape, dtype=np.uint8)
-    flat, out = mag.reshape(-1), q.reshape(-1)
-    for a in range(0, flat.size, 1 << 16):
-        d = np.abs(flat[a:a + (1 << 16), None] - pos[None, :])
-        best = d.min(axis=1, keepdims=True)
-        ties = d == best
-        # the lowest index among the nearest, moved to the even one of a tied pair
-        first = ties.argmax(axis=1)
-        second_tied = ties[np.arange(ties.shape[0]), np.minimum(first + 1, 0x7E)] & (first < 0x7E)
-        out[a:a + (1 << 16)] = np.where(second_tied & (first % 2 == 1), first + 1, first)
-    q |= np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
-    return q, s
-
-
-def test_oracle_quantization_matches_a_numpy_restatement():
-    from oracle.oracle import bf16_bits
+# ---- the oracle's quantization and FP8 decode step against independent restatements ----
+def test_oracle_quantization_and_gemv_match_numpy_restatements(lib):
     from persistent_decode_megakernel_gb300 import workloads
-    wl = workloads.generate("tiny", seed=0)
-    for m in (wl.layers[0]["wq"], wl.layers[1]["w_down"], wl.embed[:300]):
-        bits = bf16_bits(m)
-        qa, sa = quantize_fp8(bits)
-        qb, sb = _quantize_numpy(bits)
-        assert np.array_equal(sa.view(np.uint32), sb.view(np.uint32))
-        assert np.array_equal(qa, qb)
+    import oracle_pins as pins
+    pins.pin_fp8_quantize_and_gemv(lib, workloads.generate("tiny", seed=0))
 
 
-def test_fp8_decoder_matches_torch_restatement_on_dequantized_weights():
-    import torch
+def test_fp8_decoder_matches_torch_restatement_on_dequantized_weights(lib):
     from oracle import OracleDecoder
-    from oracle.oracle import FP8_SLOTS, bf16_bits
-    from oracle_pins import torch_restatement
     from persistent_decode_megakernel_gb300 import workloads
-    wl = workloads.generate("tiny", seed=0)
-    vals = _e4m3_values()
-
-    def deq(t):
-        q, s = quantize_fp8(bf16_bits(t))
-        return torch.from_numpy(vals[q] * s.astype(np.float64)[:, None])
-
-    proj = [{k: deq(w[k]) for k in FP8_SLOTS} for w in wl.layers]
-    ref, _ = torch_restatement(wl, 8, proj=proj, lm=deq(wl.embed))
-    dec = OracleDecoder(wl, fp8=True)
-    for i in range(8):
-        got = dec.step(int(wl.tokens[i]), i).astype(np.float64)
-        rel = float(np.linalg.norm(got - ref[i]) / np.linalg.norm(ref[i]))
-        assert rel < 1e-5, f"step {i}: rel L2 {rel}"
+    import oracle_pins as pins
+    pins.pin_fp8_decoder_vs_torch(lib, workloads.generate("tiny", seed=0), 8, lambda wl: OracleDecoder(wl, fp8=True))

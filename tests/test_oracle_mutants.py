@@ -104,3 +104,49 @@ def test_unmutated_copy_passes_every_pin(tmp_path, decoders):
 def test_mutant_is_caught(tmp_path, decoders, name, find, repl, occ):
     lib = _build(tmp_path, name, _mutate(open(SRC).read(), find, repl, occ))
     assert _all_pins(lib, decoders), f"mutant {name} passed every pin"
+
+
+# Planted mistakes in the FP8 weight format; the FP8 pins must reject each one.
+FP8_MUTANTS = [
+    ("fp8_truncates", "if (a - vlo < vhi - a) c = lo;", "if (1) c = lo;", None),
+    ("fp8_ties_down", "else c = (lo % 2 == 0) ? lo : lo + 1;", "else c = lo;", None),
+    ("fp8_scale_not_applied", "acc *= (double)s[r];", "acc *= 1.0;", None),
+    ("fp8_scale_range", "const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;",
+     "const float sc = amax > 0.0f ? amax / 240.0f : 1.0f;", None),
+    ("fp8_k_uses_v_codes", "project(w->wk, f8, 1,", "project(w->wk, f8, 2,", None),
+    ("fp8_lm_head_bf16", "  if (fp8)\n    orc_gemv_fp8(fp8->lm_q", "  if (0)\n    orc_gemv_fp8(fp8->lm_q", None),
+    ("fp8_subnormal_scale", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);", None),
+    ("fp8_bias_scaled", "    acc *= (double)s[r];\n    if (b != NULL) acc += (double)orc_bf16_to_f32(b[r]);",
+     "    if (b != NULL) acc += (double)orc_bf16_to_f32(b[r]);\n    acc *= (double)s[r];", None),
+]
+
+
+def _fp8_pins(lib):
+    tiny = workloads.generate("tiny", seed=0)
+    bias = workloads.generate(workloads.scaled_down(workloads.SHAPES["qwen2-0.5b"], n_layers=2, hidden=128,
+                                                    intermediate=320, n_heads=6, n_kv_heads=2, vocab=512,
+                                                    kv_capacity=32, steps=4), seed=3)
+    checks = [
+        lambda: pins.pin_fp8_codes(lib),
+        lambda: pins.pin_fp8_quantize_and_gemv(lib, tiny),
+        lambda: pins.pin_fp8_decoder_vs_torch(lib, tiny, 3, lambda wl: OracleDecoder(wl, lib=lib, fp8=True)),
+        lambda: pins.pin_fp8_decoder_vs_torch(lib, bias, 2, lambda wl: OracleDecoder(wl, lib=lib, fp8=True)),
+    ]
+    failed = []
+    for i, chk in enumerate(checks):
+        try:
+            chk()
+        except AssertionError:
+            failed.append(i)
+    return failed
+
+
+def test_unmutated_copy_passes_every_fp8_pin(tmp_path):
+    lib = _build(tmp_path, "clean8", open(SRC).read())
+    assert _fp8_pins(lib) == []
+
+
+@pytest.mark.parametrize("name,find,repl,occ", FP8_MUTANTS, ids=[m[0] for m in FP8_MUTANTS])
+def test_fp8_mutant_is_caught(tmp_path, name, find, repl, occ):
+    lib = _build(tmp_path, name, _mutate(open(SRC).read(), find, repl, occ))
+    assert _fp8_pins(lib), f"mutant {name} passed every FP8 pin"
