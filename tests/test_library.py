@@ -132,3 +132,18 @@ def test_new_entry_points_reject_bad_arguments_before_touching_a_gpu(lib):
     assert lib.mbk_quantize_fp8(None, 4, 8, w, w, None) == mbk.MBK_ERR_INVALID_ARG
     assert lib.mbk_quantize_fp8(w, 4, 7, w, w, None) == mbk.MBK_ERR_INVALID_ARG  # odd row length
     assert lib.mbk_quantize_fp8(w, 0, 8, w, w, None) == mbk.MBK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", list(workloads.SHAPES))
+@pytest.mark.parametrize("env", [{"MBK_FUSE_ATTENTION": "0"}, {"MBK_MAX_TASKS_PER_OP": "38"},
+                                 {"MBK_MAX_TASKS_PER_OP": "1"}])
+def test_schedule_variants_build_and_check(lib, monkeypatch, name, env):
+    """The schedule options (O projection as tasks of its own; fewer CTAs per op, down to one) still
+    give plans that pass the scheduler's own checks and stream every weight byte once."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    s = workloads.SHAPES[name]
+    info = mbk.mbk_plan_check(mbk.config_from_shape(s), 152)
+    base = (s.n_heads * s.head_dim * s.hidden + 2 * s.n_kv_heads * s.head_dim * s.hidden
+            + s.hidden * s.n_heads * s.head_dim + 3 * s.hidden * s.intermediate) * 2
+    assert info.weight_bytes == s.n_layers * base + s.vocab * s.hidden * 2
