@@ -173,6 +173,38 @@ int mbk_decode_steps(mbk_handle *h, const int32_t *tokens, int32_t n_steps, int3
 int mbk_decode_greedy(mbk_handle *h, int32_t first_token, int32_t n_steps, int32_t position, int32_t *tokens_out,
                       float *logits_out, void *stream);
 
+/* Prefill: n_tokens given tokens (a prompt) at positions position .. position + n_tokens - 1,
+ * computed as dense contractions over all of them on the tensor cores instead of one decode step
+ * per token.  The MegaBake article ("Where it loses") names prefill as the megakernel's weakest
+ * path; its plain definition is n_tokens teacher-forced decode steps, and that is what this computes
+ * (each token attends to the cache rows up to its own position), layer by layer: RMSNorm, the
+ * Q/K/V projection (+ bias), RoPE, the KV append, causal attention, the O projection and residual,
+ * RMSNorm, gate/up, SiLU * up, the down projection and residual; then the final norm and the tied
+ * LM head.  The cache rows of every layer at those positions are written, exactly as the decode
+ * steps would write them (bf16, nearest even).
+ *   tokens: HOST array of n_tokens ids, copied before the call returns.
+ *   logits_mode: MBK_PREFILL_LOGITS_NONE (cache only; logits_out unused and may be NULL),
+ *     MBK_PREFILL_LOGITS_LAST (the last token's logits: DEVICE fp32[vocab]) or
+ *     MBK_PREFILL_LOGITS_ALL (every token's: DEVICE fp32[n_tokens][vocab]).
+ * Numerics: projections multiply the bf16 weights by fp32 activations carried as a bf16 pair
+ * (hi = bf16(x), lo = bf16(x - hi); fp32 accumulation), so results match the fp32-activation decode
+ * within its tolerances.  Memory: the handle keeps a device workspace of about
+ * n_tokens * (4 * (2 * hidden + (n_heads + 2 * n_kv_heads) * head_dim + 2 * intermediate) +
+ * 4 * max(hidden, intermediate, n_heads * head_dim)) bytes; a call with more tokens than any
+ * before it reallocates it (a synchronising cudaFree/cudaMalloc).  Asynchronous on `stream`
+ * otherwise.  Not a counterpart of a MegaBake entry point (the pages have none for prefill).
+ * Errors: MBK_ERR_INVALID_ARG if n_tokens < 1, a token is not in [0, vocab), the positions are not
+ * inside [0, kv_capacity) (for a paged cache: mapped), logits_mode is unknown, or logits_out is NULL
+ * while logits are asked for; MBK_ERR_UNSUPPORTED for an FP8 handle (prefill reads the bf16
+ * weights) or when the driver has no tensor-map encoder; MBK_ERR_NOMEM if the workspace cannot be
+ * allocated; MBK_ERR_STATE if a diagnostic injection is armed; a sticky device error.  A device
+ * wait that runs out of time is reported like a decode step's (mbk_get_status). */
+#define MBK_PREFILL_LOGITS_NONE 0
+#define MBK_PREFILL_LOGITS_LAST 1
+#define MBK_PREFILL_LOGITS_ALL 2
+int mbk_prefill(mbk_handle *h, const int32_t *tokens, int32_t n_tokens, int32_t position, float *logits_out,
+                int32_t logits_mode, void *stream);
+
 /* As mbk_decode_step, then copies the logits into the HOST buffer logits_host (vocab floats;
  * pinned memory makes the copy asynchronous) and synchronises `stream` before returning. */
 int mbk_decode_step_host(mbk_handle *h, int32_t token_id, int32_t position, float *logits_host, void *stream);

@@ -20,9 +20,9 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmbk.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
-CU_SOURCES = ["mbk_kernel.cu", "mbk_api.cu", "mbk_static.cu"]
+CU_SOURCES = ["mbk_kernel.cu", "mbk_api.cu", "mbk_static.cu", "mbk_prefill.cu"]
 CPP_SOURCES = ["mbk_sched.cpp"]
-HEADERS = ["mbk_plan.h", "mbk_device.h", "mbk_sched.h"]
+HEADERS = ["mbk_plan.h", "mbk_device.h", "mbk_sched.h", "mbk_prefill.h"]
 
 
 def _cuda_home() -> str:

@@ -12,6 +12,7 @@
 
 #include "../../include/mbk.h"
 #include "mbk_device.h"
+#include "mbk_prefill.h"
 #include "mbk_sched.h"
 
 namespace mbk {
@@ -56,6 +57,10 @@ struct mbk_handle {
   uint8_t* d_fp8 = nullptr;
   float* d_wscale = nullptr;
   int mapped = 0;  // positions [0, mapped) have cache rows: kv_capacity, or what the page table covers
+  // prefill (mbk_prefill): the caller's bf16 weights (an FP8 handle decodes from its copies) and the
+  // workspace and tensor maps of the tensor-core path
+  std::vector<LayerW> bf16_layers;
+  PrefillState prefill;
   unsigned long long* d_trace = nullptr;
   unsigned long long* d_inject = nullptr;
   bool inject_armed = false;
@@ -120,6 +125,7 @@ void free_all(mbk_handle* h) {
   cudaFree(h->d_page_table);
   cudaFree(h->d_fp8);
   cudaFree(h->d_wscale);
+  prefill_free(h->prefill);
   cudaFree(h->d_trace);
   cudaFree(h->d_inject);
   if (h->h_status) cudaFreeHost(h->h_status);
@@ -263,6 +269,9 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   if (!h) return MBK_ERR_NOMEM;
   h->device = device;
   h->cfg = *cfg;
+  h->bf16_layers.resize(s.L);
+  for (int l = 0; l < s.L; ++l)
+    for (int k = 0; k < W_NSLOTS; ++k) h->bf16_layers[l].w[k] = reinterpret_cast<const uint16_t*>(wa.layers[l][k]);
   h->paged = kvl.num_pages > 0;
   h->num_pages = kvl.num_pages;
   h->page_size = kvl.page_size;
@@ -528,6 +537,48 @@ int mbk_decode_greedy(mbk_handle* h, int32_t first_token, int32_t n_steps, int32
   if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
   h->last_token = first_token;
   return launch_steps(h, first_token, nullptr, n_steps, position, logits_out, stream, tokens_out);
+}
+
+int mbk_prefill(mbk_handle* h, const int32_t* tokens, int32_t n_tokens, int32_t position, float* logits_out,
+                int32_t logits_mode, void* stream) {
+  if (!h || !tokens || n_tokens < 1) return MBK_ERR_INVALID_ARG;
+  if (logits_mode != MBK_PREFILL_LOGITS_NONE && logits_mode != MBK_PREFILL_LOGITS_LAST &&
+      logits_mode != MBK_PREFILL_LOGITS_ALL)
+    return MBK_ERR_INVALID_ARG;
+  if (logits_mode != MBK_PREFILL_LOGITS_NONE && !logits_out) return MBK_ERR_INVALID_ARG;
+  if (position < 0 || n_tokens > h->mapped || position > h->mapped - n_tokens) return MBK_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
+  if (h->cfg.weight_format != MBK_WEIGHTS_BF16) return MBK_ERR_UNSUPPORTED;
+  if (h->inject_armed) return MBK_ERR_STATE;
+  if (int st = sticky_status(h)) return st;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  const KernelParams& kp = h->kp;
+  PrefillModel m;
+  m.L = kp.L;
+  m.H = kp.H;
+  m.I = kp.I;
+  m.nq = kp.nq;
+  m.nkv = kp.nkv;
+  m.d = kp.d;
+  m.V = kp.V;
+  m.eps = kp.eps;
+  m.inv_H = kp.inv_H;
+  m.attn_scale = kp.attn_scale;
+  m.qkv_bias = kp.qkv_bias;
+  m.embed = kp.embed;
+  m.final_norm = kp.final_norm;
+  m.layers = h->bf16_layers;
+  m.rope = kp.rope;
+  m.kv = kp.kv;
+  m.page_table = kp.page_table;
+  m.page_size = kp.page_size;
+  m.page_shift = kp.page_shift;
+  m.page_elems = kp.page_elems;
+  m.status = kp.status;
+  m.host_status = kp.host_status;
+  m.timeout_ns = kp.timeout_ns;
+  return prefill_run(m, h->prefill, tokens, n_tokens, position, logits_out, logits_mode, (cudaStream_t)stream);
 }
 
 int mbk_decode_step_host(mbk_handle* h, int32_t token_id, int32_t position, float* logits_host, void* stream) {

@@ -1,0 +1,67 @@
+// mbk_prefill.h -- host interface of the prefill path (mbk_prefill.cu), used by the C ABI (mbk_api.cu).
+//
+// Prefill runs n tokens whose ids are known in advance (a prompt) through the decoder at positions
+// p0 .. p0 + n - 1 and appends their K/V rows to the cache.  Its plain definition is n teacher-forced
+// decode steps; with all n tokens at hand the projections become dense [n, K] x [K, N] contractions,
+// which run on the tensor cores (tcgen05) instead of the decode kernel's GEMVs.
+#pragma once
+#include <cuda.h>  // CUtensorMap and its enums (types only: the encoder is looked up at run time)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "mbk_device.h"
+
+namespace mbk {
+
+// The decoder as the prefill reads it.  All pointers are device pointers; weights are bf16 bit
+// patterns in the Hugging Face [out, in] layout, 16-byte aligned.
+struct PrefillModel {
+  int L, H, I, nq, nkv, d, V;
+  float eps, inv_H;             // RMSNorm epsilon; 1 / hidden rounded to fp32
+  float attn_scale;             // 1 / sqrt(head_dim)
+  int qkv_bias;
+  const uint16_t* embed;        // [V][H]: embedding rows and the tied LM head
+  const uint16_t* final_norm;   // [H]
+  std::vector<LayerW> layers;   // per layer, in LayerSlot order
+  const float2* rope;           // [C][d/2] (cos, sin) of position p and frequency i
+  // the KV cache: contiguous [L][2][nkv][C][d] (page_table null, page_size = C) or a pool of pages
+  // [num_pages][L][2][nkv][page_size][d] found through page_table (page_size = 1 << page_shift)
+  uint16_t* kv;
+  const int32_t* page_table;
+  int page_size, page_shift;
+  unsigned long long page_elems;
+  unsigned* status;             // device status word [4] shared with the decode kernel
+  unsigned* host_status;        // its mapped host copy (may be null)
+  unsigned long long timeout_ns;
+};
+
+// Workspace and tensor maps, owned by a handle.  The workspace grows on demand (a call with more
+// tokens than it holds reallocates it); the weight maps are encoded on the first call.
+struct PrefillState {
+  int cap = 0;                  // tokens the workspace holds
+  void* ws = nullptr;           // one device allocation holding the buffers below
+  float* x = nullptr;           // [cap][H]       residual stream
+  float* qkv = nullptr;         // [cap][qd+2kvd] projections (q and k rotated in place)
+  float* gu = nullptr;          // [cap][2I]      gate | up
+  uint16_t* a_hi = nullptr;     // [cap][max(H, qd, I)] GEMM input, bf16 high part
+  uint16_t* a_lo = nullptr;     // ... and the bf16 remainder
+  int32_t* tokens = nullptr;    // [cap]
+  std::vector<CUtensorMap> wmaps;  // per layer Wq, Wk, Wv, Wo, Wgate, Wup, Wdown; then E
+  bool smem_set = false;
+};
+
+// Logits the caller asks for (values of the C ABI's MBK_PREFILL_LOGITS_*).
+enum PrefillLogits { PL_NONE = 0, PL_LAST = 1, PL_ALL = 2 };
+
+// Runs the prefill on `stream` (asynchronous after the token copy).  tokens_host: n ids, already
+// validated by the caller; positions p0 .. p0 + n - 1 lie inside the cache.  logits: device fp32,
+// [n][V] (PL_ALL), [V] (PL_LAST) or unused (PL_NONE).  Returns an MBK_* code.
+int prefill_run(const PrefillModel& m, PrefillState& st, const int32_t* tokens_host, int n, int p0, float* logits,
+                int mode, cudaStream_t stream);
+
+// Frees the workspace (the tensor maps are host memory).
+void prefill_free(PrefillState& st);
+
+}  // namespace mbk

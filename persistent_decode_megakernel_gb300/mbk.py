@@ -28,7 +28,7 @@ MBK_ERR_STATE = -6
 EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
             "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps",
-            "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8")
+            "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8", "mbk_prefill")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -92,6 +92,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_decode_steps.restype = ctypes.c_int
         lib.mbk_decode_greedy.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         lib.mbk_decode_greedy.restype = ctypes.c_int
+        lib.mbk_prefill.argtypes = [vp, vp, i32, i32, vp, i32, vp]
+        lib.mbk_prefill.restype = ctypes.c_int
         lib.mbk_create_paged.argtypes = [ctypes.POINTER(MbkConfig), ctypes.POINTER(MbkWeights), vp, i32, i32, ctypes.c_int,
                                          ctypes.POINTER(vp)]
         lib.mbk_create_paged.restype = ctypes.c_int
@@ -167,6 +169,18 @@ def mbk_decode_steps(h, tokens, position: int, logits_ptr: int, stream_ptr: int)
     arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     return load_library().mbk_decode_steps(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), int(position),
                                            ctypes.c_void_p(logits_ptr), ctypes.c_void_p(stream_ptr))
+
+
+PREFILL_LOGITS = {None: 0, "last": 1, "all": 2}  # MBK_PREFILL_LOGITS_NONE / _LAST / _ALL
+
+
+def mbk_prefill(h, tokens, position: int, logits_ptr: int, logits_mode: int, stream_ptr: int) -> int:
+    """tokens: a sequence of token ids (copied into a host int32 array here); logits_ptr: device fp32
+    [vocab] (mode 1), [n][vocab] (mode 2), or 0 (mode 0)."""
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    return load_library().mbk_prefill(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), int(position),
+                                      ctypes.c_void_p(logits_ptr or None), int(logits_mode), ctypes.c_void_p(stream_ptr))
 
 
 def mbk_create_paged(cfg: MbkConfig, weights: MbkWeights, kv_pool_ptr: int, num_pages: int, page_size: int,
@@ -370,6 +384,19 @@ class Decoder:
         _check(mbk_decode_greedy(self.handle, first_token, n, pos0, toks.data_ptr(), out.data_ptr() if out is not None else 0,
                                  stream), "mbk_decode_greedy")
         return toks, out
+
+    def prefill(self, tokens, pos0: int, logits: str = "last", out=None):
+        """Prefill len(tokens) positions from pos0 on the tensor cores (mbk_prefill); writes their cache
+        rows.  logits: "last" -> [vocab], "all" -> [n, vocab], None -> no logits (returns None)."""
+        n = len(tokens)
+        mode = PREFILL_LOGITS[logits]
+        if out is None and mode:
+            shape = (self.shape.vocab,) if mode == 1 else (n, self.shape.vocab)
+            out = self.torch.empty(shape, dtype=self.torch.float32, device=self.device)
+        stream = self.torch.cuda.current_stream(self.device).cuda_stream
+        _check(mbk_prefill(self.handle, tokens, pos0, out.data_ptr() if out is not None else 0, mode, stream),
+               "mbk_prefill")
+        return out
 
     def status(self) -> int:
         return mbk_get_status(self.handle)
