@@ -197,7 +197,8 @@ int mbk_decode_greedy(mbk_handle *h, int32_t first_token, int32_t n_steps, int32
  * inside [0, kv_capacity) (for a paged cache: mapped), logits_mode is unknown, or logits_out is NULL
  * while logits are asked for; MBK_ERR_UNSUPPORTED for an FP8 handle (prefill reads the bf16
  * weights) or when the driver has no tensor-map encoder; MBK_ERR_NOMEM if the workspace cannot be
- * allocated; MBK_ERR_STATE if a diagnostic injection is armed; a sticky device error.  A device
+ * allocated; MBK_ERR_STATE if a decode step's diagnostic injection is armed, MBK_ERR_INVALID_ARG if a
+ * prefill injection (mbk_debug_prefill_inject) is armed for another n_tokens; a sticky device error.  A device
  * wait that runs out of time is reported like a decode step's (mbk_get_status). */
 #define MBK_PREFILL_LOGITS_NONE 0
 #define MBK_PREFILL_LOGITS_LAST 1
@@ -265,6 +266,14 @@ int mbk_debug_taps(mbk_handle *h, float *taps_out);
  * the embedding) instead of layer l-1's output, so every layer can be compared with a reference
  * from identical inputs.  It applies to one step; passing NULL cancels it.  Not for decoding. */
 int mbk_debug_inject(mbk_handle *h, const float *x_in);
+
+/* The same for prefill: makes the NEXT mbk_prefill call, which must have n_tokens tokens, read as
+ * the residual stream entering each layer l >= 1 block l of the HOST buffer x_in
+ * ([n_layers][n_tokens][hidden] fp32, copied before this call returns; block 0 is ignored) instead of
+ * layer l-1's output.  Every layer's K/V rows then come from identical inputs on both sides of a
+ * comparison.  Passing NULL cancels it.  Errors: MBK_ERR_INVALID_ARG for n_tokens outside
+ * [1, kv_capacity]; MBK_ERR_NOMEM / MBK_ERR_CUDA.  Not for decoding. */
+int mbk_debug_prefill_inject(mbk_handle *h, const float *x_in, int32_t n_tokens);
 
 /* Static schedule of the handle: writes up to `capacity` rows of 6 int32
  * {cta, type (1 QKV, 2 ATTN, 3 OPROJ, 4 GATEUP, 5 DOWN, 6 LMHEAD), layer, row0, nrows, nchunks}

@@ -61,6 +61,9 @@ struct mbk_handle {
   // workspace and tensor maps of the tensor-core path
   std::vector<LayerW> bf16_layers;
   PrefillState prefill;
+  float* d_prefill_inject = nullptr;  // mbk_debug_prefill_inject: [L][n][H] layer inputs of the next prefill
+  int prefill_inject_n = 0;           // its token count (0: not armed)
+  size_t prefill_inject_cap = 0;      // floats allocated
   unsigned long long* d_trace = nullptr;
   unsigned long long* d_inject = nullptr;
   bool inject_armed = false;
@@ -126,6 +129,7 @@ void free_all(mbk_handle* h) {
   cudaFree(h->d_fp8);
   cudaFree(h->d_wscale);
   prefill_free(h->prefill);
+  cudaFree(h->d_prefill_inject);
   cudaFree(h->d_trace);
   cudaFree(h->d_inject);
   if (h->h_status) cudaFreeHost(h->h_status);
@@ -551,6 +555,7 @@ int mbk_prefill(mbk_handle* h, const int32_t* tokens, int32_t n_tokens, int32_t 
     if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
   if (h->cfg.weight_format != MBK_WEIGHTS_BF16) return MBK_ERR_UNSUPPORTED;
   if (h->inject_armed) return MBK_ERR_STATE;
+  if (h->prefill_inject_n != 0 && h->prefill_inject_n != n_tokens) return MBK_ERR_INVALID_ARG;
   if (int st = sticky_status(h)) return st;
   if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
   const KernelParams& kp = h->kp;
@@ -578,7 +583,31 @@ int mbk_prefill(mbk_handle* h, const int32_t* tokens, int32_t n_tokens, int32_t 
   m.status = kp.status;
   m.host_status = kp.host_status;
   m.timeout_ns = kp.timeout_ns;
-  return prefill_run(m, h->prefill, tokens, n_tokens, position, logits_out, logits_mode, (cudaStream_t)stream);
+  const float* inject = h->prefill_inject_n != 0 ? h->d_prefill_inject : nullptr;
+  h->prefill_inject_n = 0;  // one call
+  return prefill_run(m, h->prefill, tokens, n_tokens, position, logits_out, logits_mode, (cudaStream_t)stream, inject);
+}
+
+int mbk_debug_prefill_inject(mbk_handle* h, const float* x_in, int32_t n_tokens) {
+  if (!h) return MBK_ERR_INVALID_ARG;
+  if (!x_in) {
+    h->prefill_inject_n = 0;
+    return MBK_OK;
+  }
+  if (n_tokens < 1 || n_tokens > h->cfg.kv_capacity) return MBK_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
+  const size_t n = (size_t)h->cfg.n_layers * n_tokens * h->cfg.hidden;
+  if (n > h->prefill_inject_cap) {
+    cudaFree(h->d_prefill_inject);
+    h->d_prefill_inject = nullptr;
+    h->prefill_inject_cap = 0;
+    if (cudaMalloc(&h->d_prefill_inject, n * sizeof(float)) != cudaSuccess) return MBK_ERR_NOMEM;
+    h->prefill_inject_cap = n;
+  }
+  if (cudaMemcpy(h->d_prefill_inject, x_in, n * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MBK_ERR_CUDA;
+  h->prefill_inject_n = n_tokens;
+  return MBK_OK;
 }
 
 int mbk_decode_step_host(mbk_handle* h, int32_t token_id, int32_t position, float* logits_host, void* stream) {

@@ -679,7 +679,7 @@ void prefill_free(PrefillState& s) {
 }
 
 int prefill_run(const PrefillModel& m, PrefillState& s, const int32_t* tokens_host, int n, int p0, float* logits,
-                int mode, cudaStream_t st) {
+                int mode, cudaStream_t st, const float* inject) {
   if (encoder() == nullptr) return MBK_ERR_UNSUPPORTED;
   const int qd = m.nq * m.d, kvd = m.nkv * m.d, qkvd = qd + 2 * kvd;
   if (!s.smem_set) {
@@ -723,6 +723,8 @@ int prefill_run(const PrefillModel& m, PrefillState& s, const int32_t* tokens_ho
   for (int l = 0; ok && l < m.L; ++l) {
     const LayerW& w = m.layers[l];
     const CUtensorMap* lm = &s.wmaps[(size_t)l * WM_PER_LAYER];
+    if (inject != nullptr && l >= 1)
+      ck(cudaMemcpyAsync(s.x, inject + (size_t)l * n * m.H, sizeof(float) * (size_t)n * m.H, cudaMemcpyDeviceToDevice, st));
     // attention sublayer
     norm_split_kernel<<<rows_grid, 256, 0, st>>>(s.x, m.H, w.w[LW_ATTN_NORM], m.eps, m.inv_H, 0, n, s.a_hi, s.a_lo);
     ck(cudaGetLastError());

@@ -58,8 +58,10 @@ enum PrefillLogits { PL_NONE = 0, PL_LAST = 1, PL_ALL = 2 };
 // Runs the prefill on `stream` (asynchronous after the token copy).  tokens_host: n ids, already
 // validated by the caller; positions p0 .. p0 + n - 1 lie inside the cache.  logits: device fp32,
 // [n][V] (PL_ALL), [V] (PL_LAST) or unused (PL_NONE).  Returns an MBK_* code.
+// inject (diagnostics; may be null): device fp32 [L][n][H]; block l >= 1 replaces the residual stream
+// entering layer l.
 int prefill_run(const PrefillModel& m, PrefillState& st, const int32_t* tokens_host, int n, int p0, float* logits,
-                int mode, cudaStream_t stream);
+                int mode, cudaStream_t stream, const float* inject = nullptr);
 
 // Frees the workspace (the tensor maps are host memory).
 void prefill_free(PrefillState& st);

@@ -28,7 +28,8 @@ MBK_ERR_STATE = -6
 EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fill", "mbk_get_status",
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
             "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps",
-            "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8", "mbk_prefill")
+            "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8", "mbk_prefill",
+            "mbk_debug_prefill_inject")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -94,6 +95,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_decode_greedy.restype = ctypes.c_int
         lib.mbk_prefill.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         lib.mbk_prefill.restype = ctypes.c_int
+        lib.mbk_debug_prefill_inject.argtypes = [vp, vp, i32]
+        lib.mbk_debug_prefill_inject.restype = ctypes.c_int
         lib.mbk_create_paged.argtypes = [ctypes.POINTER(MbkConfig), ctypes.POINTER(MbkWeights), vp, i32, i32, ctypes.c_int,
                                          ctypes.POINTER(vp)]
         lib.mbk_create_paged.restype = ctypes.c_int
@@ -181,6 +184,15 @@ def mbk_prefill(h, tokens, position: int, logits_ptr: int, logits_mode: int, str
     arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     return load_library().mbk_prefill(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), int(position),
                                       ctypes.c_void_p(logits_ptr or None), int(logits_mode), ctypes.c_void_p(stream_ptr))
+
+
+def mbk_debug_prefill_inject(h, x_in, n_tokens: int) -> int:
+    """x_in: host fp32 array [n_layers][n_tokens][hidden] (or None to cancel)."""
+    import numpy as np
+    if x_in is None:
+        return load_library().mbk_debug_prefill_inject(h, None, int(n_tokens))
+    arr = np.ascontiguousarray(np.asarray(x_in, dtype=np.float32))
+    return load_library().mbk_debug_prefill_inject(h, arr.ctypes.data_as(ctypes.c_void_p), int(n_tokens))
 
 
 def mbk_create_paged(cfg: MbkConfig, weights: MbkWeights, kv_pool_ptr: int, num_pages: int, page_size: int,
