@@ -335,3 +335,105 @@ static int decode_step(const orc_config *cfg, const uint16_t *embed, const uint1
   free(x); free(xn); free(y); free(q); free(k); free(v); free(o); free(g); free(u); free(hbuf);
   return 0;
 }
+
+/* Causal attention of the n tokens of a prefill at one layer: token t (position p0 + t) scores every
+ * key 0 .. p0 + n - 1 and masks keys above its own position with -inf before the softmax. */
+static void causal_attention(const float *q, const uint16_t *K, const uint16_t *V, int nq, int nkv, int d, int cap,
+                             int n, int p0, float *o) {
+  const int group = nq / nkv, nkeys = p0 + n;
+  const double scale = 1.0 / sqrt((double)d);
+  double *sc = (double *)malloc(sizeof(double) * (size_t)nkeys);
+  for (int t = 0; t < n; ++t)
+    for (int h = 0; h < nq; ++h) {
+      const float *qh = q + ((size_t)t * nq + h) * d;
+      const uint16_t *Kh = K + (size_t)(h / group) * cap * d;
+      const uint16_t *Vh = V + (size_t)(h / group) * cap * d;
+      double m = -INFINITY;
+      for (int j = 0; j < nkeys; ++j) {
+        if (j > p0 + t) {
+          sc[j] = -INFINITY; /* the causal mask */
+          continue;
+        }
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += (double)qh[i] * (double)orc_bf16_to_f32(Kh[(size_t)j * d + i]);
+        sc[j] = acc * scale;
+        if (sc[j] > m) m = sc[j];
+      }
+      double z = 0.0;
+      for (int j = 0; j < nkeys; ++j) {
+        sc[j] = exp(sc[j] - m); /* exp(-inf) = 0 for masked keys */
+        z += sc[j];
+      }
+      for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < nkeys; ++j) acc += sc[j] * (double)orc_bf16_to_f32(Vh[(size_t)j * d + i]);
+        o[((size_t)t * nq + h) * d + i] = (float)(acc / z);
+      }
+    }
+  free(sc);
+}
+
+int orc_prefill(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                uint16_t *kv_cache, const int32_t *tokens, int n, int p0, float *logits, int nthreads) {
+  if (!cfg || !embed || !layers || !kv_cache || !tokens || !config_ok(cfg) || n < 1 || p0 < 0 ||
+      p0 > cfg->kv_capacity - n)
+    return -1;
+  for (int t = 0; t < n; ++t)
+    if (tokens[t] < 0 || tokens[t] >= cfg->vocab) return -1;
+  const int L = cfg->n_layers, H = cfg->hidden, I = cfg->intermediate;
+  const int nq = cfg->n_heads, nkv = cfg->n_kv_heads, d = cfg->head_dim, cap = cfg->kv_capacity;
+  const size_t qdim = (size_t)nq * d, kvdim = (size_t)nkv * d;
+  float *x = (float *)malloc(sizeof(float) * (size_t)n * H);
+  float *q = (float *)malloc(sizeof(float) * (size_t)n * qdim);
+  float *o = (float *)malloc(sizeof(float) * (size_t)n * qdim);
+  float *xn = (float *)malloc(sizeof(float) * H);
+  float *y = (float *)malloc(sizeof(float) * H);
+  float *kr = (float *)malloc(sizeof(float) * kvdim);
+  float *vr = (float *)malloc(sizeof(float) * kvdim);
+  float *gt = (float *)malloc(sizeof(float) * I);
+  float *ut = (float *)malloc(sizeof(float) * I);
+  float *ht = (float *)malloc(sizeof(float) * I);
+
+  for (int t = 0; t < n; ++t)
+    for (int i = 0; i < H; ++i) x[(size_t)t * H + i] = orc_bf16_to_f32(embed[(size_t)tokens[t] * H + i]);
+  for (int l = 0; l < L; ++l) {
+    const orc_layer *w = &layers[l];
+    uint16_t *Kc = kv_cache + (size_t)l * 2 * nkv * cap * d;
+    uint16_t *Vc = Kc + (size_t)nkv * cap * d;
+    /* every token's projections and cache rows first */
+    for (int t = 0; t < n; ++t) {
+      const int pos = p0 + t;
+      float *qt = q + (size_t)t * qdim;
+      orc_rmsnorm(x + (size_t)t * H, w->attn_norm, H, cfg->rms_eps, xn);
+      orc_gemv(w->wq, xn, cfg->qkv_bias ? w->bq : NULL, nq * d, H, qt, nthreads);
+      orc_gemv(w->wk, xn, cfg->qkv_bias ? w->bk : NULL, nkv * d, H, kr, nthreads);
+      orc_gemv(w->wv, xn, cfg->qkv_bias ? w->bv : NULL, nkv * d, H, vr, nthreads);
+      orc_rope(qt, nq, d, pos, cfg->rope_theta);
+      orc_rope(kr, nkv, d, pos, cfg->rope_theta);
+      for (int h = 0; h < nkv; ++h)
+        for (int i = 0; i < d; ++i) {
+          Kc[((size_t)h * cap + pos) * d + i] = orc_f32_to_bf16(kr[(size_t)h * d + i]);
+          Vc[((size_t)h * cap + pos) * d + i] = orc_f32_to_bf16(vr[(size_t)h * d + i]);
+        }
+    }
+    causal_attention(q, Kc, Vc, nq, nkv, d, cap, n, p0, o);
+    for (int t = 0; t < n; ++t) {
+      float *xt = x + (size_t)t * H;
+      orc_gemv(w->wo, o + (size_t)t * qdim, NULL, H, nq * d, y, nthreads);
+      for (int i = 0; i < H; ++i) xt[i] = (float)((double)xt[i] + (double)y[i]);
+      orc_rmsnorm(xt, w->mlp_norm, H, cfg->rms_eps, xn);
+      orc_gemv(w->w_gate, xn, NULL, I, H, gt, nthreads);
+      orc_gemv(w->w_up, xn, NULL, I, H, ut, nthreads);
+      orc_silu_mul(gt, ut, I, ht);
+      orc_gemv(w->w_down, ht, NULL, H, I, y, nthreads);
+      for (int i = 0; i < H; ++i) xt[i] = (float)((double)xt[i] + (double)y[i]);
+    }
+  }
+  if (logits)
+    for (int t = 0; t < n; ++t) {
+      orc_rmsnorm(x + (size_t)t * H, final_norm, H, cfg->rms_eps, xn);
+      orc_gemv(embed, xn, NULL, cfg->vocab, H, logits + (size_t)t * cfg->vocab, nthreads);
+    }
+  free(x); free(q); free(o); free(xn); free(y); free(kr); free(vr); free(gt); free(ut); free(ht);
+  return 0;
+}

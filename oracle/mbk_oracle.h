@@ -123,6 +123,17 @@ int orc_decode_step_fp8(const orc_config *cfg, const uint16_t *embed, const uint
                         const orc_fp8_weights *fp8, uint16_t *kv_cache, int token, int pos, float *logits, float *taps,
                         int nthreads);
 
+/* ---- prefill: n given tokens at positions p0 .. p0 + n - 1 (its plain definition) ----
+ * The pages give prefill no computation of its own (the article, "Where it loses", only measures the
+ * megakernel's prefill path), so this is the teacher-forced decode of the n tokens written
+ * layer-major: each layer takes all n tokens, appends all their K/V rows, then token t attends over
+ * the cache rows 0 .. p0 + t through an explicit causal mask on the scores of every key up to
+ * p0 + n - 1 (masked scores are -inf, so they add exact zeros).  Every other op is the decode step's.
+ * logits: fp32 [n][V], or NULL (cache only).  Returns 0, or -1 for an invalid argument.
+ * Pin: equals n calls of orc_decode_step bit for bit (logits and cache). */
+int orc_prefill(const orc_config *cfg, const uint16_t *embed, const uint16_t *final_norm, const orc_layer *layers,
+                uint16_t *kv_cache, const int32_t *tokens, int n, int p0, float *logits, int nthreads);
+
 /* Number of OpenMP threads the oracle would use for nthreads <= 0 (1 without OpenMP). */
 int orc_max_threads(void);
 

@@ -93,6 +93,9 @@ def bind(lib):
     lib.orc_decode_step_fp8.argtypes = [ctypes.POINTER(_Config), _P, _P, ctypes.POINTER(_Layer),
                                         ctypes.POINTER(_Fp8Weights), _P, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int]
     lib.orc_decode_step_fp8.restype = ctypes.c_int
+    lib.orc_prefill.argtypes = [ctypes.POINTER(_Config), _P, _P, ctypes.POINTER(_Layer), _P, _P, ctypes.c_int,
+                                ctypes.c_int, _P, ctypes.c_int]
+    lib.orc_prefill.restype = ctypes.c_int
     return lib
 
 
@@ -197,3 +200,17 @@ class OracleDecoder:
         if rc != 0:
             raise ValueError(f"oracle rejected token={token} pos={pos}")
         return (logits, tap) if taps else logits
+
+    def prefill(self, tokens, p0: int, logits: bool = True):
+        """The n given tokens at positions p0 .. p0 + n - 1, layer by layer (orc_prefill); logits [n][V]."""
+        if self.fp8 is not None:
+            raise ValueError("the oracle's prefill takes the bf16 weights")
+        s = self.shape
+        toks = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        out = np.empty((toks.size, s.vocab), dtype=np.float32) if logits else None
+        rc = self.lib.orc_prefill(ctypes.byref(self.cfg), self.embed.ctypes.data, self.final_norm.ctypes.data,
+                                  self.layers, self.kv.ctypes.data, toks.ctypes.data, int(toks.size), int(p0),
+                                  _ptr(out), self.nthreads)
+        if rc != 0:
+            raise ValueError(f"oracle rejected a prefill of {toks.size} tokens at {p0}")
+        return out

@@ -351,3 +351,22 @@ def pin_fp8_decoder_vs_torch(lib, wl, n_steps, decoder_cls):
         got = dec.step(int(wl.tokens[i]), wl.shape.pos0 + i).astype(np.float64)
         rel = float(np.linalg.norm(got - ref[i]) / np.linalg.norm(ref[i]))
         assert rel < 1e-5, f"step {i}: rel L2 {rel}"
+
+
+def pin_prefill_equals_decode_steps(lib_unused, wl, n, p0, decoder_cls, seed=21):
+    """The oracle's prefill (layer-major over the prompt, causal attention through an explicit mask on
+    the scores of every key of the prompt) against its teacher-forced decode steps: the prefill's
+    definition is those steps, and with masked scores adding exact zeros the two agree bit for bit --
+    logits of every token and every cache row.  A prefill that lets a token see a later key, hides its
+    own row, rotates by the wrong position or writes a row to the wrong place differs."""
+    s = wl.shape
+    g = torch.Generator().manual_seed(seed)
+    toks = [int(t) for t in torch.randint(0, s.vocab, (p0 + n,), generator=g)]
+    a, b = decoder_cls(wl), decoder_cls(wl)
+    for i in range(p0):
+        a.step(toks[i], i)
+        b.step(toks[i], i)
+    steps = np.stack([a.step(toks[p0 + i], p0 + i) for i in range(n)])
+    pre = b.prefill(toks[p0:p0 + n], p0)
+    assert np.array_equal(steps.view(np.uint32), pre.view(np.uint32))
+    assert np.array_equal(a.kv, b.kv)

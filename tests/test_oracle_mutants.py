@@ -43,6 +43,13 @@ MUTANTS = [
     ("final_norm_gain_dropped", "orc_rmsnorm(x, final_norm, H, cfg->rms_eps, xn);", "orc_rmsnorm(x, NULL, H, cfg->rms_eps, xn);", None),
     ("v_row_from_k", "Vc[((size_t)h * cap + pos) * d + t] = orc_f32_to_bf16(v[(size_t)h * d + t]);",
      "Vc[((size_t)h * cap + pos) * d + t] = orc_f32_to_bf16(k[(size_t)h * d + t]);", None),
+    # the prefill's own code (layer-major, explicit causal mask)
+    ("prefill_not_causal", "if (j > p0 + t) {", "if (j > p0 + n - 1) {", None),
+    ("prefill_mask_one_ahead", "if (j > p0 + t) {", "if (j > p0 + t + 1) {", None),
+    ("prefill_q_rotated_by_token_index", "orc_rope(qt, nq, d, pos, cfg->rope_theta);",
+     "orc_rope(qt, nq, d, t, cfg->rope_theta);", None),
+    ("prefill_row_at_token_index", "Kc[((size_t)h * cap + pos) * d + i] = orc_f32_to_bf16(kr[(size_t)h * d + i]);",
+     "Kc[((size_t)h * cap + t) * d + i] = orc_f32_to_bf16(kr[(size_t)h * d + i]);", None),
 ]
 
 
@@ -85,6 +92,7 @@ def _all_pins(lib, decoders):
         lambda: pins.pin_decoder_vs_torch(lib, tiny, 4, lambda wl: OracleDecoder(wl, lib=lib)),
         lambda: pins.pin_decoder_vs_torch(lib, gains, 3, lambda wl: OracleDecoder(wl, lib=lib)),
         lambda: pins.pin_decoder_vs_torch(lib, bias, 3, lambda wl: OracleDecoder(wl, lib=lib)),
+        lambda: pins.pin_prefill_equals_decode_steps(lib, tiny, 12, 5, lambda wl: OracleDecoder(wl, lib=lib)),
     ]
     failed = []
     for i, chk in enumerate(checks):
