@@ -147,3 +147,13 @@ def test_schedule_variants_build_and_check(lib, monkeypatch, name, env):
     base = (s.n_heads * s.head_dim * s.hidden + 2 * s.n_kv_heads * s.head_dim * s.hidden
             + s.hidden * s.n_heads * s.head_dim + 3 * s.hidden * s.intermediate) * 2
     assert info.weight_bytes == s.n_layers * base + s.vocab * s.hidden * 2
+
+
+def test_prefill_entry_points_reject_a_null_handle_before_touching_a_gpu(lib):
+    toks = (ctypes.c_int32 * 2)(1, 2)
+    assert lib.mbk_prefill(None, toks, 2, 0, None, 0, None) == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_prefill(None, None, 0, 0, None, 1, None) == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_debug_prefill_inject(None, None, 0) == mbk.MBK_ERR_INVALID_ARG
+    # the Python wrapper marshals a token sequence and the logits modes
+    assert mbk.mbk_prefill(None, [1, 2, 3], 0, 0, mbk.PREFILL_LOGITS["last"], 0) == mbk.MBK_ERR_INVALID_ARG
+    assert set(mbk.PREFILL_LOGITS.values()) == {0, 1, 2}
