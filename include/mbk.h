@@ -310,6 +310,31 @@ typedef struct {
  * fails.  Weight addresses are taken from a fake base so no device memory is needed. */
 int mbk_plan_check(const mbk_config *cfg, int num_sms, mbk_plan_info *info);
 
+/* Execution model of the schedule's exchange protocol (host only; no GPU needed).  Builds the plan as
+ * mbk_plan_check does and runs one step at `position` through a model of the kernel's waits: every CTA
+ * runs its task list in order, and a task runs once every activation word it reads (its input vector,
+ * residual rows, per-KV-head partials, the active context splits' outputs, or for attention its KV
+ * head's q/k/v words) has been written in this step; it then writes its output words.  Readiness only
+ * grows within a step, so if tasks remain when no task is ready the plan can deadlock on the GPU
+ * whatever the timing (the kernel's bounded waits would then report MBK_ERR_TIMEOUT).  The depths
+ * count exchange rounds: the longest chain of tasks each reading a word its predecessor wrote.  The
+ * same environment knobs as a handle apply (MBK_MAX_TASKS_PER_OP, MBK_FUSE_ATTENTION and the
+ * fault-injection knob MBK_DEBUG_DROP_TASK).  Returns MBK_OK when every task ran and no word was
+ * written twice, MBK_ERR_STATE otherwise (details in *info), MBK_ERR_INVALID_ARG for a bad argument
+ * or an unsupported shape. */
+typedef struct {
+  int tasks_total;              /* tasks in the plan */
+  int tasks_run;                /* tasks that could run: all of them unless the plan can deadlock */
+  int exchange_depth;           /* longest chain of tasks each reading a word written by the one before */
+  int schedule_depth;           /* the same, with each CTA's task order counted as a dependency too */
+  int64_t words_written_twice;  /* output words written by more than one task (0 in a valid plan) */
+  int stuck_cta;                /* -1, or the first CTA whose next task never becomes ready */
+  int stuck_task_type;          /* that task's type (1 QKV, 2 ATTN, 3 OPROJ, 4 GATEUP, 5 DOWN, 6 LMHEAD) */
+  int stuck_layer;              /* ... and layer */
+  int64_t stuck_word;           /* a word it waits for that no task writes before it (-1 if none) */
+} mbk_sim_info;
+int mbk_plan_simulate(const mbk_config *cfg, int num_sms, int position, mbk_sim_info *info);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libmbk.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 CU_SOURCES = ["mbk_kernel.cu", "mbk_api.cu", "mbk_static.cu", "mbk_prefill.cu"]
-CPP_SOURCES = ["mbk_sched.cpp"]
+CPP_SOURCES = ["mbk_sched.cpp", "mbk_simulate.cpp"]
 HEADERS = ["mbk_plan.h", "mbk_device.h", "mbk_sched.h", "mbk_prefill.h"]
 
 

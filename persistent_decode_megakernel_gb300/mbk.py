@@ -29,7 +29,7 @@ EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fil
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
             "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps",
             "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8", "mbk_prefill",
-            "mbk_debug_prefill_inject")
+            "mbk_debug_prefill_inject", "mbk_plan_simulate")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -66,6 +66,12 @@ class MbkPlanInfo(ctypes.Structure):
                 ("stage_bytes", ctypes.c_int), ("num_stages", ctypes.c_int), ("attn_splits", ctypes.c_int),
                 ("weight_bytes", ctypes.c_int64), ("max_cta_bytes", ctypes.c_int64), ("act_words", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int)]
+
+
+class MbkSimInfo(ctypes.Structure):
+    _fields_ = [("tasks_total", ctypes.c_int), ("tasks_run", ctypes.c_int), ("exchange_depth", ctypes.c_int),
+                ("schedule_depth", ctypes.c_int), ("words_written_twice", ctypes.c_int64), ("stuck_cta", ctypes.c_int),
+                ("stuck_task_type", ctypes.c_int), ("stuck_layer", ctypes.c_int), ("stuck_word", ctypes.c_int64)]
 
 
 _lib = None
@@ -116,6 +122,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_destroy.restype = None
         lib.mbk_plan_check.argtypes = [ctypes.POINTER(MbkConfig), ctypes.c_int, ctypes.POINTER(MbkPlanInfo)]
         lib.mbk_plan_check.restype = ctypes.c_int
+        lib.mbk_plan_simulate.argtypes = [ctypes.POINTER(MbkConfig), ctypes.c_int, ctypes.c_int, ctypes.POINTER(MbkSimInfo)]
+        lib.mbk_plan_simulate.restype = ctypes.c_int
         lib.mbk_debug_taps.argtypes = [vp, vp]
         lib.mbk_debug_taps.restype = ctypes.c_int
         lib.mbk_debug_plan.argtypes = [vp, vp, ctypes.c_int64]
@@ -152,6 +160,13 @@ def mbk_plan_check(cfg: MbkConfig, num_sms: int) -> MbkPlanInfo:
     info = MbkPlanInfo()
     _check(load_library().mbk_plan_check(ctypes.byref(cfg), int(num_sms), ctypes.byref(info)), "mbk_plan_check")
     return info
+
+
+def mbk_plan_simulate(cfg: MbkConfig, num_sms: int, position: int):
+    """Runs one step of the schedule through the host model of the kernel's waits: (return code, MbkSimInfo)."""
+    info = MbkSimInfo()
+    rc = load_library().mbk_plan_simulate(ctypes.byref(cfg), int(num_sms), int(position), ctypes.byref(info))
+    return rc, info
 
 
 def mbk_create(cfg: MbkConfig, weights: MbkWeights, kv_cache_ptr: int, device: int) -> ctypes.c_void_p:

@@ -157,3 +157,59 @@ def test_prefill_entry_points_reject_a_null_handle_before_touching_a_gpu(lib):
     # the Python wrapper marshals a token sequence and the logits modes
     assert mbk.mbk_prefill(None, [1, 2, 3], 0, 0, mbk.PREFILL_LOGITS["last"], 0) == mbk.MBK_ERR_INVALID_ARG
     assert set(mbk.PREFILL_LOGITS.values()) == {0, 1, 2}
+
+
+# ---- the host execution model of the exchange protocol (mbk_plan_simulate)
+def _rounds_per_layer(s, fused):
+    return 4 if fused else 5  # QKV, attention (+ Wo when fused), [O projection], gate/up, down
+
+
+@pytest.mark.parametrize("name", list(workloads.SHAPES))
+@pytest.mark.parametrize("env", [{}, {"MBK_FUSE_ATTENTION": "0"}, {"MBK_MAX_TASKS_PER_OP": "38"},
+                                 {"MBK_MAX_TASKS_PER_OP": "1"}])
+def test_every_plan_runs_to_completion_in_the_wait_model(lib, monkeypatch, name, env):
+    """Every CTA's task list, run in order with each task waiting for the words it reads, completes at
+    the first position, the last, and the boundaries of the context splits: no schedule can deadlock
+    on the GPU.  Its depth is the exchange rounds per layer times the layers, plus the LM head."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    s = workloads.SHAPES[name]
+    cfg = mbk.config_from_shape(s)
+    info = mbk.mbk_plan_check(cfg, 152)
+    fused = None
+    positions = sorted({0, s.pos0, s.pos0 + s.steps - 1, s.kv_capacity - 1, min(1023, s.kv_capacity - 1),
+                        min(1024, s.kv_capacity - 1)})
+    for pos in positions:
+        rc, sim = mbk.mbk_plan_simulate(cfg, 152, pos)
+        assert rc == mbk.MBK_OK, (pos, sim.stuck_cta, sim.stuck_task_type, sim.stuck_layer, sim.stuck_word)
+        assert sim.tasks_run == sim.tasks_total == info.num_tasks and sim.words_written_twice == 0
+        depth = (sim.exchange_depth - 1) / s.n_layers
+        assert depth in (4, 5), sim.exchange_depth
+        fused = depth == 4 if fused is None else fused
+        assert sim.exchange_depth == s.n_layers * _rounds_per_layer(s, fused) + 1
+        assert sim.schedule_depth >= sim.exchange_depth
+    if env.get("MBK_FUSE_ATTENTION") == "0":
+        assert not fused
+
+
+def test_headline_plan_has_four_exchange_rounds_per_layer(lib):
+    rc, sim = mbk.mbk_plan_simulate(mbk.config_from_shape(workloads.SHAPES["smollm-135m"]), 152, 64)
+    assert rc == mbk.MBK_OK and sim.exchange_depth == 30 * 4 + 1 and sim.schedule_depth == sim.exchange_depth
+
+
+@pytest.mark.parametrize("drop", [0, 5, 400])
+def test_a_dropped_task_leaves_its_consumers_waiting(lib, monkeypatch, drop):
+    """The host-side fault injection a handle applies (one task removed from its CTA's list) shows up
+    in the model as a CTA stuck on a word that nothing writes, as the GPU's bounded waits would."""
+    monkeypatch.setenv("MBK_DEBUG_DROP_TASK", str(drop))
+    rc, sim = mbk.mbk_plan_simulate(mbk.config_from_shape(workloads.SHAPES["smollm-135m"]), 152, 10)
+    assert rc == mbk.MBK_ERR_STATE
+    assert sim.tasks_run < sim.tasks_total - 1
+    assert sim.stuck_cta >= 0 and sim.stuck_word >= 0 and 1 <= sim.stuck_task_type <= 6
+
+
+def test_simulate_rejects_bad_arguments(lib):
+    cfg = mbk.config_from_shape(workloads.SHAPES["tiny"])
+    assert mbk.mbk_plan_simulate(cfg, 0, 0)[0] == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_plan_simulate(cfg, 152, cfg.kv_capacity)[0] == mbk.MBK_ERR_INVALID_ARG
+    assert lib.mbk_plan_simulate(None, 152, 0, None) == mbk.MBK_ERR_INVALID_ARG
