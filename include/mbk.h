@@ -206,6 +206,28 @@ int mbk_decode_greedy(mbk_handle *h, int32_t first_token, int32_t n_steps, int32
 int mbk_prefill(mbk_handle *h, const int32_t *tokens, int32_t n_tokens, int32_t position, float *logits_out,
                 int32_t logits_mode, void *stream);
 
+/* Small-batch decode, and prompts of several sequences, in one step: n_seq sequences share a PAGED
+ * handle's pool (mbk_create_paged), each with its own page table, and sequence s contributes counts[s]
+ * tokens at positions starts[s] .. starts[s] + counts[s] - 1 -- one token for a decode step, or a
+ * chunk of a prompt.  The MegaBake README ("Current status") lists small-batch decode under "Next";
+ * the reading here: the step is, for every sequence, its counts[s] teacher-forced decode steps on its
+ * own cache (each token attends to its sequence's rows up to its own position), and the sequences do
+ * not interact.  All tokens of the step go through the prefill's tensor-core contractions together,
+ * so every weight is read once per step for up to 128 tokens, whatever the mix of decode tokens and
+ * prompt chunks.
+ *   tokens: HOST int32 array of sum(counts) ids, grouped by sequence in sequence order.
+ *   page_tables: HOST int32 [n_seq][ceil(kv_capacity / page_size)]: entry q of table s is the pool page
+ *     holding positions q * page_size .. of sequence s (entries past the last position used are not read).
+ *   logits_mode: MBK_PREFILL_LOGITS_NONE, _LAST (the last token of each sequence: DEVICE fp32
+ *     [n_seq][vocab]) or _ALL (every token, in token order: DEVICE fp32 [sum(counts)][vocab]).
+ * The handle's own page table (mbk_set_page_table) is neither used nor changed.
+ * Errors: MBK_ERR_INVALID_ARG for a NULL array, n_seq < 1, a contiguous handle, counts[s] < 1, a
+ * position outside [0, kv_capacity), a token outside [0, vocab), a table entry outside the pool, a
+ * page used twice (within or across the sequences' used ranges), an unknown logits_mode or NULL
+ * logits_out while logits are asked for; as mbk_prefill otherwise.  Not yet run on a GPU. */
+int mbk_batch_step(mbk_handle *h, int32_t n_seq, const int32_t *counts, const int32_t *starts, const int32_t *tokens,
+                   const int32_t *page_tables, float *logits_out, int32_t logits_mode, void *stream);
+
 /* As mbk_decode_step, then copies the logits into the HOST buffer logits_host (vocab floats;
  * pinned memory makes the copy asynchronous) and synchronises `stream` before returning. */
 int mbk_decode_step_host(mbk_handle *h, int32_t token_id, int32_t position, float *logits_host, void *stream);

@@ -543,19 +543,13 @@ int mbk_decode_greedy(mbk_handle* h, int32_t first_token, int32_t n_steps, int32
   return launch_steps(h, first_token, nullptr, n_steps, position, logits_out, stream, tokens_out);
 }
 
-int mbk_prefill(mbk_handle* h, const int32_t* tokens, int32_t n_tokens, int32_t position, float* logits_out,
-                int32_t logits_mode, void* stream) {
-  if (!h || !tokens || n_tokens < 1) return MBK_ERR_INVALID_ARG;
-  if (logits_mode != MBK_PREFILL_LOGITS_NONE && logits_mode != MBK_PREFILL_LOGITS_LAST &&
-      logits_mode != MBK_PREFILL_LOGITS_ALL)
-    return MBK_ERR_INVALID_ARG;
-  if (logits_mode != MBK_PREFILL_LOGITS_NONE && !logits_out) return MBK_ERR_INVALID_ARG;
-  if (position < 0 || n_tokens > h->mapped || position > h->mapped - n_tokens) return MBK_ERR_INVALID_ARG;
-  for (int32_t i = 0; i < n_tokens; ++i)
-    if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
+namespace {
+// The prefill path for n tokens grouped by sequence (mbk_prefill, mbk_batch_step); arguments validated.
+int run_tokens(mbk_handle* h, const PrefillBatch& batch, const int32_t* tokens, int32_t n, float* logits_out,
+               int32_t logits_mode, void* stream) {
   if (h->cfg.weight_format != MBK_WEIGHTS_BF16) return MBK_ERR_UNSUPPORTED;
   if (h->inject_armed) return MBK_ERR_STATE;
-  if (h->prefill_inject_n != 0 && h->prefill_inject_n != n_tokens) return MBK_ERR_INVALID_ARG;
+  if (h->prefill_inject_n != 0 && h->prefill_inject_n != n) return MBK_ERR_INVALID_ARG;
   if (int st = sticky_status(h)) return st;
   if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
   const KernelParams& kp = h->kp;
@@ -585,7 +579,55 @@ int mbk_prefill(mbk_handle* h, const int32_t* tokens, int32_t n_tokens, int32_t 
   m.timeout_ns = kp.timeout_ns;
   const float* inject = h->prefill_inject_n != 0 ? h->d_prefill_inject : nullptr;
   h->prefill_inject_n = 0;  // one call
-  return prefill_run(m, h->prefill, tokens, n_tokens, position, logits_out, logits_mode, (cudaStream_t)stream, inject);
+  return prefill_run(m, h->prefill, tokens, n, batch, logits_out, logits_mode, (cudaStream_t)stream, inject);
+}
+
+bool logits_mode_ok(int32_t mode, const float* logits_out) {
+  if (mode != MBK_PREFILL_LOGITS_NONE && mode != MBK_PREFILL_LOGITS_LAST && mode != MBK_PREFILL_LOGITS_ALL) return false;
+  return mode == MBK_PREFILL_LOGITS_NONE || logits_out != nullptr;
+}
+}  // namespace
+
+int mbk_prefill(mbk_handle* h, const int32_t* tokens, int32_t n_tokens, int32_t position, float* logits_out,
+                int32_t logits_mode, void* stream) {
+  if (!h || !tokens || n_tokens < 1 || !logits_mode_ok(logits_mode, logits_out)) return MBK_ERR_INVALID_ARG;
+  if (position < 0 || n_tokens > h->mapped || position > h->mapped - n_tokens) return MBK_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
+  PrefillBatch b;
+  b.n_seq = 1;
+  b.counts = &n_tokens;
+  b.starts = &position;
+  return run_tokens(h, b, tokens, n_tokens, logits_out, logits_mode, stream);
+}
+
+int mbk_batch_step(mbk_handle* h, int32_t n_seq, const int32_t* counts, const int32_t* starts, const int32_t* tokens,
+                   const int32_t* page_tables, float* logits_out, int32_t logits_mode, void* stream) {
+  if (!h || n_seq < 1 || !counts || !starts || !tokens || !page_tables) return MBK_ERR_INVALID_ARG;
+  if (!h->paged || !logits_mode_ok(logits_mode, logits_out)) return MBK_ERR_INVALID_ARG;
+  const int C = h->cfg.kv_capacity, ps = h->page_size;
+  std::vector<char> used(h->num_pages, 0);
+  int64_t n = 0;
+  for (int32_t q = 0; q < n_seq; ++q) {
+    if (counts[q] < 1 || starts[q] < 0 || counts[q] > C || starts[q] > C - counts[q]) return MBK_ERR_INVALID_ARG;
+    const int32_t* t = page_tables + (size_t)q * h->max_pages;
+    const int need = (starts[q] + counts[q] + ps - 1) / ps;  // pages the sequence's positions reach
+    for (int i = 0; i < need; ++i) {
+      if (t[i] < 0 || t[i] >= h->num_pages || used[t[i]]) return MBK_ERR_INVALID_ARG;  // in the pool, not shared
+      used[t[i]] = 1;
+    }
+    n += counts[q];
+  }
+  if (n > (int64_t)1 << 24) return MBK_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return MBK_ERR_INVALID_ARG;
+  PrefillBatch b;
+  b.n_seq = n_seq;
+  b.counts = counts;
+  b.starts = starts;
+  b.tables = page_tables;
+  b.max_pages = h->max_pages;
+  return run_tokens(h, b, tokens, (int32_t)n, logits_out, logits_mode, stream);
 }
 
 int mbk_debug_prefill_inject(mbk_handle* h, const float* x_in, int32_t n_tokens) {

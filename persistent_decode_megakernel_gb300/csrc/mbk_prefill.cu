@@ -371,13 +371,13 @@ __global__ void embed_kernel(const uint16_t* E, const int32_t* tokens, int n, in
   }
 }
 
-// Rows row0 .. row0 + n - 1 of x [.][H]: xn = x / sqrt(mean(x^2) + eps) * gain, written to rows
-// 0 .. n - 1 of the GEMM input pair (hi, lo) [.][H].
-__global__ void norm_split_kernel(const float* x, int H, const uint16_t* gain, float eps, float inv_H, int row0, int n,
-                                  uint16_t* hi, uint16_t* lo) {
+// Rows rows[r] (or r, when rows is null), r < n, of x [.][H]: xn = x / sqrt(mean(x^2) + eps) * gain,
+// written to rows 0 .. n - 1 of the GEMM input pair (hi, lo) [.][H].
+__global__ void norm_split_kernel(const float* x, int H, const uint16_t* gain, float eps, float inv_H,
+                                  const int32_t* rows, int n, uint16_t* hi, uint16_t* lo) {
   __shared__ float red[32];
   for (int r = blockIdx.x; r < n; r += gridDim.x) {
-    const float* xr = x + (size_t)(row0 + r) * H;
+    const float* xr = x + (size_t)(rows != nullptr ? rows[r] : r) * H;
     float ss = 0.f;
     for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
     const float inv = rsqrtf(block_sum(ss, red) * inv_H + eps);
@@ -385,29 +385,39 @@ __global__ void norm_split_kernel(const float* x, int H, const uint16_t* gain, f
   }
 }
 
-// Element offset of cache row p of (layer, kv = 0 for K / 1 for V, KV head h), contiguous or paged.
+// The cache: contiguous (tables null, page_size = capacity) or a pool of pages found through one page
+// table per sequence, tables[seq * max_pages + q] holding positions q * page_size ...
 struct KvGeom {
   uint16_t* kv;
-  const int32_t* page_table;
+  const int32_t* tables;
+  int max_pages;
   int page_size, page_shift, nkv, d;
   unsigned long long page_elems;
 };
-__device__ __forceinline__ size_t kv_index(const KvGeom& g, int layer, int kv, int h, int p) {
+__device__ __forceinline__ const int32_t* table_of(const KvGeom& g, int seq) {
+  return g.tables != nullptr ? g.tables + (size_t)seq * g.max_pages : nullptr;
+}
+// Element offset of cache row p of (layer, kv = 0 for K / 1 for V, KV head h) of the sequence whose
+// page table is `table` (null: contiguous).
+__device__ __forceinline__ size_t kv_index(const KvGeom& g, const int32_t* table, int layer, int kv, int h, int p) {
   size_t page = 0;
   int r = p;
-  if (g.page_table != nullptr) {
-    page = (size_t)(unsigned)g.page_table[p >> g.page_shift];
+  if (table != nullptr) {
+    page = (size_t)(unsigned)table[p >> g.page_shift];
     r = p & (g.page_size - 1);
   }
   return page * g.page_elems + ((((size_t)layer * 2 + kv) * g.nkv + h) * g.page_size + r) * g.d;
 }
 
-// Token t at position p0 + t: rotate its q and k heads in place (rotate-half pairs (i, i + d/2) by
-// the angle of table row p), then store its K and V rows in the cache as bf16 (nearest even).
-__global__ void rope_kv_kernel(float* qkv, int ld, int n, int p0, int nq, const float2* rope, KvGeom g, int layer) {
+// Token t (position pos[t] of sequence seq[t]): rotate its q and k heads in place (rotate-half pairs
+// (i, i + d/2) by the angle of table row p), then store its K and V rows in its sequence's cache as
+// bf16 (nearest even).
+__global__ void rope_kv_kernel(float* qkv, int ld, int n, const int32_t* pos, const int32_t* seq, int nq,
+                               const float2* rope, KvGeom g, int layer) {
   const int d = g.d, half = d / 2, nkv = g.nkv;
   for (int t = blockIdx.x; t < n; t += gridDim.x) {
-    const int p = p0 + t;
+    const int p = pos[t];
+    const int32_t* table = table_of(g, seq[t]);
     float* row = qkv + (size_t)t * ld;
     for (int e = threadIdx.x; e < (nq + nkv) * half; e += blockDim.x) {
       const int hh = e / half, i = e - hh * half;  // heads: q heads, then k heads (contiguous)
@@ -420,7 +430,7 @@ __global__ void rope_kv_kernel(float* qkv, int ld, int n, int p0, int nq, const 
     __syncthreads();
     for (int e = threadIdx.x; e < 2 * nkv * d; e += blockDim.x) {
       const int sel = e / (nkv * d), rem = e - sel * nkv * d, h = rem / d, j = rem - h * d;
-      g.kv[kv_index(g, layer, sel, h, p) + j] = to_bf16(row[(size_t)(nq + sel * nkv) * d + rem]);
+      g.kv[kv_index(g, table, layer, sel, h, p) + j] = to_bf16(row[(size_t)(nq + sel * nkv) * d + rem]);
     }
     __syncthreads();
   }
@@ -437,7 +447,8 @@ __global__ void silu_split_kernel(const float* gu, int n, int I, uint16_t* hi, u
 }
 
 // ------------------------------------------------------------------ causal attention
-// One CTA: kAttnWarps consecutive tokens (one per warp) and one KV head with its g query heads.
+// One CTA: a tile of at most kAttnWarps tokens of one sequence at consecutive positions (one per warp;
+// tiles are built on the host) and one KV head with its g query heads.
 // Keys are staged 32 at a time in shared memory (one per lane for the scores; K rows padded to an
 // odd number of words so that the lanes' rows fall in different banks), each warp keeps an online
 // softmax per query head (running max, sum and output), and a token stops at its own position.
@@ -449,7 +460,10 @@ struct AttnArgs {
   const float* qkv;             // rotated q at columns [0, nq * d) of row t
   int ld;
   KvGeom kv;
-  int layer, nq, g, n, p0;
+  const int32_t* pos;           // [n] position of each token
+  const int32_t* seq;           // [n] its sequence
+  const int2* tiles;            // [blocks] (first token, tokens) of each tile
+  int layer, nq, g;
   float scale_log2;             // 1/sqrt(d) * log2(e): scores in base 2
   uint16_t* o_hi;               // [n][nq * d] attention output, split for the O GEMM
   uint16_t* o_lo;
@@ -471,10 +485,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32) prefill_attn_kernel(const Att
   float* qs = reinterpret_cast<float*>(vs + kAttnKeys * VW);  // [warps][g][D]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y, g = a.g;
-  const int t0 = blockIdx.x * kAttnWarps, t = t0 + warp;
-  const bool active = t < a.n;
-  const int pos = a.p0 + t;
-  const int last = a.p0 + min(t0 + kAttnWarps, a.n) - 1;  // the CTA's largest position
+  const int2 tile = a.tiles[blockIdx.x];
+  const int t0 = tile.x, t = t0 + warp;
+  const bool active = warp < tile.y;
+  const int pos = active ? a.pos[t] : -1;
+  const int last = a.pos[t0 + tile.y - 1];  // the tile's largest position (positions increase in a tile)
+  const int32_t* table = table_of(a.kv, a.seq[t0]);
   float* q = qs + (size_t)warp * g * D;
   if (active)
     for (int e = lane; e < g * D; e += 32) q[e] = a.qkv[(size_t)t * a.ld + (size_t)kvh * g * D + e];
@@ -495,8 +511,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) prefill_attn_kernel(const Att
       const int r = e / (D / 8), piece = e - r * (D / 8), p = c0 + r;
       uint4 kk = make_uint4(0u, 0u, 0u, 0u), vv = kk;
       if (p <= last) {
-        kk = *reinterpret_cast<const uint4*>(a.kv.kv + kv_index(a.kv, a.layer, 0, kvh, p) + piece * 8);
-        vv = *reinterpret_cast<const uint4*>(a.kv.kv + kv_index(a.kv, a.layer, 1, kvh, p) + piece * 8);
+        kk = *reinterpret_cast<const uint4*>(a.kv.kv + kv_index(a.kv, table, a.layer, 0, kvh, p) + piece * 8);
+        vv = *reinterpret_cast<const uint4*>(a.kv.kv + kv_index(a.kv, table, a.layer, 1, kvh, p) + piece * 8);
       }
       uint32_t* kd = ks + r * KW + piece * 4;
       kd[0] = kk.x;
@@ -622,20 +638,22 @@ cudaError_t gemm(const PrefillModel& m, const CUtensorMap& a_hi, const CUtensorM
   return cudaGetLastError();
 }
 
-cudaError_t attention(const PrefillModel& m, const PrefillState& s, int layer, int n, int p0, cudaStream_t st) {
+cudaError_t attention(const PrefillModel& m, const PrefillState& s, const KvGeom& geom, int layer, int ntiles,
+                      cudaStream_t st) {
   AttnArgs a;
   a.qkv = s.qkv;
   a.ld = (m.nq + 2 * m.nkv) * m.d;
-  a.kv = KvGeom{m.kv, m.page_table, m.page_size, m.page_shift, m.nkv, m.d, m.page_elems};
+  a.kv = geom;
+  a.pos = s.pos;
+  a.seq = s.seq;
+  a.tiles = s.tiles;
   a.layer = layer;
   a.nq = m.nq;
   a.g = m.nq / m.nkv;
-  a.n = n;
-  a.p0 = p0;
   a.scale_log2 = m.attn_scale * 1.4426950408889634f;
   a.o_hi = s.a_hi;
   a.o_lo = s.a_lo;
-  const dim3 grid((unsigned)((n + kAttnWarps - 1) / kAttnWarps), (unsigned)m.nkv);
+  const dim3 grid((unsigned)ntiles, (unsigned)m.nkv);
   if (m.d == 64)
     prefill_attn_kernel<64><<<grid, kAttnWarps * 32, attn_smem<64>(a.g), st>>>(a);
   else
@@ -653,18 +671,50 @@ bool ensure_workspace(const PrefillModel& m, PrefillState& s, int n) {
   const size_t kmax = std::max(std::max((size_t)m.H, (size_t)m.I), qd);
   const size_t b_x = round256(sizeof(float) * cap * m.H), b_qkv = round256(sizeof(float) * cap * (qd + 2 * kvd));
   const size_t b_gu = round256(sizeof(float) * cap * 2 * m.I), b_a = round256(2 * cap * kmax);
-  const size_t b_tok = round256(sizeof(int32_t) * cap);
+  const size_t b_int = round256(sizeof(int32_t) * 6 * (size_t)cap);  // tokens, pos, seq, rows, tiles (2 each)
   unsigned char* w = nullptr;
-  if (cudaMalloc(reinterpret_cast<void**>(&w), b_x + b_qkv + b_gu + 2 * b_a + b_tok) != cudaSuccess) return false;
+  if (cudaMalloc(reinterpret_cast<void**>(&w), b_x + b_qkv + b_gu + 2 * b_a + b_int) != cudaSuccess) return false;
   s.ws = w;
   s.x = reinterpret_cast<float*>(w);
   s.qkv = reinterpret_cast<float*>(w + b_x);
   s.gu = reinterpret_cast<float*>(w + b_x + b_qkv);
   s.a_hi = reinterpret_cast<uint16_t*>(w + b_x + b_qkv + b_gu);
   s.a_lo = reinterpret_cast<uint16_t*>(w + b_x + b_qkv + b_gu + b_a);
-  s.tokens = reinterpret_cast<int32_t*>(w + b_x + b_qkv + b_gu + 2 * b_a);
+  s.tokens = reinterpret_cast<int32_t*>(w + b_x + b_qkv + b_gu + 2 * b_a);  // the int region: see pack_tokens
+  s.pos = s.tokens + cap;
+  s.seq = s.pos + cap;
+  s.rows = s.seq + cap;
+  s.tiles = reinterpret_cast<int2*>(s.rows + cap);
   s.cap = cap;
   return true;
+}
+
+// The int region of the workspace as one host image [tokens | pos | seq | rows | tiles] (cap entries
+// each, tiles two): the positions and sequence of every token, the last token of every sequence, and
+// the attention tiles (at most kAttnWarps consecutive tokens of one sequence).  Returns the tile count.
+int pack_tokens(const PrefillBatch& b, const int32_t* tokens, int n, int cap, std::vector<int32_t>& img) {
+  img.assign((size_t)6 * cap, 0);
+  int32_t* tok = img.data();
+  int32_t* pos = tok + cap;
+  int32_t* seq = pos + cap;
+  int32_t* rows = seq + cap;
+  int32_t* tiles = rows + cap;
+  int t = 0, nt = 0;
+  for (int q = 0; q < b.n_seq; ++q) {
+    for (int i = 0; i < b.counts[q]; ++i, ++t) {
+      tok[t] = tokens[t];
+      pos[t] = b.starts[q] + i;
+      seq[t] = q;
+      if (i % kAttnWarps == 0) {
+        tiles[2 * nt] = t;
+        tiles[2 * nt + 1] = std::min(kAttnWarps, b.counts[q] - i);
+        ++nt;
+      }
+    }
+    rows[q] = t - 1;
+  }
+  (void)n;
+  return nt;
 }
 
 }  // namespace
@@ -674,12 +724,16 @@ void prefill_free(PrefillState& s) {
   s.ws = nullptr;
   s.x = s.qkv = s.gu = nullptr;
   s.a_hi = s.a_lo = nullptr;
-  s.tokens = nullptr;
+  s.tokens = s.pos = s.seq = s.rows = nullptr;
+  s.tiles = nullptr;
   s.cap = 0;
+  if (s.tables != nullptr) cudaFree(s.tables);
+  s.tables = nullptr;
+  s.tables_cap = 0;
 }
 
-int prefill_run(const PrefillModel& m, PrefillState& s, const int32_t* tokens_host, int n, int p0, float* logits,
-                int mode, cudaStream_t st, const float* inject) {
+int prefill_run(const PrefillModel& m, PrefillState& s, const int32_t* tokens_host, int n, const PrefillBatch& batch,
+                float* logits, int mode, cudaStream_t st, const float* inject) {
   if (encoder() == nullptr) return MBK_ERR_UNSUPPORTED;
   const int qd = m.nq * m.d, kvd = m.nkv * m.d, qkvd = qd + 2 * kvd;
   if (!s.smem_set) {
@@ -711,34 +765,52 @@ int prefill_run(const PrefillModel& m, PrefillState& s, const int32_t* tokens_ho
   if (!make_map(&ah_H, s.a_hi, n, m.H) || !make_map(&al_H, s.a_lo, n, m.H) || !make_map(&ah_q, s.a_hi, n, qd) ||
       !make_map(&al_q, s.a_lo, n, qd) || !make_map(&ah_I, s.a_hi, n, m.I) || !make_map(&al_I, s.a_lo, n, m.I))
     return MBK_ERR_UNSUPPORTED;
-  if (cudaMemcpyAsync(s.tokens, tokens_host, sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  std::vector<int32_t> img;
+  const int ntiles = pack_tokens(batch, tokens_host, n, s.cap, img);
+  if (cudaMemcpyAsync(s.tokens, img.data(), sizeof(int32_t) * img.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MBK_ERR_CUDA;
+  KvGeom geom{m.kv, m.page_table, 0, m.page_size, m.page_shift, m.nkv, m.d, m.page_elems};
+  if (batch.tables != nullptr) {  // the batch's own page tables
+    const size_t ne = (size_t)batch.n_seq * batch.max_pages;
+    if (ne > s.tables_cap) {
+      if (s.tables != nullptr) cudaFree(s.tables);
+      s.tables = nullptr;
+      s.tables_cap = 0;
+      if (cudaMalloc(reinterpret_cast<void**>(&s.tables), sizeof(int32_t) * ne) != cudaSuccess) return MBK_ERR_NOMEM;
+      s.tables_cap = ne;
+    }
+    if (cudaMemcpyAsync(s.tables, batch.tables, sizeof(int32_t) * ne, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MBK_ERR_CUDA;
+    geom.tables = s.tables;
+    geom.max_pages = batch.max_pages;
+  }
 
   const unsigned rows_grid = (unsigned)std::min(n, 4096);
   bool ok = true;
   auto ck = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
   embed_kernel<<<rows_grid, 256, 0, st>>>(m.embed, s.tokens, n, m.H, s.x);
   ck(cudaGetLastError());
-  const KvGeom geom{m.kv, m.page_table, m.page_size, m.page_shift, m.nkv, m.d, m.page_elems};
   for (int l = 0; ok && l < m.L; ++l) {
     const LayerW& w = m.layers[l];
     const CUtensorMap* lm = &s.wmaps[(size_t)l * WM_PER_LAYER];
     if (inject != nullptr && l >= 1)
       ck(cudaMemcpyAsync(s.x, inject + (size_t)l * n * m.H, sizeof(float) * (size_t)n * m.H, cudaMemcpyDeviceToDevice, st));
     // attention sublayer
-    norm_split_kernel<<<rows_grid, 256, 0, st>>>(s.x, m.H, w.w[LW_ATTN_NORM], m.eps, m.inv_H, 0, n, s.a_hi, s.a_lo);
+    norm_split_kernel<<<rows_grid, 256, 0, st>>>(s.x, m.H, w.w[LW_ATTN_NORM], m.eps, m.inv_H, nullptr, n, s.a_hi,
+                                                 s.a_lo);
     ck(cudaGetLastError());
     const Seg qkv[3] = {{&lm[WM_Q], qd, 0, m.qkv_bias ? w.w[LW_BQ] : nullptr},
                         {&lm[WM_K], kvd, qd, m.qkv_bias ? w.w[LW_BK] : nullptr},
                         {&lm[WM_V], kvd, qd + kvd, m.qkv_bias ? w.w[LW_BV] : nullptr}};
     ck(gemm(m, ah_H, al_H, qkv, 3, n, m.H, s.qkv, qkvd, 0, st));
-    rope_kv_kernel<<<rows_grid, 256, 0, st>>>(s.qkv, qkvd, n, p0, m.nq, m.rope, geom, l);
+    rope_kv_kernel<<<rows_grid, 256, 0, st>>>(s.qkv, qkvd, n, s.pos, s.seq, m.nq, m.rope, geom, l);
     ck(cudaGetLastError());
-    ck(attention(m, s, l, n, p0, st));
+    ck(attention(m, s, geom, l, ntiles, st));
     const Seg o[1] = {{&lm[WM_O], m.H, 0, nullptr}};
     ck(gemm(m, ah_q, al_q, o, 1, n, qd, s.x, m.H, 1, st));
     // MLP sublayer
-    norm_split_kernel<<<rows_grid, 256, 0, st>>>(s.x, m.H, w.w[LW_MLP_NORM], m.eps, m.inv_H, 0, n, s.a_hi, s.a_lo);
+    norm_split_kernel<<<rows_grid, 256, 0, st>>>(s.x, m.H, w.w[LW_MLP_NORM], m.eps, m.inv_H, nullptr, n, s.a_hi,
+                                                 s.a_lo);
     ck(cudaGetLastError());
     const Seg gu[2] = {{&lm[WM_GATE], m.I, 0, nullptr}, {&lm[WM_UP], m.I, m.I, nullptr}};
     ck(gemm(m, ah_H, al_H, gu, 2, n, m.H, s.gu, 2 * m.I, 0, st));
@@ -748,10 +820,11 @@ int prefill_run(const PrefillModel& m, PrefillState& s, const int32_t* tokens_ho
     ck(gemm(m, ah_I, al_I, down, 1, n, m.I, s.x, m.H, 1, st));
   }
   if (ok && mode != PL_NONE) {
-    // final norm of every row (or of the last one, into row 0), then the tied LM head
-    const int rows = mode == PL_ALL ? n : 1;
-    norm_split_kernel<<<std::min(rows, 4096), 256, 0, st>>>(s.x, m.H, m.final_norm, m.eps, m.inv_H, n - rows, rows,
-                                                            s.a_hi, s.a_lo);
+    // final norm of every row (or of the last token of each sequence, into rows 0 .., n_seq - 1),
+    // then the tied LM head
+    const int rows = mode == PL_ALL ? n : batch.n_seq;
+    norm_split_kernel<<<std::min(rows, 4096), 256, 0, st>>>(s.x, m.H, m.final_norm, m.eps, m.inv_H,
+                                                            mode == PL_ALL ? nullptr : s.rows, rows, s.a_hi, s.a_lo);
     ck(cudaGetLastError());
     const Seg lmh[1] = {{&s.wmaps[(size_t)m.L * WM_PER_LAYER], m.V, 0, nullptr}};
     ck(gemm(m, ah_H, al_H, lmh, 1, rows, m.H, logits, m.V, 0, st));

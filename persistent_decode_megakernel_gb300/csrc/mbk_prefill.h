@@ -48,20 +48,39 @@ struct PrefillState {
   uint16_t* a_hi = nullptr;     // [cap][max(H, qd, I)] GEMM input, bf16 high part
   uint16_t* a_lo = nullptr;     // ... and the bf16 remainder
   int32_t* tokens = nullptr;    // [cap]
+  int32_t* pos = nullptr;       // [cap] position of each token
+  int32_t* seq = nullptr;       // [cap] its sequence
+  int32_t* rows = nullptr;      // [cap] the last token of each sequence (logits of the last tokens)
+  int2* tiles = nullptr;        // [cap] attention tiles: (first token, tokens) of one sequence
+  int32_t* tables = nullptr;    // page tables of a batch of sequences (grown on demand)
+  size_t tables_cap = 0;        // int32 entries allocated there
   std::vector<CUtensorMap> wmaps;  // per layer Wq, Wk, Wv, Wo, Wgate, Wup, Wdown; then E
   bool smem_set = false;
+};
+
+// The tokens of one call: n_seq sequences, sequence s contributing counts[s] consecutive tokens at
+// positions starts[s] .. starts[s] + counts[s] - 1; the token array holds them grouped by sequence,
+// in sequence order.  tables: HOST [n_seq][max_pages] page tables of a paged pool, or null to address
+// the cache as the model does (one sequence: contiguous, or the handle's own page table).
+struct PrefillBatch {
+  int n_seq = 1;
+  const int32_t* counts = nullptr;
+  const int32_t* starts = nullptr;
+  const int32_t* tables = nullptr;
+  int max_pages = 0;
 };
 
 // Logits the caller asks for (values of the C ABI's MBK_PREFILL_LOGITS_*).
 enum PrefillLogits { PL_NONE = 0, PL_LAST = 1, PL_ALL = 2 };
 
-// Runs the prefill on `stream` (asynchronous after the token copy).  tokens_host: n ids, already
-// validated by the caller; positions p0 .. p0 + n - 1 lie inside the cache.  logits: device fp32,
-// [n][V] (PL_ALL), [V] (PL_LAST) or unused (PL_NONE).  Returns an MBK_* code.
-// inject (diagnostics; may be null): device fp32 [L][n][H]; block l >= 1 replaces the residual stream
-// entering layer l.
-int prefill_run(const PrefillModel& m, PrefillState& st, const int32_t* tokens_host, int n, int p0, float* logits,
-                int mode, cudaStream_t stream, const float* inject = nullptr);
+// Runs the tokens of `batch` on `stream` (asynchronous after the host-to-device copies).  tokens_host:
+// n = sum of counts ids, grouped by sequence; everything already validated by the caller (positions
+// inside each sequence's cache, page tables inside the pool, no page shared between sequences).
+// logits: device fp32, [n][V] (PL_ALL), [n_seq][V] (PL_LAST: the last token of each sequence) or
+// unused (PL_NONE).  Returns an MBK_* code.  inject (diagnostics; may be null): device fp32 [L][n][H];
+// block l >= 1 replaces the residual stream entering layer l.
+int prefill_run(const PrefillModel& m, PrefillState& st, const int32_t* tokens_host, int n, const PrefillBatch& batch,
+                float* logits, int mode, cudaStream_t stream, const float* inject = nullptr);
 
 // Frees the workspace (the tensor maps are host memory).
 void prefill_free(PrefillState& st);

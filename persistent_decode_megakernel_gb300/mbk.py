@@ -29,7 +29,7 @@ EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fil
             "mbk_error_string", "mbk_destroy", "mbk_plan_check", "mbk_debug_taps", "mbk_debug_plan",
             "mbk_trace_enable", "mbk_trace_read", "mbk_debug_inject", "mbk_decode_step_static", "mbk_decode_steps",
             "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8", "mbk_prefill",
-            "mbk_debug_prefill_inject", "mbk_plan_simulate")
+            "mbk_debug_prefill_inject", "mbk_plan_simulate", "mbk_batch_step")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
 
 
@@ -102,6 +102,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mbk_prefill.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         lib.mbk_prefill.restype = ctypes.c_int
         lib.mbk_debug_prefill_inject.argtypes = [vp, vp, i32]
+        lib.mbk_batch_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp]
+        lib.mbk_batch_step.restype = ctypes.c_int
         lib.mbk_debug_prefill_inject.restype = ctypes.c_int
         lib.mbk_create_paged.argtypes = [ctypes.POINTER(MbkConfig), ctypes.POINTER(MbkWeights), vp, i32, i32, ctypes.c_int,
                                          ctypes.POINTER(vp)]
@@ -199,6 +201,20 @@ def mbk_prefill(h, tokens, position: int, logits_ptr: int, logits_mode: int, str
     arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     return load_library().mbk_prefill(h, arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), int(position),
                                       ctypes.c_void_p(logits_ptr or None), int(logits_mode), ctypes.c_void_p(stream_ptr))
+
+
+def mbk_batch_step(h, counts, starts, tokens, page_tables, logits_ptr: int, logits_mode: int, stream_ptr: int) -> int:
+    """counts, starts: one entry per sequence; tokens: sum(counts) ids grouped by sequence; page_tables:
+    [n_seq][max_pages] pool pages (all copied into host int32 arrays here)."""
+    import numpy as np
+    c = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
+    s = np.ascontiguousarray(np.asarray(starts, dtype=np.int32))
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    p = np.ascontiguousarray(np.asarray(page_tables, dtype=np.int32))
+    vp = ctypes.c_void_p
+    return load_library().mbk_batch_step(h, int(c.size), c.ctypes.data_as(vp), s.ctypes.data_as(vp),
+                                         t.ctypes.data_as(vp), p.ctypes.data_as(vp), vp(logits_ptr or None),
+                                         int(logits_mode), vp(stream_ptr))
 
 
 def mbk_debug_prefill_inject(h, x_in, n_tokens: int) -> int:
@@ -423,6 +439,22 @@ class Decoder:
         stream = self.torch.cuda.current_stream(self.device).cuda_stream
         _check(mbk_prefill(self.handle, tokens, pos0, out.data_ptr() if out is not None else 0, mode, stream),
                "mbk_prefill")
+        return out
+
+    def batch_step(self, chunks, page_tables, logits: str = "last", out=None):
+        """One step over several sequences of a paged decoder (mbk_batch_step): chunks = [(start,
+        [tokens...]), ...], one per sequence; page_tables [n_seq][max_pages].  logits "last" ->
+        [n_seq, vocab], "all" -> [sum of tokens, vocab], None -> no logits."""
+        counts = [len(t) for _, t in chunks]
+        starts = [p for p, _ in chunks]
+        tokens = [x for _, t in chunks for x in t]
+        mode = PREFILL_LOGITS[logits]
+        if out is None and mode:
+            rows = len(chunks) if mode == 1 else len(tokens)
+            out = self.torch.empty((rows, self.shape.vocab), dtype=self.torch.float32, device=self.device)
+        stream = self.torch.cuda.current_stream(self.device).cuda_stream
+        _check(mbk_batch_step(self.handle, counts, starts, tokens, page_tables, out.data_ptr() if out is not None else 0,
+                              mode, stream), "mbk_batch_step")
         return out
 
     def status(self) -> int:

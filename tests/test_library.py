@@ -154,6 +154,9 @@ def test_prefill_entry_points_reject_a_null_handle_before_touching_a_gpu(lib):
     assert lib.mbk_prefill(None, toks, 2, 0, None, 0, None) == mbk.MBK_ERR_INVALID_ARG
     assert lib.mbk_prefill(None, None, 0, 0, None, 1, None) == mbk.MBK_ERR_INVALID_ARG
     assert lib.mbk_debug_prefill_inject(None, None, 0) == mbk.MBK_ERR_INVALID_ARG
+    one = (ctypes.c_int32 * 1)(1)
+    assert lib.mbk_batch_step(None, 1, one, one, one, one, None, 0, None) == mbk.MBK_ERR_INVALID_ARG
+    assert mbk.mbk_batch_step(None, [1], [0], [5], [[0]], 0, 0, 0) == mbk.MBK_ERR_INVALID_ARG
     # the Python wrapper marshals a token sequence and the logits modes
     assert mbk.mbk_prefill(None, [1, 2, 3], 0, 0, mbk.PREFILL_LOGITS["last"], 0) == mbk.MBK_ERR_INVALID_ARG
     assert set(mbk.PREFILL_LOGITS.values()) == {0, 1, 2}
