@@ -216,3 +216,27 @@ def test_simulate_rejects_bad_arguments(lib):
     assert mbk.mbk_plan_simulate(cfg, 0, 0)[0] == mbk.MBK_ERR_INVALID_ARG
     assert mbk.mbk_plan_simulate(cfg, 152, cfg.kv_capacity)[0] == mbk.MBK_ERR_INVALID_ARG
     assert lib.mbk_plan_simulate(None, 152, 0, None) == mbk.MBK_ERR_INVALID_ARG
+
+
+EDGE_SHAPES = {
+    "mha128": workloads.DecoderShape("mha128", 2, 512, 1024, 4, 4, 128, 2048, 64, 1e-5, 1e4, False, steps=12),
+    "mqa16": workloads.DecoderShape("mqa16", 2, 1024, 2048, 16, 1, 64, 2048, 96, 1e-5, 1e4, False, steps=12),
+    "gqa128": workloads.DecoderShape("gqa128", 2, 1024, 2048, 8, 2, 128, 2048, 96, 1e-5, 1e4, False, steps=12),
+    "ragged-split": workloads.scaled_down(workloads.SHAPES["smollm-135m-long"], n_layers=2, kv_capacity=1500,
+                                          prefill=1494, pos0=1494, steps=6, vocab=8192),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE_SHAPES))
+@pytest.mark.parametrize("fuse", ["-1", "0"])
+@pytest.mark.parametrize("fp8", [0, 1])
+def test_edge_shapes_run_to_completion_in_the_wait_model(lib, monkeypatch, name, fuse, fp8):
+    """The GPU tests' edge shapes (MQA with 16 query heads per KV head, head_dim 128 as MHA and GQA, a
+    ragged last context split), with either O-projection schedule and either weight format."""
+    monkeypatch.setenv("MBK_FUSE_ATTENTION", fuse)
+    s = EDGE_SHAPES[name]
+    cfg = mbk.config_from_shape(s, weight_format=fp8)
+    for pos in sorted({0, s.kv_capacity // 2, s.kv_capacity - 1, min(1024, s.kv_capacity - 1)}):
+        rc, sim = mbk.mbk_plan_simulate(cfg, 152, pos)
+        assert rc == mbk.MBK_OK and sim.tasks_run == sim.tasks_total, (name, pos, sim.stuck_task_type)
+        assert sim.exchange_depth in (4 * s.n_layers + 1, 5 * s.n_layers + 1)
