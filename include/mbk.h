@@ -41,11 +41,15 @@
  * on one stream (or on streams ordered by the caller); two steps of one handle must never run
  * concurrently.  Different handles are independent.
  *
+ * Beside the decode step, mbk_prefill runs a prompt's tokens as dense contractions on the tensor
+ * cores (tcgen05) and mbk_batch_step runs several sequences of a paged pool in one step through the
+ * same kernels; both are compiled but have not yet been run on a GPU.
+ *
  * Errors: every function returning int returns MBK_OK (0) or a negative MBK_ERR_* code.  Host
  * checks run before any launch and leave device state unchanged.  A device-side failure (a wait
  * that ran out of time) is recorded in a device status word; it is returned by the next
- * decode or mbk_kv_fill call on the handle and by mbk_get_status, and is sticky until
- * mbk_destroy.
+ * decode, prefill, batch or mbk_kv_fill call on the handle and by mbk_get_status, and is sticky
+ * until mbk_destroy.
  */
 #ifndef MBK_H
 #define MBK_H
