@@ -306,11 +306,14 @@ int mbk_debug_prefill_inject(mbk_handle *h, const float *x_in, int32_t n_tokens)
  * in global task order to the HOST buffer `out` and returns the number of tasks (or a negative code). */
 int64_t mbk_debug_plan(mbk_handle *h, int32_t *out, int64_t capacity);
 
-/* Per-task timing: when enabled, every later step records for each task four globaltimer stamps
- * (ns): {begin, inputs ready, end, first weight stage ready (0 if none)}.  Enabling allocates a
- * device buffer of 32 bytes per task; disabling frees it.  mbk_trace_read copies the stamps of the
- * most recently completed traced step (synchronise first) into the HOST buffer `out`
- * (4 uint64 per task, global task order) and returns the number of tasks (or a negative code). */
+/* Per-task timing: when enabled, every later step records for each task eight globaltimer stamps
+ * (ns): {begin, inputs ready, end, first weight stage ready (0 if none), then four phase marks of the
+ * task, 0 where unused}.  Attention tasks mark: 4 the query rotation and the K/V rows staged, 5 the
+ * (position block, head) items done, 6 the output merged (before the fused O rows).
+ * Enabling allocates a device buffer of 64 bytes per task; disabling frees it.  mbk_trace_read
+ * copies the stamps of the most recently completed traced step (synchronise first) into the HOST
+ * buffer `out` (8 uint64 per task, global task order) and returns the number of tasks (or a
+ * negative code). */
 int mbk_trace_enable(mbk_handle *h, int enable);
 int64_t mbk_trace_read(mbk_handle *h, uint64_t *out, int64_t capacity_tasks);
 

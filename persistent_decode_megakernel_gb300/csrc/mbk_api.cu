@@ -768,7 +768,7 @@ int mbk_trace_enable(mbk_handle* h, int enable) {
   if (!h) return MBK_ERR_INVALID_ARG;
   if (cudaSetDevice(h->device) != cudaSuccess) return MBK_ERR_CUDA;
   if (enable && !h->d_trace) {
-    size_t bytes = sizeof(unsigned long long) * 4 * std::max<size_t>(1, h->plan.tasks.size());
+    size_t bytes = sizeof(unsigned long long) * kTraceStamps * std::max<size_t>(1, h->plan.tasks.size());
     if (cudaMalloc(&h->d_trace, bytes) != cudaSuccess) return MBK_ERR_NOMEM;
     if (cudaMemset(h->d_trace, 0, bytes) != cudaSuccess) return MBK_ERR_CUDA;
   } else if (!enable && h->d_trace) {
@@ -784,7 +784,7 @@ int64_t mbk_trace_read(mbk_handle* h, uint64_t* out, int64_t capacity_tasks) {
   if (!h || !out || !h->d_trace) return MBK_ERR_INVALID_ARG;
   int64_t n = std::min<int64_t>(capacity_tasks, (int64_t)h->plan.tasks.size());
   if (cudaSetDevice(h->device) != cudaSuccess ||
-      cudaMemcpy(out, h->d_trace, sizeof(uint64_t) * 4 * n, cudaMemcpyDeviceToHost) != cudaSuccess)
+      cudaMemcpy(out, h->d_trace, sizeof(uint64_t) * kTraceStamps * n, cudaMemcpyDeviceToHost) != cudaSuccess)
     return MBK_ERR_CUDA;
   return (int64_t)h->plan.tasks.size();
 }

@@ -166,7 +166,7 @@ struct Ctx {
 };
 
 __device__ __forceinline__ void trace_mark(Ctx& c, int k) {
-  if (c.P->trace != nullptr && c.ctid == 0) c.P->trace[(size_t)c.task_index * 4 + k] = global_ns();
+  if (c.P->trace != nullptr && c.ctid == 0) c.P->trace[(size_t)c.task_index * kTraceStamps + k] = global_ns();
 }
 __device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile unsigned*)&c.ctl->abort != 0u; }
 __device__ __forceinline__ void put_word(Ctx& c, unsigned long long* p, float v) {
@@ -215,22 +215,24 @@ __device__ __forceinline__ const unsigned long long* word_addr(const InVec& v, i
   return e < v.n1 ? v.src + e : (e < v.n1 + v.n2 ? v.src2 + (e - v.n1) : v.src3 + (e - v.n1 - v.n2));
 }
 
-// Every thread polls its elements ctid + k*kCT four at a time; all loads of a group are in flight
-// together and every retry re-loads all words still pending, so a late group costs one round trip
-// per retry, not one per word.  The gains are loaded with the words and used only after the group
-// arrived, so their latency hides behind the wait.  Values are consumed in element order whatever
-// their arrival order, which keeps the sum of squares deterministic.  After a failed wait the
-// remaining words read as 0.
-__device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detail) {
+// Threads tid = 0..nth-1 poll elements tid + k*nth, kPollWords at a time; all loads of a group are in
+// flight together and every retry re-loads all words still pending, so a late group costs one round
+// trip per retry, not one per word (the hidden and intermediate vectors of the decoder shapes fit one
+// group).  The gains are loaded with the words and used only after the group arrived, so their
+// latency hides behind the wait.  Values are consumed in element order whatever their arrival order,
+// which keeps the sum of squares deterministic.  After a failed wait the remaining words read as 0.
+constexpr int kPollWords = 8;
+__device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detail, int tid = -1, int nth = kCT) {
+  if (tid < 0) tid = c.ctid;
   float ss = 0.f;
 #pragma unroll 1
-  for (int e0 = c.ctid; e0 < v.n; e0 += 4 * kCT) {
-    unsigned long long w[4];
-    uint32_t graw[4];
+  for (int e0 = tid; e0 < v.n; e0 += kPollWords * nth) {
+    unsigned long long w[kPollWords];
+    uint32_t graw[kPollWords];
     unsigned pend = 0u;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int e = e0 + k * kCT;
+    for (int k = 0; k < kPollWords; ++k) {
+      const int e = e0 + k * nth;
       w[k] = 0ull;
       graw[k] = 0x3f80u;  // bf16 1.0
       if (e < v.n) {
@@ -247,25 +249,25 @@ __device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detai
     unsigned long long t0 = 0ull;
     while (pend != 0u) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+      for (int k = 0; k < kPollWords; ++k)
         if (((pend >> k) & 1u) && (unsigned)(w[k] >> 32) == c.tag) pend &= ~(1u << k);
       if (pend == 0u) break;
       if ((++spins & 31u) == 0u && (t0 = wait_check(c.P, c.ctl, t0, c.task_index, detail | (unsigned)e0)) == 0ull) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < kPollWords; ++k)
           if ((pend >> k) & 1u) w[k] = 0ull;
         break;
       }
       if (c.P->poll_backoff_ns) __nanosleep(c.P->poll_backoff_ns);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int e = e0 + k * kCT;
+      for (int k = 0; k < kPollWords; ++k) {
+        const int e = e0 + k * nth;
         if ((pend >> k) & 1u) w[k] = ld_word(word_addr(v, e));
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int e = e0 + k * kCT;
+    for (int k = 0; k < kPollWords; ++k) {
+      const int e = e0 + k * nth;
       if (e < v.n) {
         float x = __uint_as_float((uint32_t)w[k]);
         if (v.gain != nullptr) {
@@ -282,18 +284,19 @@ __device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detai
 // poll_vec for vectors that are sums: element e = base word (or embedding value) + the nterm
 // partial words of e, two elements per thread at a time with every word of both in flight together.
 // The sum is taken in a fixed order (base, then heads in order), so it is deterministic.
-__device__ __forceinline__ float poll_sum(Ctx& c, const InVec& v, unsigned detail) {
+__device__ __forceinline__ float poll_sum(Ctx& c, const InVec& v, unsigned detail, int tid = -1, int nth = kCT) {
+  if (tid < 0) tid = c.ctid;
   constexpr int T = 1 + kMaxFusedKvHeads;
   const int nt = 1 + v.nterm;
   float ss = 0.f;
 #pragma unroll 1
-  for (int e0 = c.ctid; e0 < v.n; e0 += 2 * kCT) {
+  for (int e0 = tid; e0 < v.n; e0 += 2 * nth) {
     unsigned long long w[2][T];
     uint32_t graw[2];
     unsigned pend = 0u;  // bit k * T + t
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int e = e0 + k * kCT;
+      const int e = e0 + k * nth;
       graw[k] = 0x3f80u;
 #pragma unroll
       for (int t = 0; t < T; ++t) w[k][t] = 0ull;
@@ -333,7 +336,7 @@ __device__ __forceinline__ float poll_sum(Ctx& c, const InVec& v, unsigned detai
       if (c.P->poll_backoff_ns) __nanosleep(c.P->poll_backoff_ns);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int e = e0 + k * kCT;
+        const int e = e0 + k * nth;
         if ((pend >> (k * T)) & 1u) w[k][0] = ld_word(v.src + e);
 #pragma unroll
         for (int t = 1; t < T; ++t)
@@ -342,7 +345,7 @@ __device__ __forceinline__ float poll_sum(Ctx& c, const InVec& v, unsigned detai
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int e = e0 + k * kCT;
+      const int e = e0 + k * nth;
       if (e < v.n) {
         float x = __uint_as_float((uint32_t)w[k][0]);
 #pragma unroll
@@ -816,6 +819,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
 #pragma unroll 1
   for (int st = 0; st < nst; ++st) stage_wait(c, (unsigned)st);
   compute_sync();
+  trace_mark(c, 4);
   const int rshift = 31 - __clz(R);
   const unsigned ns = c.ns;
   auto krow = [&](int j) -> const uint16_t* {
@@ -908,6 +912,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   }
   stages_release(c, (unsigned)nst);
   compute_sync();
+  trace_mark(c, 5);
 
   const int istride = g * (d + 4);  // items of one head are g apart
   if (wo) {
@@ -948,6 +953,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
         for (int j = 0; j < 8; ++j) ov[k][j] *= inv;
       }
     }
+    trace_mark(c, 6);
     const size_t row_bytes = (size_t)O * (F8 ? 1 : 2);
     unsigned long long* out = P.words + t.out_off;
     // FP8: the scales of Wo's rows (one per full row, shared by every KV head's segment)
@@ -1203,15 +1209,22 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
   if (one_batch) b0 = batch_wait(c, (int)t.nchunks);
   // 2. inputs: the vector, then (O, down) the residual rows -- one polling loop for both
   float ss = 0.f;
-  if (combine) combine_splits(c, l, sv, res);
-#pragma unroll 1
-  for (int j = combine ? 1 : 0; j < 2; ++j) {
-    InVec v = x;
-    if (j == 1) v = r;
-    if (v.n > 0) {
-      const unsigned detail = j == 0 ? 0x100000u : 0x400000u;
-      const float s = v.nterm > 0 ? poll_sum(c, v, detail) : poll_vec(c, v, detail);
-      if (j == 0) ss = s;
+  if (combine) {
+    combine_splits(c, l, sv, res);
+    if (r.n > 0) {
+      if (r.nterm > 0) poll_sum(c, r, 0x400000u);
+      else poll_vec(c, r, 0x400000u);
+    }
+  } else {
+    // one pass for both vectors: with residual rows (O, down) the last warp polls them while the
+    // other warps poll the input vector, so neither waits behind the other's round trips
+    const int nx = r.n > 0 ? kCT - 32 : kCT;
+    if (c.ctid < nx) {
+      ss = x.nterm > 0 ? poll_sum(c, x, 0x100000u, c.ctid, nx) : poll_vec(c, x, 0x100000u, c.ctid, nx);
+    } else if (r.nterm > 0) {
+      poll_sum(c, r, 0x400000u, c.ctid - nx, 32);
+    } else {
+      poll_vec(c, r, 0x400000u, c.ctid - nx, 32);
     }
   }
   if (type == T_QKV) {
@@ -1559,7 +1572,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const Task t = tasks[k % kTaskWindow];
     c.task_index = ti;
     c.first_stage = true;
-    if (P.trace != nullptr && c.ctid == 0) P.trace[(size_t)ti * 4 + 3] = 0;
+    if (P.trace != nullptr && c.ctid == 0)
+      for (int k = 3; k < kTraceStamps; ++k) P.trace[(size_t)ti * kTraceStamps + k] = 0;
     trace_mark(c, 0);
     if (t.type == T_ATTN)
       task_attn<kF8>(c, t, sv, res);

@@ -119,6 +119,9 @@ constexpr int kMaxLayers = 64;
 constexpr int kTaskWindow = 160;      // task records staged in shared memory at a time
 constexpr int kMaxFusedKvHeads = 4;   // the O projection is fused into attention for at most this many KV heads
 constexpr int kMaxFusedGroupWidth = 512;  // ... and query-head groups of at most this many elements (g * head_dim)
+// Trace stamps per task: begin, inputs ready, end, first weight stage, then up to four phase marks of
+// the task (0 where a task type has fewer phases).
+constexpr int kTraceStamps = 8;
 
 struct PlanShape {
   int L, H, I, nq, nkv, d, V, C;

@@ -231,11 +231,10 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   p.act_words = (uint64_t)a.per_layer * s.L;
 
   // shared memory layout: [barriers + flags 1 KB][input vector][results][residuals][ring]
-  const int O = g * s.d;
   // attention: rotated queries, current K/V (raw, then the bf16 row appended) and the partial
   // output (o, m, l) of every (32-position block, query head) item of a split
   const int attn_items = (p.split_len + 31) / 32 * g;
-  int attn_floats = O + 3 * s.d + attn_items * (s.d + 4);
+  const int attn_floats = g * s.d + 3 * s.d + attn_items * (s.d + 4);
   p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
   p.sv_floats = (p.sv_floats + 31) / 32 * 32;
 

@@ -31,6 +31,7 @@ EXPORTED = ("mbk_create", "mbk_decode_step", "mbk_decode_step_host", "mbk_kv_fil
             "mbk_decode_greedy", "mbk_create_paged", "mbk_set_page_table", "mbk_quantize_fp8", "mbk_prefill",
             "mbk_debug_prefill_inject", "mbk_plan_simulate", "mbk_batch_step")
 TASK_TYPES = {1: "qkv", 2: "attn", 3: "oproj", 4: "gateup", 5: "down", 6: "lmhead"}
+TRACE_STAMPS = 8  # per task: begin, inputs ready, end, first weight stage, four phase marks
 
 
 class MbkError(RuntimeError):
@@ -319,7 +320,7 @@ def mbk_trace_read(h):
     import numpy as np
     lib = load_library()
     n = lib.mbk_debug_plan(h, None, 0)
-    out = np.zeros((n, 4), dtype=np.uint64)
+    out = np.zeros((n, TRACE_STAMPS), dtype=np.uint64)
     r = lib.mbk_trace_read(h, out.ctypes.data, n)
     if r < 0:
         raise MbkError(int(r), "mbk_trace_read")
