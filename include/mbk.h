@@ -270,8 +270,10 @@ void mbk_destroy(mbk_handle *h);
  *  - All calls on a device share the array, which keeps the last call's contents: the schedule is
  *    rebuilt and uploaded (then the stream is synchronised once) only when the config or any
  *    pointer differs from the previous call; the exchange words and the status word are cleared
- *    on every call.  Calls whose GPU work overlaps (two streams, two threads) race on the array:
- *    order them on one stream.
+ *    on every call.  A call that needs a rebuild must therefore be made outside stream capture:
+ *    inside a capture it returns MBK_ERR_STATE and leaves the capture untouched.  Calls whose GPU
+ *    work overlaps (two streams, two threads) race on the array: order them on one stream.
+ *  - Device-side waits are bounded by MBK_WAIT_TIMEOUT_MS (default 1000), as for a handle.
  *  - Returns MBK_ERR_INVALID_ARG for the same argument errors as mbk_create / mbk_decode_step and
  *    when the shape needs more than MBK_STATIC_SCRATCH_BYTES (nothing is launched then);
  *    MBK_ERR_UNSUPPORTED or MBK_ERR_CUDA as mbk_create.  A device-side wait that times out is not

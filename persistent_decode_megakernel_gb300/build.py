@@ -21,8 +21,8 @@ LIB = os.path.join(PKG, "libmbk.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 CU_SOURCES = ["mbk_kernel.cu", "mbk_api.cu", "mbk_static.cu", "mbk_prefill.cu"]
-CPP_SOURCES = ["mbk_sched.cpp", "mbk_simulate.cpp"]
-HEADERS = ["mbk_plan.h", "mbk_device.h", "mbk_sched.h", "mbk_prefill.h"]
+CPP_SOURCES = ["mbk_sched.cpp", "mbk_simulate.cpp", "mbk_args.cpp"]
+HEADERS = ["mbk_plan.h", "mbk_device.h", "mbk_sched.h", "mbk_prefill.h", "mbk_args.h"]
 
 
 def _cuda_home() -> str:

@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "../../include/mbk.h"
+#include "mbk_args.h"
 #include "mbk_device.h"
 #include "mbk_prefill.h"
 #include "mbk_sched.h"
@@ -73,41 +74,10 @@ struct mbk_handle {
 
 namespace {
 
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
 int lm_task_count(const Plan& p) {
   int n = 0;
   for (const Task& t : p.tasks) n += t.type == T_LMHEAD ? 1 : 0;
   return n;
-}
-
-PlanShape shape_of(const mbk_config& c) {
-  PlanShape s;
-  s.L = c.n_layers;
-  s.H = c.hidden;
-  s.I = c.intermediate;
-  s.nq = c.n_heads;
-  s.nkv = c.n_kv_heads;
-  s.d = c.head_dim;
-  s.V = c.vocab;
-  s.C = c.kv_capacity;
-  s.qkv_bias = c.qkv_bias ? 1 : 0;
-  s.wb = c.weight_format == MBK_WEIGHTS_FP8 ? 1 : 2;
-  return s;
-}
-
-int env_int(const char* name, int dflt) {
-  const char* v = getenv(name);
-  if (!v || !*v) return dflt;
-  return atoi(v);
-}
-
-int config_check(const mbk_config* cfg) {
-  if (!cfg) return MBK_ERR_INVALID_ARG;
-  if (!(cfg->rms_eps >= 0.0) || !(cfg->rope_theta > 0.0) || !std::isfinite(cfg->rope_theta)) return MBK_ERR_INVALID_ARG;
-  if (cfg->weight_format != MBK_WEIGHTS_BF16 && cfg->weight_format != MBK_WEIGHTS_FP8) return MBK_ERR_INVALID_ARG;
-  if (!validate_shape(shape_of(*cfg)).empty()) return MBK_ERR_INVALID_ARG;
-  return MBK_OK;
 }
 
 void free_all(mbk_handle* h) {
@@ -234,29 +204,9 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
                 mbk_handle** out) {
   if (!out) return MBK_ERR_INVALID_ARG;
   *out = nullptr;
-  if (config_check(cfg) != MBK_OK || !weights || !weights->embed || !weights->final_norm || !weights->layers || !kv_cache)
-    return MBK_ERR_INVALID_ARG;
-  const PlanShape s = shape_of(*cfg);
-  // every tensor pointer present and 16-byte aligned
-  if (!aligned16(weights->embed) || !aligned16(weights->final_norm) || !aligned16(kv_cache)) return MBK_ERR_INVALID_ARG;
   WeightAddrs wa;
-  wa.embed = (uint64_t)(uintptr_t)weights->embed;
-  wa.final_norm = (uint64_t)(uintptr_t)weights->final_norm;
-  wa.layers.resize(s.L);
-  for (int l = 0; l < s.L; ++l) {
-    const mbk_layer_weights& lw = weights->layers[l];
-    const void* ptrs[W_NSLOTS] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.bq, lw.bk, lw.bv, lw.wo, lw.mlp_norm, lw.w_gate, lw.w_up, lw.w_down};
-    for (int k = 0; k < W_NSLOTS; ++k) {
-      bool is_bias = (k == W_BQ || k == W_BK || k == W_BV);
-      if (is_bias && !s.qkv_bias) {
-        wa.layers[l][k] = 0;
-        continue;
-      }
-      if (!ptrs[k]) return MBK_ERR_INVALID_ARG;
-      if (!is_bias && k != W_ATTN_NORM && k != W_MLP_NORM && !aligned16(ptrs[k])) return MBK_ERR_INVALID_ARG;
-      wa.layers[l][k] = (uint64_t)(uintptr_t)ptrs[k];
-    }
-  }
+  if (gather_weights(cfg, weights, kv_cache, &wa) != MBK_OK) return MBK_ERR_INVALID_ARG;
+  const PlanShape s = shape_of(*cfg);
 
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MBK_ERR_UNSUPPORTED;

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -17,6 +18,7 @@
 #include <vector>
 
 #include "../../include/mbk.h"
+#include "mbk_args.h"
 #include "mbk_device.h"
 #include "mbk_sched.h"
 
@@ -69,23 +71,13 @@ std::string plan_key(const mbk_config& c, const mbk_weights& w, const void* kv) 
 
 extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* weights, void* kv_cache,
                                       int32_t token_id, int32_t position, float* logits_out, void* stream) {
-  if (!cfg || !weights || !weights->embed || !weights->final_norm || !weights->layers || !kv_cache || !logits_out)
-    return MBK_ERR_INVALID_ARG;
-  if (cfg->n_layers <= 0 || token_id < 0 || token_id >= cfg->vocab || position < 0 || position >= cfg->kv_capacity)
-    return MBK_ERR_INVALID_ARG;
-  PlanShape s;
-  s.L = cfg->n_layers;
-  s.H = cfg->hidden;
-  s.I = cfg->intermediate;
-  s.nq = cfg->n_heads;
-  s.nkv = cfg->n_kv_heads;
-  s.d = cfg->head_dim;
-  s.V = cfg->vocab;
-  s.C = cfg->kv_capacity;
-  s.qkv_bias = cfg->qkv_bias ? 1 : 0;
+  // the same argument checks as mbk_create (config, every weight pointer present and 16-byte
+  // aligned), then the step's own; all of them before any CUDA call
+  WeightAddrs wa;
+  if (!logits_out || gather_weights(cfg, weights, kv_cache, &wa) != MBK_OK) return MBK_ERR_INVALID_ARG;
+  if (token_id < 0 || token_id >= cfg->vocab || position < 0 || position >= cfg->kv_capacity) return MBK_ERR_INVALID_ARG;
   if (cfg->weight_format != MBK_WEIGHTS_BF16) return MBK_ERR_INVALID_ARG;  // this entry streams the bf16 weights
-  if (!validate_shape(s).empty() || !(cfg->rms_eps >= 0.0) || !(cfg->rope_theta > 0.0)) return MBK_ERR_INVALID_ARG;
-  if (((uintptr_t)weights->embed | (uintptr_t)kv_cache) & 15u) return MBK_ERR_INVALID_ARG;
+  const PlanShape s = shape_of(*cfg);
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MBK_ERR_CUDA;
@@ -112,24 +104,11 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
 
   const std::string key = plan_key(*cfg, *weights, kv_cache);
   if (key != D.resident_key) {
+    // a new schedule is uploaded and the stream synchronised once: not possible inside a capture
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MBK_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return MBK_ERR_STATE;
     // build the schedule (host memory) and lay it out in the array
-    WeightAddrs wa;
-    wa.embed = (uint64_t)(uintptr_t)weights->embed;
-    wa.final_norm = (uint64_t)(uintptr_t)weights->final_norm;
-    wa.layers.resize(s.L);
-    for (int l = 0; l < s.L; ++l) {
-      const mbk_layer_weights& lw = weights->layers[l];
-      const void* ptrs[W_NSLOTS] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.bq, lw.bk, lw.bv, lw.wo, lw.mlp_norm, lw.w_gate, lw.w_up, lw.w_down};
-      for (int k = 0; k < W_NSLOTS; ++k) {
-        const bool is_bias = (k == W_BQ || k == W_BK || k == W_BV);
-        if (is_bias && !s.qkv_bias) {
-          wa.layers[l][k] = 0;
-          continue;
-        }
-        if (!ptrs[k]) return MBK_ERR_INVALID_ARG;
-        wa.layers[l][k] = (uint64_t)(uintptr_t)ptrs[k];
-      }
-    }
     PlanOptions opt;
     opt.smem_limit = D.smem_optin;
     Plan plan;
@@ -198,7 +177,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     kp.words = reinterpret_cast<unsigned long long*>(b + o_words);
     kp.status = reinterpret_cast<unsigned*>(b + o_status);
     kp.host_status = nullptr;
-    kp.timeout_ns = 1000000000ull;
+    kp.timeout_ns = (unsigned long long)std::max(1, env_int("MBK_WAIT_TIMEOUT_MS", 1000)) * 1000000ull;
     kp.trace = nullptr;
     kp.inject = nullptr;
     kp.poll_backoff_ns = 0;

@@ -240,3 +240,55 @@ def test_edge_shapes_run_to_completion_in_the_wait_model(lib, monkeypatch, name,
         rc, sim = mbk.mbk_plan_simulate(cfg, 152, pos)
         assert rc == mbk.MBK_OK and sim.tasks_run == sim.tasks_total, (name, pos, sim.stuck_task_type)
         assert sim.exchange_depth in (4 * s.n_layers + 1, 5 * s.n_layers + 1)
+
+
+def _fake_weights(shape, misalign=None):
+    """Weight and cache pointers that are never dereferenced (every case below fails its argument
+    checks before any CUDA call); each tensor 64 KB apart, 16-byte aligned unless `misalign` names a
+    layer field to offset by 8 bytes."""
+    base = [0x7000_0000_0000]
+
+    def nxt():
+        base[0] += 0x10000
+        return base[0]
+
+    layers = (mbk.MbkLayerWeights * shape.n_layers)()
+    for layer in layers:
+        for k in mbk.LAYER_FIELDS:
+            if k in ("bq", "bk", "bv") and not shape.qkv_bias:
+                continue
+            setattr(layer, k, nxt() + (8 if k == misalign else 0))
+    w = mbk.MbkWeights(nxt(), nxt(), layers)
+    w._keep = layers
+    return w, nxt(), nxt()
+
+
+def test_static_step_checks_arguments_like_create_before_touching_a_gpu(lib):
+    """mbk_decode_step_static rejects, before any CUDA call, every argument mbk_create rejects
+    (including a misaligned projection weight and a non-finite RoPE theta) and its own step
+    arguments; the shared check also rejects the misaligned weight through mbk_create."""
+    shape = workloads.SHAPES["tiny"]
+    cfg = mbk.config_from_shape(shape)
+    w, kv, logits = _fake_weights(shape)
+    st = lib.mbk_decode_step_static
+    E = mbk.MBK_ERR_INVALID_ARG
+    assert st(None, ctypes.byref(w), ctypes.c_void_p(kv), 0, 0, ctypes.c_void_p(logits), None) == E
+    assert st(ctypes.byref(cfg), None, ctypes.c_void_p(kv), 0, 0, ctypes.c_void_p(logits), None) == E
+    assert st(ctypes.byref(cfg), ctypes.byref(w), None, 0, 0, ctypes.c_void_p(logits), None) == E
+    assert st(ctypes.byref(cfg), ctypes.byref(w), ctypes.c_void_p(kv), 0, 0, None, None) == E
+    for tok, pos in ((-1, 0), (shape.vocab, 0), (0, -1), (0, shape.kv_capacity)):
+        assert st(ctypes.byref(cfg), ctypes.byref(w), ctypes.c_void_p(kv), tok, pos, ctypes.c_void_p(logits), None) == E
+    fp8 = mbk.config_from_shape(shape)
+    fp8.weight_format = mbk.MBK_WEIGHTS_FP8
+    assert st(ctypes.byref(fp8), ctypes.byref(w), ctypes.c_void_p(kv), 0, 0, ctypes.c_void_p(logits), None) == E
+    bad = mbk.config_from_shape(shape)
+    bad.rope_theta = float("inf")
+    assert st(ctypes.byref(bad), ctypes.byref(w), ctypes.c_void_p(kv), 0, 0, ctypes.c_void_p(logits), None) == E
+    for field in ("wq", "wo", "w_down"):
+        wm, kvm, lm = _fake_weights(shape, misalign=field)
+        assert st(ctypes.byref(cfg), ctypes.byref(wm), ctypes.c_void_p(kvm), 0, 0, ctypes.c_void_p(lm), None) == E
+        h = ctypes.c_void_p()
+        assert lib.mbk_create(ctypes.byref(cfg), ctypes.byref(wm), ctypes.c_void_p(kvm), 0, ctypes.byref(h)) == E
+        assert not h.value
+    wk, kvk, lk = _fake_weights(shape)
+    assert st(ctypes.byref(cfg), ctypes.byref(wk), ctypes.c_void_p(kvk + 8), 0, 0, ctypes.c_void_p(lk), None) == E
