@@ -53,6 +53,20 @@ def algorithmic_bytes(shape, positions, fp8: bool = False) -> float:
     return fixed + kv
 
 
+def steps_per_call(steps: int, positions: int) -> int:
+    """Largest power of two dividing both the requested steps and the workload's positions that still
+    leaves at least 5 timed launches (1 when none does)."""
+    best, spc = 1, 1
+    while spc <= positions:
+        if positions % spc == 0 and steps % spc == 0 and steps // spc >= 5:
+            best = spc
+        spc *= 2
+    return best
+
+
+NOMINAL_HBM_GBS = 8000.0  # HBM3e nominal, GB300
+
+
 def load_peaks():
     p = os.path.join(_ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -198,8 +212,9 @@ def run_ours(args, shape_name):
     fp8 = getattr(args, "weights", "bf16") == "fp8"
     dec = mbk.Decoder(wl, device=local, fp8=fp8)
     stream = torch.cuda.current_stream()
-    # one call decodes `spc` consecutive teacher-forced positions (mbk_decode_steps; 1 = mbk_decode_step)
-    spc = args.steps_per_call if args.steps_per_call > 0 else s.steps
+    # one call decodes `spc` consecutive teacher-forced positions (mbk_decode_steps; 1 = mbk_decode_step):
+    # exactly --steps steps are timed, in at least 5 launches when --steps allows it
+    spc = args.steps_per_call if args.steps_per_call > 0 else steps_per_call(args.steps, s.steps)
     if s.steps % spc:
         raise SystemExit(f"--steps-per-call must divide the workload's {s.steps} positions")
     steps = (args.steps + spc - 1) // spc * spc
@@ -315,6 +330,7 @@ def run_ours(args, shape_name):
         cpu = {"value": round(ctps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{cn} teacher-forced decode steps of the same workload (time-bounded to {budget:.0f} s)"}
     traffic = profiled_traffic(shape_name) if not fp8 else None
+    others = measure_others(shape_name, fp8, local, peak) if (rank == 0 and not args.no_others) else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s", "n_gpus": world, "steps": steps,
@@ -329,10 +345,14 @@ def run_ours(args, shape_name):
                        "single_step_tokens_per_s": round(single_tps, 2) if single_tps else None,
                        "greedy_tokens_per_s": round(greedy_tps, 2) if greedy_tps else None,
                        "per_step_time_over_launches": spread,
+                       "e2e_path": "mbk_decode_step_host (C ABI, host logits) per step" if spc == 1 else
+                                   "mbk_decode_steps per launch, then the launch's logits copied to pinned host memory",
+                       "others": others,
                        "vs_baseline_note": "pages' H200 MIG 60-SM number, context only",
                        "weights": "fp8 (E4M3, per-row fp32 scales, quantized by the library)" if fp8 else "bf16"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                         "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                          "algorithmic_bytes_per_step": round(algo), "kernel_avg_us_per_step": round(kernel_avg_ms * 1e3, 3),
                          "per": "decode step (a launch of n steps moves n times the bytes in n times the time)",
                          "kernel": "mbk::decode_kernel"},
@@ -347,6 +367,47 @@ def run_ours(args, shape_name):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_others(main: str, fp8: bool, device: int, peak: float):
+    """The other decoder shapes, a few launches each (one launch = the workload's teacher-forced
+    positions): tokens/s, roofline fraction of the measured and of the nominal HBM peak."""
+    import torch
+
+    from persistent_decode_megakernel_gb300 import mbk, workloads
+    out = []
+    for name in ("tiny", "smollm-135m", "qwen2-0.5b", "smollm-135m-long", "smollm-1.7b"):
+        if name == main:
+            continue
+        wl = workloads.generate(name, seed=0)
+        s = wl.shape
+        dec = mbk.Decoder(wl, device=device, fp8=fp8)
+        toks = [int(t) for t in wl.tokens[:s.steps]]
+        logits = torch.empty((s.steps, s.vocab), dtype=torch.float32, device=dec.device)
+        for _ in range(2):
+            dec.steps(toks, s.pos0, logits)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+        for a, b in ev:
+            a.record(stream)
+            dec.steps(toks, s.pos0, logits)
+            b.record(stream)
+        torch.cuda.synchronize()
+        assert dec.status() == 0, f"device-side wait timed out ({name})"
+        per_step = sorted(a.elapsed_time(b) * 1e-3 / s.steps for a, b in ev)
+        med = per_step[len(per_step) // 2]
+        algo = algorithmic_bytes(s, [s.pos0 + i for i in range(s.steps)], fp8)
+        ach = algo / med / 1e9
+        fits_l2 = algo < 100e6  # the tiny decoder's working set stays in the 129 MB L2
+        out.append({"workload": name, "tokens_per_s": round(1.0 / med, 1), "us_per_step_median": round(med * 1e6, 2),
+                    "launches": len(ev), "steps_per_launch": s.steps, "algorithmic_bytes_per_step": round(algo),
+                    "achieved_gbs": round(ach, 1), "frac": None if fits_l2 else round(ach / peak, 4),
+                    "frac_of_nominal_8tbs": None if fits_l2 else round(ach / NOMINAL_HBM_GBS, 4),
+                    "note": "fits in L2: no HBM roofline" if fits_l2 else None})
+        dec.close()
+        del dec, logits, wl
+    return out
 
 
 def profiled_traffic(shape_name: str):
@@ -376,11 +437,12 @@ def _kernel_hash() -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=8192)
+    ap.add_argument("--steps", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="smollm-135m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the other decoder shapes' lines in config.others")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
                     help="fp8: stream the library's FP8 (E4M3, per-row scale) copies of the weights")
     ap.add_argument("--steps-per-call", type=int, default=0,

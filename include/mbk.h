@@ -311,7 +311,9 @@ int64_t mbk_debug_plan(mbk_handle *h, int32_t *out, int64_t capacity);
 /* Per-task timing: when enabled, every later step records for each task eight globaltimer stamps
  * (ns): {begin, inputs ready, end, first weight stage ready (0 if none), then four phase marks of the
  * task, 0 where unused}.  Attention tasks mark: 4 the query rotation and the K/V rows staged, 5 the
- * (position block, head) items done, 6 the output merged (before the fused O rows).
+ * (position block, head) items done, 6 the output merged (before the fused O rows).  Projection
+ * tasks put the SM clock count (clock64) at their end in slot 7, so that a trace also shows the
+ * clock the step ran at.
  * Enabling allocates a device buffer of 64 bytes per task; disabling frees it.  mbk_trace_read
  * copies the stamps of the most recently completed traced step (synchronise first) into the HOST
  * buffer `out` (8 uint64 per task, global task order) and returns the number of tasks (or a

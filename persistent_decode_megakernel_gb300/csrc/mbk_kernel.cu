@@ -1581,6 +1581,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       task_gemv<kF8>(c, t, sv, res, add);
     compute_sync();  // the next task reuses the shared vectors
     trace_mark(c, 2);
+    // tracing: the SM clock count at the end of a projection task (slot 7; attention tasks use it
+    // for a phase mark), so a trace also gives the clock the tasks ran at
+    if (P.trace != nullptr && c.ctid == 0 && t.type != T_ATTN) P.trace[(size_t)ti * kTraceStamps + 7] = clock64();
   }
   // this CTA is done with the step: publish it (with the cache rows its tasks appended) to the
   // producers that copy those rows in the next step

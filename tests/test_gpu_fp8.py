@@ -55,6 +55,7 @@ def test_fp8_parity(name, steps):
     wl = workloads.generate(name, seed=0)
     rep = run_parity(wl, steps=steps, mode="sync", fp8=True)
     print(f"\n{name} fp8 sync: {rep}")
+    print(rep.json_line().replace('"mode": "sync"', '"mode": "sync-fp8"'))
     rep.check()
 
 

@@ -24,13 +24,29 @@ def _built():
 CONFIGS = ["tiny", "smollm-135m", "qwen2-0.5b", "smollm-135m-long", "smollm-1.7b"]
 
 
+_SYNC_ARGMAX = {}  # config -> (steps agreeing, steps) of the sync runs in this session
+
+
 @pytest.mark.parametrize("name", CONFIGS)
 def test_full_config_parity(name):
     """Every step of the config's teacher-forced stream, each step from the oracle's state."""
     wl = workloads.generate(name, seed=0)
     rep = run_parity(wl, mode="sync")
     print(f"\n{name} sync: {rep}")
+    print(rep.json_line())
+    _SYNC_ARGMAX[name] = (round(rep.argmax_agree * rep.steps), rep.steps)
     rep.check()
+
+
+def test_argmax_agrees_on_99_percent_of_the_five_streams():
+    """The greedy argmax of the five decoder streams (416 teacher-forced steps) agrees on >= 99% of
+    steps; each disagreement was already checked to be a near tie of the oracle."""
+    if len(_SYNC_ARGMAX) < len(CONFIGS):
+        pytest.skip("needs the five sync runs of this module")
+    agree = sum(a for a, _ in _SYNC_ARGMAX.values())
+    steps = sum(n for _, n in _SYNC_ARGMAX.values())
+    print(f"\nPARITY_JSON {{\"pooled_argmax_agree\": {agree / steps}, \"steps\": {steps}}}")
+    assert agree / steps >= 0.99
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -40,6 +56,7 @@ def test_kv_rows_region_by_region(name):
     wl = workloads.generate(name, seed=0)
     rep = run_parity(wl, mode="layers")
     print(f"\n{name} layers: {rep}")
+    print(rep.json_line())
     rep.check()
 
 
@@ -49,6 +66,7 @@ def test_full_config_free_running(name):
     wl = workloads.generate(name, seed=0)
     rep = run_parity(wl, mode="free")
     print(f"\n{name} free: {rep}")
+    print(rep.json_line())
     rep.check()
 
 
