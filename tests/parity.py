@@ -237,8 +237,24 @@ class ParityReport:
 
 
 def _rows_to_gpu(dec, orc_kv: np.ndarray, rows: slice) -> None:
+    """Oracle cache rows `rows` into the GPU cache (through the page table of a paged decoder)."""
     src = torch.from_numpy(np.ascontiguousarray(orc_kv[:, :, :, rows]).view(np.int16)).view(torch.bfloat16)
-    dec.kv[:, :, :, rows] = src.to(dec.device)
+    if dec.paged is None:
+        dec.kv[:, :, :, rows] = src.to(dec.device)
+        return
+    ps = dec.paged[1]
+    a = rows.start
+    while a < rows.stop:  # one copy per run of positions inside a page
+        b = min(rows.stop, (a // ps + 1) * ps)
+        page = dec.pages[a // ps]
+        dec.pool[page, :, :, :, a % ps:a % ps + (b - a)] = src[:, :, :, a - rows.start:b - rows.start].to(dec.device)
+        a = b
+
+
+def _row_from_gpu(dec, pos: int) -> np.ndarray:
+    """GPU cache row `pos` of every layer as bf16 bit patterns [L][2][nkv][d]."""
+    row = dec.kv[:, :, :, pos] if dec.paged is None else dec.pool[dec.pages[pos // dec.paged[1]], :, :, :, pos % dec.paged[1]]
+    return row.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
 def _step_stats(got: np.ndarray, ref: np.ndarray, i: int, rels, maxs, dis, decisive) -> int:
@@ -256,20 +272,22 @@ def _step_stats(got: np.ndarray, ref: np.ndarray, i: int, rels, maxs, dis, decis
     return 1
 
 
-def run_parity(wl, device: int = 0, steps: int | None = None, mode: str = "sync", fp8: bool = False) -> ParityReport:
-    """Run `steps` teacher-forced steps of `wl` on both sides in `mode` ("sync", "layers" or "free")."""
+def run_parity(wl, device: int = 0, steps: int | None = None, mode: str = "sync", fp8: bool = False,
+               paged=None) -> ParityReport:
+    """Run `steps` teacher-forced steps of `wl` on both sides in `mode` ("sync", "layers" or "free").
+    paged: None (contiguous cache) or (num_pages, page_size, table) for a paged GPU cache."""
     from oracle import OracleDecoder
     from persistent_decode_megakernel_gb300 import mbk
     from persistent_decode_megakernel_gb300.mbk import Decoder
 
     s = wl.shape
     n = s.steps if steps is None else steps
-    dec = Decoder(wl, device=device, fp8=fp8)  # fp8: both sides on the FP8 copies of the weights
+    dec = Decoder(wl, device=device, fp8=fp8, paged=paged)  # fp8: both sides on the FP8 copies
     orc = OracleDecoder(wl, fp8=fp8)
     prefill = KvCompare(0, 0, 0, 0.0, 0.0)
     if s.prefill:
         torch.cuda.synchronize()
-        prefill = kv_compare(dec.kv, orc.kv, slice(0, s.prefill), prefill_allowance(wl))
+        prefill = kv_compare(dec.logical_kv(), orc.kv, slice(0, s.prefill), prefill_allowance(wl))
         if mode in ("sync", "layers"):
             _rows_to_gpu(dec, orc.kv, slice(0, s.prefill))
     rels: List[float] = []
@@ -294,7 +312,7 @@ def run_parity(wl, device: int = 0, steps: int | None = None, mode: str = "sync"
             t0 = time.perf_counter()
             got = dec.step(tok, pos).cpu().numpy().astype(np.float64)
             t_gpu += time.perf_counter() - t0
-            g_rows = dec.kv[:, :, :, pos].view(torch.int16).cpu().numpy().view(np.uint16)
+            g_rows = _row_from_gpu(dec, pos)
             gtaps = None
             if mode == "sync":
                 gtaps = mbk.mbk_debug_taps(dec.handle, s.n_layers, s.hidden)
@@ -326,6 +344,6 @@ def run_parity(wl, device: int = 0, steps: int | None = None, mode: str = "sync"
             agree += _step_stats(got[i], ref, i, rels, maxs, dis, decisive)
         t_orc = time.perf_counter() - t0
         # each side's own cache: reported, not asserted (rounding choices compound across steps)
-        kv = kv_compare(dec.kv, orc.kv, slice(s.pos0, s.pos0 + n))
+        kv = kv_compare(dec.logical_kv(), orc.kv, slice(s.pos0, s.pos0 + n))
     dec.close()
     return ParityReport(n, max(rels), max(maxs), agree / n, kv, prefill, t_gpu, t_orc, mode, dis, s.name, decisive[0], decisive[1])

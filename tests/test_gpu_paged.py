@@ -87,3 +87,18 @@ def test_paged_cache_rejects_bad_tables_and_unmapped_positions():
     assert mbk.mbk_set_page_table(c.handle, [0], stream) == mbk.MBK_ERR_INVALID_ARG
     c.close()
     d.close()
+
+
+@pytest.mark.parametrize("shape,page", [("smollm-135m", 32), ("smollm-135m-long", 64)])
+def test_paged_cache_against_the_oracle(shape, page):
+    """A decoder on a shuffled page table against the CPU oracle, every step from the oracle's state
+    (sync mode, the bars of the contiguous parity tests): logits, argmax and every new cache row."""
+    from parity import run_parity
+    wl = workloads.generate(shape, seed=0)
+    s = wl.shape
+    n_logical = (s.kv_capacity + page - 1) // page
+    table = _table(n_logical, n_logical + 5, seed=13)
+    rep = run_parity(wl, mode="sync", paged=(n_logical + 5, page, table))
+    print(f"\n{shape} paged sync: {rep}")
+    print(rep.json_line().replace('"mode": "sync"', '"mode": "sync-paged"'))
+    rep.check()
