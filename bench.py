@@ -331,6 +331,7 @@ def run_ours(args, shape_name):
                "sample": f"{cn} teacher-forced decode steps of the same workload (time-bounded to {budget:.0f} s)"}
     traffic = profiled_traffic(shape_name) if not fp8 else None
     others = measure_others(shape_name, fp8, local, peak) if (rank == 0 and not args.no_others) else None
+    prefill = measure_prefill(local) if (rank == 0 and not args.no_others and not fp8) else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s", "n_gpus": world, "steps": steps,
@@ -348,6 +349,7 @@ def run_ours(args, shape_name):
                        "e2e_path": "mbk_decode_step_host (C ABI, host logits) per step" if spc == 1 else
                                    "mbk_decode_steps per launch, then the launch's logits copied to pinned host memory",
                        "others": others,
+                       "prefill": prefill,
                        "vs_baseline_note": "pages' H200 MIG 60-SM number, context only",
                        "weights": "fp8 (E4M3, per-row fp32 scales, quantized by the library)" if fp8 else "bf16"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -410,6 +412,55 @@ def measure_others(main: str, fp8: bool, device: int, peak: float):
     return out
 
 
+def load_tensor_peak():
+    p = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    return 1900.0, "fallback (burst)"
+
+
+def measure_prefill(device: int, n: int = 4096):
+    """A prompt of n tokens through mbk_prefill on the 135M shape with an 8,192-row cache (the long-
+    context shape's cache, positions 0..n-1), last-row logits: time, tokens/s, and the algorithmic work
+    against the bf16 tensor peak.  Work = 2 x the projection MACs of every token (the LM head for the
+    last token only) + the causal attention's 4 nq d (t + 1) flops per token and layer; the tensor cores
+    execute the projections twice (the bf16 high/low pair of each input), counted as overhead."""
+    import torch
+
+    from persistent_decode_megakernel_gb300 import mbk, workloads
+    wl = workloads.generate("smollm-135m-long", seed=0)
+    s = wl.shape
+    g = torch.Generator().manual_seed(1)
+    toks = [int(t) for t in torch.randint(0, s.vocab, (n,), generator=g)]
+    dec = mbk.Decoder(wl, device=device)
+    out = torch.empty(s.vocab, dtype=torch.float32, device=dec.device)
+    dec.prefill(toks, 0, logits="last", out=out)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+    for a, b in ev:
+        a.record(stream)
+        dec.prefill(toks, 0, logits="last", out=out)
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert dec.status() == 0, "device-side wait timed out in the prefill"
+    dec.close()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)[1]
+    H, I, d = s.hidden, s.intermediate, s.head_dim
+    proj = s.n_layers * (H * s.n_heads * d + 2 * H * s.n_kv_heads * d + s.n_heads * d * H + 3 * H * I)
+    gemm = 2.0 * proj * n + 2.0 * s.vocab * H
+    attn = 4.0 * s.n_heads * d * s.n_layers * n * (n + 1) / 2
+    peak, kind = load_tensor_peak()
+    tf = (gemm + attn) / (ms * 1e-3) / 1e12
+    return {"workload": f"prefill of {n} tokens, SmolLM-135M shape, last-row logits", "ms_median_of_3": round(ms, 3),
+            "tokens_per_s": round(n / (ms * 1e-3), 1), "gemm_tflop": round(gemm / 1e12, 3),
+            "attention_tflop": round(attn / 1e12, 3), "achieved_tflops": round(tf, 2),
+            "peak_tflops": peak, "peak_kind": kind, "frac": round(tf / peak, 4),
+            "note": "tensor cores run the projections twice (bf16 high/low input pair): overhead, not work; "
+                    "the causal attention runs on CUDA cores"}
+
+
 def profiled_traffic(shape_name: str):
     """DRAM bytes per launch from the committed ncu summary of this workload, or None when the
     summary is missing or was taken on different kernel sources."""
@@ -442,7 +493,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="smollm-135m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-others", action="store_true", help="skip the other decoder shapes' lines in config.others")
+    ap.add_argument("--no-others", action="store_true", help="skip config.others (the other decoder shapes) and config.prefill")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
                     help="fp8: stream the library's FP8 (E4M3, per-row scale) copies of the weights")
     ap.add_argument("--steps-per-call", type=int, default=0,
