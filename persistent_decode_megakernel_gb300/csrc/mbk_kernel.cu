@@ -211,6 +211,20 @@ struct InVec {
   const unsigned long long* terms;
   int nterm, tstride;
 };
+// Where element e of a polled vector lands: in order (xlayout 0), in the split GEMV layout (1), or
+// (2, an attention task's queries | K | V, n1 = g * d query elements, n2 = d) with every query head in
+// a row of d + d/8 floats in which each run of 32 elements sits 16 bytes after the previous one
+// (attn_qpos), the K and V rows after the heads.
+__device__ __forceinline__ int attn_qpos(int i) { return i + ((i >> 5) << 2); }  // i < d: element of one head
+__device__ __forceinline__ int dst_index(const InVec& v, int e) {
+  if (v.xlayout == 1) return xpos(e, v.n);
+  if (v.xlayout == 2) {
+    const int dsh = 31 - __clz(v.n2);
+    if (e < v.n1) return (e >> dsh) * (v.n2 + (v.n2 >> 3)) + attn_qpos(e & (v.n2 - 1));
+    return v.n1 + (v.n1 >> 3) + (e - v.n1);
+  }
+  return e;
+}
 __device__ __forceinline__ const unsigned long long* word_addr(const InVec& v, int e) {
   return e < v.n1 ? v.src + e : (e < v.n1 + v.n2 ? v.src2 + (e - v.n1) : v.src3 + (e - v.n1 - v.n2));
 }
@@ -274,7 +288,7 @@ __device__ __forceinline__ float poll_vec(Ctx& c, const InVec& v, unsigned detai
           ss = fmaf(x, x, ss);
           x *= __uint_as_float(graw[k] << 16);
         }
-        v.dst[v.xlayout ? xpos(e, v.n) : e] = x;
+        v.dst[dst_index(v, e)] = x;
       }
     }
   }
@@ -751,11 +765,15 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   const int nblk = (np + 31) >> 5;            // 32-position blocks
   const int items = nblk * g;
 
-  float* sq = sv;                             // [g][d]  queries (rotated in place)
-  float* kc = sq + O;                         // [d]     current K (raw)
+  const int QS = d + (d >> 3);                // floats per query head (attn_qpos: each run of 32 elements
+                                              // 16 bytes after the previous one, so that lane-rotated
+                                              // 16-byte chunk reads of a head touch distinct banks)
+  float* sq = sv;                             // [g][QS]  queries (rotated in place)
+  float* kc = sq + g * QS;                    // [d]     current K (raw)
   float* vc = kc + d;                         // [d]     current V (raw)
   uint16_t* cur = reinterpret_cast<uint16_t*>(vc + d);  // [2][d] bf16: the rotated K, V row appended
   float* pw = vc + 2 * d;                     // [items][d + 4]  per-item o, m, l (16-byte aligned items)
+  float* pbw = pw + items * (d + 4) + c.warp * 32;  // [warp][32]  this warp's item probabilities
   const float2* cs = c.ctl->rope;             // this step's cos/sin (loaded at kernel start)
 
   // 1. the packed queries and (owner) the current K/V row, in one poll: they land in sq|kc|vc
@@ -772,7 +790,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
     v.emb = nullptr;
     v.gain = nullptr;
     v.dst = sq;
-    v.xlayout = 0;
+    v.xlayout = 2;
     v.terms = nullptr;
     v.nterm = 0;
     v.tstride = 0;
@@ -785,10 +803,11 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   for (int e = c.ctid; e < g * half; e += kCT) {
     const int h = e >> hshift, i = e & (half - 1);
     const float2 r = cs[i];
-    float* q = sq + (h << dshift);
-    const float x0 = q[i], x1 = q[i + half];
-    q[i] = x0 * r.x - x1 * r.y;
-    q[i + half] = x1 * r.x + x0 * r.y;
+    float* q = sq + h * QS;
+    const int i0 = attn_qpos(i), i1 = attn_qpos(i + half);
+    const float x0 = q[i0], x1 = q[i1];
+    q[i0] = x0 * r.x - x1 * r.y;
+    q[i1] = x1 * r.x + x0 * r.y;
   }
   if (owner && c.ctid >= kCT - half) {
     const int i = c.ctid - (kCT - half);
@@ -845,13 +864,14 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
     float s = -INFINITY;
     if (valid) {
       const uint4* kr = reinterpret_cast<const uint4*>(krow(j));
-      const float4* qh = reinterpret_cast<const float4*>(sq + (h << dshift));
+      const float4* qh = reinterpret_cast<const float4*>(sq + h * QS);
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll 4
       for (int k = 0; k < nchunk; ++k) {
         const int cch = (k + c.lane) & (nchunk - 1);
         const uint4 kw = kr[cch];
-        const float4 q0 = qh[2 * cch], q1 = qh[2 * cch + 1];
+        const int qc = 2 * cch + (cch >> 2);  // the chunk's first float4 (attn_qpos)
+        const float4 q0 = qh[qc], q1 = qh[qc + 1];
         s0 = fmaf(bf16_lo(kw.x), q0.x, s0);
         s1 = fmaf(bf16_hi(kw.x), q0.y, s1);
         s2 = fmaf(bf16_lo(kw.y), q0.z, s2);
@@ -866,16 +886,50 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
     const float m = warp_max(s);
     const float p = valid ? exp2f(s - m) : 0.f;
     const float lsum = warp_sum(p);
-    // the block's output: lane owns element pairs 2*lane (+64); position jj's weight comes from lane
-    // jj.  A block's cached rows are consecutive rows of one stage (32 divides R); the appended
-    // row, if the block holds it, comes last.
+    // the block's output: lane owns element pairs 2*lane (+64); the 32 positions' weights go through
+    // the warp's buffer and come back four at a time as broadcast loads (fewer shared-memory and
+    // shuffle operations than one shuffle per position).  A block's cached rows are consecutive rows
+    // of one stage (32 divides R); the appended row, if the block holds it, comes last.
+    pbw[c.lane] = p;
+    __syncwarp();
     const int ncache = max(0, min(nj, nh - j0b));
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
     if (ncache > 0) {
       const uint16_t* vb = vrow(j0b) + 2 * c.lane;
-#pragma unroll 8
-      for (int jj = 0; jj < ncache; ++jj) {
-        const float pj = __shfl_sync(0xffffffffu, p, jj);
+      const float4* pb4 = reinterpret_cast<const float4*>(pbw);
+      int jj = 0;
+#pragma unroll 2
+      for (; jj + 4 <= ncache; jj += 4) {
+        const float4 p4 = pb4[jj >> 2];
+        const uint32_t v0 = *reinterpret_cast<const uint32_t*>(vb + jj * d);
+        const uint32_t v1 = *reinterpret_cast<const uint32_t*>(vb + (jj + 1) * d);
+        const uint32_t v2 = *reinterpret_cast<const uint32_t*>(vb + (jj + 2) * d);
+        const uint32_t v3 = *reinterpret_cast<const uint32_t*>(vb + (jj + 3) * d);
+        a0 = fmaf(p4.x, bf16_lo(v0), a0);
+        a1 = fmaf(p4.x, bf16_hi(v0), a1);
+        b0 = fmaf(p4.y, bf16_lo(v1), b0);
+        b1 = fmaf(p4.y, bf16_hi(v1), b1);
+        a0 = fmaf(p4.z, bf16_lo(v2), a0);
+        a1 = fmaf(p4.z, bf16_hi(v2), a1);
+        b0 = fmaf(p4.w, bf16_lo(v3), b0);
+        b1 = fmaf(p4.w, bf16_hi(v3), b1);
+        if (d > 64) {
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vb + jj * d + 64);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + (jj + 1) * d + 64);
+          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vb + (jj + 2) * d + 64);
+          const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vb + (jj + 3) * d + 64);
+          a2 = fmaf(p4.x, bf16_lo(w0), a2);
+          a3 = fmaf(p4.x, bf16_hi(w0), a3);
+          b2 = fmaf(p4.y, bf16_lo(w1), b2);
+          b3 = fmaf(p4.y, bf16_hi(w1), b3);
+          a2 = fmaf(p4.z, bf16_lo(w2), a2);
+          a3 = fmaf(p4.z, bf16_hi(w2), a3);
+          b2 = fmaf(p4.w, bf16_lo(w3), b2);
+          b3 = fmaf(p4.w, bf16_hi(w3), b3);
+        }
+      }
+      for (; jj < ncache; ++jj) {
+        const float pj = pbw[jj];
         const uint32_t v01 = *reinterpret_cast<const uint32_t*>(vb + jj * d);
         a0 = fmaf(pj, bf16_lo(v01), a0);
         a1 = fmaf(pj, bf16_hi(v01), a1);
@@ -886,8 +940,12 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
         }
       }
     }
+    a0 += b0;
+    a1 += b1;
+    a2 += b2;
+    a3 += b3;
     if (nj > ncache) {  // the appended row
-      const float pj = __shfl_sync(0xffffffffu, p, ncache);
+      const float pj = pbw[ncache];
       const uint16_t* vr = cur + d + 2 * c.lane;
       const uint32_t v01 = *reinterpret_cast<const uint32_t*>(vr);
       a0 = fmaf(pj, bf16_lo(v01), a0);
@@ -909,6 +967,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
       pi[d] = m;
       pi[d + 1] = lsum;
     }
+    __syncwarp();  // every lane has read the warp's weights before the next item writes them
   }
   stages_release(c, (unsigned)nst);
   compute_sync();

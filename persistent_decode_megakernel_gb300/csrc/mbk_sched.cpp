@@ -231,10 +231,11 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   p.act_words = (uint64_t)a.per_layer * s.L;
 
   // shared memory layout: [barriers + flags 1 KB][input vector][results][residuals][ring]
-  // attention: rotated queries, current K/V (raw, then the bf16 row appended) and the partial
-  // output (o, m, l) of every (32-position block, query head) item of a split
+  // attention: rotated queries (d + d/8 floats a head), current K/V (raw, then the bf16 row appended),
+  // the partial output (o, m, l) of every (32-position block, query head) item of a split, and each
+  // compute warp's 32 item weights
   const int attn_items = (p.split_len + 31) / 32 * g;
-  const int attn_floats = g * s.d + 3 * s.d + attn_items * (s.d + 4);
+  const int attn_floats = g * (s.d + s.d / 8) + 3 * s.d + attn_items * (s.d + 4) + kComputeWarps * 32;
   p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
   p.sv_floats = (p.sv_floats + 31) / 32 * 32;
 
