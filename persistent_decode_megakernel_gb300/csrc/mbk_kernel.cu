@@ -376,46 +376,6 @@ __device__ __forceinline__ float poll_sum(Ctx& c, const InVec& v, unsigned detai
   return ss;
 }
 
-// Polls a set of up to K words of this thread: word k (k < K, valid(k)) at addr(k); sink(k, value)
-// runs once per valid word, k static.  Used by the split combine of long contexts.
-template <int K, typename V, typename A, typename F>
-__device__ __forceinline__ void poll_set(Ctx& c, unsigned detail, V&& valid, A&& addr, F&& sink) {
-  unsigned long long w[K];
-  unsigned pend = 0u;
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    w[k] = 0ull;
-    if (valid(k)) {
-      w[k] = ld_word(addr(k));
-      pend |= 1u << k;
-    }
-  }
-  unsigned spins = 0u;
-  unsigned long long t0 = 0ull;
-  for (;;) {
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      if ((pend >> k) & 1u) {
-        if ((unsigned)(w[k] >> 32) == c.tag) {
-          pend &= ~(1u << k);
-          sink(k, __uint_as_float((unsigned)w[k]));
-        }
-      }
-    }
-    if (pend == 0u) return;
-    if ((++spins & 31u) == 0u && (t0 = wait_check(c.P, c.ctl, t0, c.task_index, detail)) == 0ull) {
-#pragma unroll
-      for (int k = 0; k < K; ++k)
-        if ((pend >> k) & 1u) sink(k, 0.f);
-      return;
-    }
-    if (c.P->poll_backoff_ns) __nanosleep(c.P->poll_backoff_ns);
-#pragma unroll
-    for (int k = 0; k < K; ++k)
-      if ((pend >> k) & 1u) w[k] = ld_word(addr(k));
-  }
-}
-
 // ------------------------------------------------------------------ weight ring (consumer side)
 // Keeps testing a ring stage whose first test failed; records a failure after the timeout.
 __device__ __noinline__ void spin_stage(uint64_t* full, unsigned parity, const KernelParams* P, Ctl* ctl, unsigned task,
@@ -1088,54 +1048,48 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
 
 // Attention output of every query head into o[nq*d] (split GEMV layout) when the context has
 // several splits: the active splits of each head are combined by their log-sum-exp weights
-// (split-context "flash decoding", README "Current status").  `ml` is scratch for
-// splits * nq * 2 floats.  Contains one block barrier; none after the last step.
-__device__ __forceinline__ void combine_splits(Ctx& c, int l, float* o, float* ml) {
+// (split-context "flash decoding", README "Current status").  One poll brings every active split's o
+// words and (m, l) words into `scratch` (nsplit * (nq*d + nq*2) floats) -- threads tid of nth take
+// part, up to eight words each in flight -- and, after the block barrier, each output is the
+// weighted mean of the splits' normalised outputs, weights l_s 2^(m_s - max m), summed in split order.
+// The caller's other threads may poll other words meanwhile; every compute thread reaches the barrier.
+__device__ __forceinline__ void combine_splits(Ctx& c, int l, float* o, float* scratch, int tid, int nth) {
   const KernelParams& P = *c.P;
   const int d = P.d, nqd = P.nq * d, dshift = 31 - __clz(d);
   const int nact = c.pos / P.split_len + 1;
-  const unsigned long long* ob = layer_words(P, l) + P.act.att;  // o words [split][head][d]
-  // (m, l) of every active split and head: a prefix of the [split][head][2] words
-  {
+  const unsigned long long* ob = layer_words(P, l) + P.act.att;  // o words [split][head][d], then (m, l)
+  const int no = nact * nqd;              // o words of the active splits (a prefix of [split][head][d])
+  if (tid >= 0) {
     InVec v;
-    v.src = ob + (size_t)P.nsplit * nqd;
+    v.src = ob;
+    v.src2 = ob + (size_t)P.nsplit * nqd;  // (m, l) of the active splits: a prefix of [split][head][2]
+    v.src3 = nullptr;
+    v.n1 = no;
+    v.n2 = nact * P.nq * 2;
+    v.n = v.n1 + v.n2;
     v.emb = nullptr;
     v.gain = nullptr;
-    v.dst = ml;
-    v.n = nact * P.nq * 2;
+    v.dst = scratch;
     v.xlayout = 0;
-    v.src2 = v.src3 = nullptr;
-    v.n1 = v.n;
-    v.n2 = 0;
     v.terms = nullptr;
     v.nterm = 0;
     v.tstride = 0;
-    poll_vec(c, v, 0x310000u);
+    poll_vec(c, v, 0x310000u, tid, nth);
   }
   compute_sync();
-  // each output: the weighted mean of the splits' normalised outputs, weights l_s 2^(m_s - max m),
-  // summed in split order
+  const float* ml = scratch + no;
 #pragma unroll 1
   for (int e = c.ctid; e < nqd; e += kCT) {
     const int h = e >> dshift;
     float M = -INFINITY;
     for (int s = 0; s < nact; ++s) M = fmaxf(M, ml[(s * P.nq + h) * 2]);
     float num = 0.f, den = 0.f;
-#pragma unroll 1
-    for (int s0 = 0; s0 < nact; s0 += 4) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      poll_set<4>(
-          c, 0x340000u | (unsigned)s0, [&](int k) { return s0 + k < nact; },
-          [&](int k) { return ob + (size_t)(s0 + k) * nqd + e; }, [&](int k, float x) { v[k] = x; });
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (s0 + k < nact) {
-          const float* m = ml + ((s0 + k) * P.nq + h) * 2;
-          const float wgt = m[1] * exp2f(m[0] - M);
-          num = fmaf(wgt, v[k], num);
-          den += wgt;
-        }
-      }
+#pragma unroll 4
+    for (int s = 0; s < nact; ++s) {
+      const float* m = ml + (s * P.nq + h) * 2;
+      const float wgt = m[1] * exp2f(m[0] - M);
+      num = fmaf(wgt, scratch[s * nqd + e], num);
+      den += wgt;
     }
     o[xpos(e, nqd)] = num / den;
   }
@@ -1269,11 +1223,14 @@ __device__ __forceinline__ void task_gemv(Ctx& c, const Task& t, float* sv, floa
   // 2. inputs: the vector, then (O, down) the residual rows -- one polling loop for both
   float ss = 0.f;
   if (combine) {
-    combine_splits(c, l, sv, res);
-    if (r.n > 0) {
-      if (r.nterm > 0) poll_sum(c, r, 0x400000u);
-      else poll_vec(c, r, 0x400000u);
+    // the splits' words and (O projection) the residual rows in one pass: the last warp polls the
+    // residual rows while the others poll the splits
+    const int nsp = r.n > 0 ? kCT - 32 : kCT;
+    if (c.ctid >= nsp) {
+      if (r.nterm > 0) poll_sum(c, r, 0x400000u, c.ctid - nsp, 32);
+      else poll_vec(c, r, 0x400000u, c.ctid - nsp, 32);
     }
+    combine_splits(c, l, sv, sv + P.nq * P.d, c.ctid < nsp ? c.ctid : -1, nsp);
   } else {
     // one pass for both vectors: with residual rows (O, down) the last warp polls them while the
     // other warps poll the input vector, so neither waits behind the other's round trips

@@ -237,6 +237,9 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   const int attn_items = (p.split_len + 31) / 32 * g;
   const int attn_floats = g * (s.d + s.d / 8) + 3 * s.d + attn_items * (s.d + 4) + kComputeWarps * 32;
   p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
+  // the O projection of a split context combines the splits from the o and (m, l) words of every
+  // active split, polled into the vector area after the combined output
+  if (p.nsplit > 1) p.sv_floats = std::max(p.sv_floats, qd + p.nsplit * (qd + 2 * s.nq));
   p.sv_floats = (p.sv_floats + 31) / 32 * 32;
 
   // tasks
