@@ -334,6 +334,8 @@ typedef struct {
   int64_t max_cta_bytes;   /* largest per-CTA share of those bytes */
   int64_t act_words;       /* 8-byte activation exchange words per step */
   int smem_bytes;          /* dynamic shared memory per CTA */
+  int combine_group;       /* splits whose outputs one poll of the split combine brings (<= attn_splits) */
+  int attn_mma;            /* 1: attention runs on the tensor cores (head_dim 64, <= 8 query heads per KV head) */
 } mbk_plan_info;
 
 /* Builds the schedule for `cfg` as if on a GPU with `num_sms` SMs, checks it (every weight row

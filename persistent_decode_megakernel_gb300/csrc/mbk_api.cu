@@ -68,6 +68,7 @@ struct mbk_handle {
   unsigned long long* d_trace = nullptr;
   unsigned long long* d_inject = nullptr;
   bool inject_armed = false;
+  CUtensorMap kvmap{};  // the KV cache as swizzled tiles (tensor-core attention; unused otherwise)
   int last_token = 0;
   int sticky = MBK_OK;
 };
@@ -137,6 +138,7 @@ int mbk_plan_check(const mbk_config* cfg, int num_sms, mbk_plan_info* info) {
   PlanOptions opt;
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
   opt.fuse_attention = env_int("MBK_FUSE_ATTENTION", -1);
+  opt.attn_mma = env_int("MBK_ATTN_MMA", 1);
   std::string err = build_plan(s, w, num_sms, opt, &p);
   if (!err.empty()) return MBK_ERR_STATE;
   info->num_ctas = p.num_ctas;
@@ -149,6 +151,8 @@ int mbk_plan_check(const mbk_config* cfg, int num_sms, mbk_plan_info* info) {
   info->max_cta_bytes = p.max_cta_bytes;
   info->act_words = (int64_t)p.act_words;
   info->smem_bytes = p.smem_bytes;
+  info->combine_group = p.combine_group;
+  info->attn_mma = p.attn_mma ? 1 : 0;
   return MBK_OK;
 }
 
@@ -278,6 +282,7 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   opt.smem_limit = smem_optin;
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
   opt.fuse_attention = env_int("MBK_FUSE_ATTENTION", -1);
+  opt.attn_mma = env_int("MBK_ATTN_MMA", 1);
   std::string err = build_plan(s, wa, prop.multiProcessorCount, opt, &h->plan);
   if (!err.empty()) {
     free_all(h);
@@ -380,6 +385,7 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   kp.act = p.act;
   kp.nsplit = p.nsplit;
   kp.split_len = p.split_len;
+  kp.combine_group = p.combine_group;
   kp.rows_per_stage = p.attn_rows_per_stage;
   kp.num_stages = p.num_stages;
   kp.off_sv = p.off_sv;
@@ -403,6 +409,11 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   kp.page_shift = 0;
   while (h->paged && (1 << kp.page_shift) < h->page_size) ++kp.page_shift;
   kp.page_elems = h->paged ? (unsigned long long)s.L * 2 * s.nkv * h->page_size * s.d : 0ull;
+  // tensor-core attention: the whole cache (or pool) as rows of 64 bf16; the CUDA-core path if the
+  // map cannot be made
+  kp.attn_box_rows = std::min(kp.page_size, 64);
+  const uint64_t kv_rows = h->paged ? (uint64_t)h->num_pages * (kp.page_elems / 64) : (uint64_t)s.L * 2 * s.nkv * s.C;
+  kp.attn_mma = p.attn_mma && make_kv_tile_map(&h->kvmap, kv_cache, kv_rows, (uint32_t)kp.attn_box_rows) ? 1 : 0;
   kp.wbytes = s.wb;
   kp.wscale_layer = wscale_layer;
   kp.wscale = h->d_wscale;
@@ -446,7 +457,7 @@ int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, i
     kp.inject = h->d_inject;  // one step only
     h->inject_armed = false;
   }
-  void* args[] = {&kp, &sp};
+  void* args[] = {&kp, &sp, &h->kvmap};
   cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(sp.greedy != 0, h->kp.wbytes == 1), dim3(h->grid),
                                               dim3(kThreads), args,
                                               (size_t)h->plan.smem_bytes, (cudaStream_t)stream);

@@ -27,6 +27,7 @@ struct KernelParams {
   const uint32_t* chunk_off;    // [grid + 1]
   ActLayout act;
   int nsplit, split_len, rows_per_stage, num_stages;
+  int combine_group;            // split combine: splits whose o words one poll brings (<= nsplit)
   uint32_t off_sv, off_res, off_resid, off_tasks, off_ring;
   // tensors
   const uint16_t* embed;
@@ -49,6 +50,11 @@ struct KernelParams {
   const int32_t* page_table;
   int page_size, page_shift;
   unsigned long long page_elems;  // bf16 elements of one page: L * 2 * nkv * page_size * d
+  // Attention on the tensor cores (head_dim 64, at most 8 query heads per KV head): the producer
+  // copies K/V stages as 2-D tiles of attn_box_rows rows (min(64, page_size)) through the tensor map
+  // passed beside these parameters -- the whole cache (or page pool) as rows of 64 bf16, 128-byte
+  // swizzle.  0: rows are bulk-copied and the attention runs on the CUDA cores.
+  int attn_mma, attn_box_rows;
   // Streamed projection weights: bf16 (wbytes 2, wscale null) or FP8 E4M3 copies (wbytes 1) with one
   // fp32 scale per output row: per layer [q|k|v rows][Wo rows][gate rows][up rows][Wd rows]
   // (wscale_layer floats), then the LM head's V rows.

@@ -20,6 +20,7 @@
 // descriptors) are issued before a task waits for its inputs and consumed after.
 // Every wait is bounded by a globaltimer budget; on expiry the CTA records timeout status and
 // finishes its task list without waiting or writing, so the launch always terminates.
+#include <cuda.h>  // CUtensorMap (the type only)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -68,6 +69,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+// 2-D TMA tile copy global -> shared memory (box and 128-byte swizzle from the tensor map), completing
+// on mbarrier `bar`; x is the innermost coordinate (elements), y the row.
+__device__ __forceinline__ void tile_load(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+          smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -163,6 +173,7 @@ struct Ctx {
   int warp, lane;       // compute warp 0..kComputeWarps-1
   unsigned task_index;
   bool first_stage;     // tracing: the task has not yet received a weight stage
+  bool mma;             // attention on the tensor cores: K/V stages arrive as 128-byte-swizzled tiles
 };
 
 __device__ __forceinline__ void trace_mark(Ctx& c, int k) {
@@ -694,6 +705,182 @@ __device__ __forceinline__ float res_row(const float* res, int i, int gpr) {
   return v;
 }
 
+// ------------------------------------------------------------------ attention on the tensor cores
+// Head dimension 64, at most 8 query heads per KV head.  The producer brings each stage's K rows
+// (64 of them, 128 bytes each) and then its V rows as 2-D TMA tiles with the 128-byte swizzle: the
+// 16-byte chunk c of row r sits at chunk c ^ (r & 7), so the 8 rows a fragment load touches fall in
+// different banks.  Both products run transposed on mma.sync m16n8k16 (bf16 operands, fp32
+// accumulation), so that the 16-row side of the tile holds positions or dimensions and the 8-column
+// side the (at most 8) query heads:
+//   S^T = K Q^T   A = 16 K rows (ldmatrix), B = the queries, rows = positions, cols = heads;
+//   O^T += V^T P^T  A = V rows loaded transposed (ldmatrix.trans), rows = 16 of the 64 dimensions;
+//                   B = the probabilities: S^T's accumulator fragments as bf16, transposed 8x8 in
+//                   registers (movmatrix).
+// fp32 operands reach the bf16 MMAs as high/low pairs (x = hi + lo, hi = bf16(x), lo = bf16(x - hi)):
+// two MMAs per product, with the relative error of the pair (about 2^-17) instead of bf16's 2^-9.
+// K and V are bf16 in the cache, so they go in exactly.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const float h0 = __bfloat162float(__float2bfloat16_rn(x0)), h1 = __bfloat162float(__float2bfloat16_rn(x1));
+  hi = bf16x2(h0, h1);
+  lo = bf16x2(x0 - h0, x1 - h1);
+}
+// D += A B for one m16n8k16 tile
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+constexpr int kMmaRows = kStageBytes / (2 * 64 * 2);  // K (then V) rows of one stage at head_dim 64
+// byte offset of 16-byte chunk `ch` of row r inside a swizzled tile of 128-byte rows (1024-byte aligned)
+__device__ __forceinline__ uint32_t swz128(int r, int ch) { return (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) << 4); }
+
+// The (block, head) work of one attention task on the tensor cores.  16-position blocks of the nh
+// cached rows go round-robin over the compute warps; each warp keeps a running softmax (max m, sum l,
+// unnormalised o) per query head over its blocks and writes it as one partial; the current row
+// (owner split) is a partial of its own (m = its score, l = 1, o = its V row).  Partial p of head h
+// goes to pw + (p * g + h) * (d + 4) as o[d], m, l -- the item layout the merge reads.  Returns the
+// number of partials.  sq holds the rotated fp32 queries (attn_qpos layout, QS floats a head), cur
+// the current K and V rows as bf16, s_first the ring slot of the task's first stage.
+__device__ __forceinline__ int attn_items_mma(Ctx& c, const float* sq, int QS, int g, int nh, bool owner,
+                                              const uint16_t* cur, unsigned s_first, float scale, float* pw) {
+  constexpr int D = 64;
+  const int gid = c.lane >> 2, tig = c.lane & 3, mi = c.lane >> 3, rr = c.lane & 7;
+  const int nkb = (nh + 15) >> 4;
+  const int nwp = min(kComputeWarps, nkb);
+  if (c.warp < nkb) {
+    // B = Q^T: b0 = Q[head gid][16 ks + 2 tig, +1], b1 = the same 8 columns on (zero for heads >= g)
+    uint32_t qh[4][2], ql[4][2];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float2 x = make_float2(0.f, 0.f);
+        if (gid < g) x = *reinterpret_cast<const float2*>(sq + gid * QS + attn_qpos(16 * ks + 8 * hf + 2 * tig));
+        split_pair(x.x, x.y, qh[ks][hf], ql[ks][hf]);
+      }
+    }
+    float ot[4][4];  // O^T tile mt: dims 16 mt + gid (+ 8) by heads 2 tig, 2 tig + 1
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2 tig and 2 tig + 1 (l: this lane's rows)
+#pragma unroll 1
+    for (int kb = c.warp; kb < nkb; kb += kComputeWarps) {
+      const int j0 = kb << 4, r0 = j0 & (kMmaRows - 1);
+      unsigned slot = s_first + (unsigned)(j0 / kMmaRows);
+      slot = slot >= c.ns ? slot - c.ns : slot;
+      const uint32_t kaddr = smem_addr(c.ring + (size_t)slot * kStageBytes), vaddr = kaddr + kMmaRows * 128u;
+      // S^T: A = K rows r0 .. r0 + 15 by dims 16 ks .. 16 ks + 15 (one ldmatrix.x4 per k-step)
+      const int arow = r0 + rr + ((mi & 1) ? 8 : 0);
+      float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kaddr + swz128(arow, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+        mma_16816(sh, a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
+        mma_16816(sl, a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+      }
+      // sc[0], sc[1]: position j0 + gid, heads 2 tig, 2 tig + 1; sc[2], sc[3]: position j0 + gid + 8
+      float sc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = j0 + gid + ((k & 2) ? 8 : 0);
+        sc[k] = j < nh ? (sh[k] + sl[k]) * scale : -INFINITY;
+      }
+      float bm0 = fmaxf(sc[0], sc[2]), bm1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {  // over the 8 lanes holding the block's other positions
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+      }
+      const float nm0 = fmaxf(m0, bm0), nm1 = fmaxf(m1, bm1);  // finite: position j0 < nh is valid
+      const float cr0 = exp2f(m0 - nm0), cr1 = exp2f(m1 - nm1);  // rescale of the running sums (0 at first)
+      m0 = nm0;
+      m1 = nm1;
+      const float p0 = exp2f(sc[0] - m0), p1 = exp2f(sc[1] - m1), p2 = exp2f(sc[2] - m0), p3 = exp2f(sc[3] - m1);
+      l0 = fmaf(l0, cr0, p0 + p2);
+      l1 = fmaf(l1, cr1, p1 + p3);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ot[i][0] *= cr0;
+        ot[i][1] *= cr1;
+        ot[i][2] *= cr0;
+        ot[i][3] *= cr1;
+      }
+      // B = P^T (k = positions, n = heads)
+      uint32_t h01, l01, h23, l23;
+      split_pair(p0, p1, h01, l01);
+      split_pair(p2, p3, h23, l23);
+      const uint32_t bh0 = transpose8x8(h01), bh1 = transpose8x8(h23), bl0 = transpose8x8(l01), bl1 = transpose8x8(l23);
+      // O^T: A = V^T, dims 16 mt .. 16 mt + 15 by the block's 16 positions
+      const int vrow = r0 + rr + ((mi & 2) ? 8 : 0);
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vaddr + swz128(vrow, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        mma_16816(ot[mt], a0, a1, a2, a3, bh0, bh1);
+        mma_16816(ot[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = 2 * tig + hh;
+      if (h < g) {
+        float* pp = pw + (size_t)(c.warp * g + h) * (D + 4);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          pp[16 * mt + gid] = ot[mt][hh];
+          pp[16 * mt + gid + 8] = ot[mt][2 + hh];
+        }
+        if (gid == 0) {
+          pp[D] = hh ? m1 : m0;
+          pp[D + 1] = hh ? l1 : l0;
+        }
+      }
+    }
+  }
+  if (owner) {  // the current row: head h on warp kComputeWarps - 1 - h (the warps with the fewest blocks)
+    const int h = kComputeWarps - 1 - c.warp;
+    if (h >= 0 && h < g) {
+      const float2 q = *reinterpret_cast<const float2*>(sq + h * QS + attn_qpos(2 * c.lane));
+      const uint32_t kw = *reinterpret_cast<const uint32_t*>(cur + 2 * c.lane);
+      const uint32_t vw = *reinterpret_cast<const uint32_t*>(cur + D + 2 * c.lane);
+      const float sdot = warp_sum(fmaf(q.x, bf16_lo(kw), q.y * bf16_hi(kw)));
+      float* pp = pw + (size_t)(nwp * g + h) * (D + 4);
+      *reinterpret_cast<float2*>(pp + 2 * c.lane) = make_float2(bf16_lo(vw), bf16_hi(vw));
+      if (c.lane == 0) {
+        pp[D] = sdot * scale;
+        pp[D + 1] = 1.f;
+      }
+    }
+  }
+  return nwp + (owner ? 1 : 0);
+}
+
 // ------------------------------------------------------------------ attention task
 // One KV head, one context split: the g query heads sharing the KV head are packed into the task,
 // so each K/V row is read once from HBM (README, "Current status", decode attention).  Cached
@@ -797,6 +984,20 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   slot_after(c, 0, s_first, ph_unused);
 #pragma unroll 1
   for (int st = 0; st < nst; ++st) stage_wait(c, (unsigned)st);
+  if (c.mma && (nh & 15) != 0) {
+    // tensor-core path: V rows nh .. (end of the last 16-row block) hold whatever the tile copy read
+    // past the task's rows; zero them so that their zero weights cannot meet a NaN.  The fence orders
+    // these writes before the producer's next tile copy into the slot.
+    const int nz = (16 - (nh & 15)) * 8;  // 16-byte chunks
+    for (int i = c.ctid; i < nz; i += kCT) {
+      const int r = nh + (i >> 3);
+      unsigned slot = s_first + (unsigned)(r / kMmaRows);
+      slot = slot >= c.ns ? slot - c.ns : slot;
+      *reinterpret_cast<uint4*>(c.ring + (size_t)slot * kStageBytes + kMmaRows * 128 + (r & (kMmaRows - 1)) * 128 +
+                                (i & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
   compute_sync();
   trace_mark(c, 4);
   const int rshift = 31 - __clz(R);
@@ -812,8 +1013,10 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   // 2. work items: (block, head) -> per-item o (unnormalised), m, l
   const float scale = P.attn_scale * 1.4426950408889634f;
   const int nchunk = d >> 3;  // 16-byte K chunks per row
+  int nparts = nblk;          // partials per query head for the merge
+  if (c.mma) nparts = attn_items_mma(c, sq, QS, g, nh, owner, cur, s_first, scale, pw);
 #pragma unroll 1
-  for (int it = c.warp; it < items; it += kComputeWarps) {
+  for (int it = c.mma ? items : c.warp; it < items; it += kComputeWarps) {  // (CUDA-core items)
     const int blk = it / g, h = it - blk * g;
     const int j = (blk << 5) + c.lane;
     const bool valid = j < np;
@@ -949,10 +1152,10 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
         const int e0 = v << 3, h = e0 >> dshift, tt = e0 & (d - 1);
         const float* ph = pw + h * (d + 4);
         float M = -INFINITY;
-        for (int q = 0; q < nblk; ++q) M = fmaxf(M, ph[q * istride + d]);
+        for (int q = 0; q < nparts; ++q) M = fmaxf(M, ph[q * istride + d]);
         float den = 0.f;
 #pragma unroll 1
-        for (int q = 0; q < nblk; ++q) {
+        for (int q = 0; q < nparts; ++q) {
           const float* pq = ph + q * istride;
           const float f = exp2f(pq[d] - M);
           den = fmaf(pq[d + 1], f, den);
@@ -1030,10 +1233,10 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
     const int h = e >> dshift, tt = e & (d - 1);
     const float* ph = pw + h * (d + 4);
     float M = -INFINITY;
-    for (int q = 0; q < nblk; ++q) M = fmaxf(M, ph[q * istride + d]);
+    for (int q = 0; q < nparts; ++q) M = fmaxf(M, ph[q * istride + d]);
     float num = 0.f, den = 0.f;
 #pragma unroll 4
-    for (int q = 0; q < nblk; ++q) {
+    for (int q = 0; q < nparts; ++q) {
       const float f = exp2f(ph[q * istride + d] - M);
       num = fmaf(ph[q * istride + tt], f, num);
       den = fmaf(ph[q * istride + d + 1], f, den);
@@ -1046,17 +1249,75 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   }
 }
 
+// The split combine when the active splits' o words do not fit one poll: combine_group splits per
+// poll into `scratch` ([group][nq*d] floats), the first poll also bringing the (m, l) words of every
+// active split (after the first group's o words).  The sums run on in `o` in split order, so the
+// result is the one a single poll gives.  Each group costs a poll and two block barriers.  Kept out
+// of line (Ctx by value): only caches longer than the shared memory's combine area take it.
+__device__ __noinline__ void combine_splits_grouped(Ctx c, int l, float* o, float* scratch, int tid, int nth) {
+  const KernelParams& P = *c.P;
+  const int d = P.d, nqd = P.nq * d, dshift = 31 - __clz(d);
+  const int nact = c.pos / P.split_len + 1;
+  const int cg = P.combine_group, ng0 = min(cg, nact);
+  const unsigned long long* ob = layer_words(P, l) + P.act.att;  // o words [split][head][d], then (m, l)
+  const float* ml = scratch + ng0 * nqd;  // (m, l) of the active splits, [split][head][2]
+#pragma unroll 1
+  for (int g0 = 0; g0 < nact; g0 += cg) {
+    const int ng = min(cg, nact - g0);
+    if (tid >= 0) {
+      InVec v;
+      v.src = ob + (size_t)g0 * nqd;
+      v.src2 = ob + (size_t)P.nsplit * nqd;  // (m, l) of the active splits: a prefix of [split][head][2]
+      v.src3 = nullptr;
+      v.n1 = ng * nqd;
+      v.n2 = g0 == 0 ? nact * P.nq * 2 : 0;
+      v.n = v.n1 + v.n2;
+      v.emb = nullptr;
+      v.gain = nullptr;
+      v.dst = scratch;
+      v.xlayout = 0;
+      v.terms = nullptr;
+      v.nterm = 0;
+      v.tstride = 0;
+      poll_vec(c, v, 0x310000u, tid, nth);
+    }
+    compute_sync();
+    const bool last = g0 + ng == nact;
+#pragma unroll 1
+    for (int e = c.ctid; e < nqd; e += kCT) {
+      const int h = e >> dshift;
+      float M = -INFINITY;
+      for (int s = 0; s < nact; ++s) M = fmaxf(M, ml[(s * P.nq + h) * 2]);
+      float num = g0 == 0 ? 0.f : o[xpos(e, nqd)], den = 0.f;
+#pragma unroll 4
+      for (int s = 0; s < (last ? nact : g0 + ng); ++s) {  // den (kept by the last group) needs every split
+        const float* m = ml + (s * P.nq + h) * 2;
+        const float wgt = m[1] * exp2f(m[0] - M);
+        if (s >= g0) num = fmaf(wgt, scratch[(s - g0) * nqd + e], num);
+        den += wgt;
+      }
+      o[xpos(e, nqd)] = last ? num / den : num;
+    }
+    if (!last) compute_sync();  // the next group's words overwrite the scratch
+  }
+}
+
 // Attention output of every query head into o[nq*d] (split GEMV layout) when the context has
 // several splits: the active splits of each head are combined by their log-sum-exp weights
 // (split-context "flash decoding", README "Current status").  One poll brings every active split's o
 // words and (m, l) words into `scratch` (nsplit * (nq*d + nq*2) floats) -- threads tid of nth take
 // part, up to eight words each in flight -- and, after the block barrier, each output is the
 // weighted mean of the splits' normalised outputs, weights l_s 2^(m_s - max m), summed in split order.
-// The caller's other threads may poll other words meanwhile; every compute thread reaches the barrier.
+// (combine_splits_grouped takes over when they do not fit one poll.)  The caller's other threads may
+// poll other words meanwhile; every compute thread reaches the barrier.
 __device__ __forceinline__ void combine_splits(Ctx& c, int l, float* o, float* scratch, int tid, int nth) {
   const KernelParams& P = *c.P;
   const int d = P.d, nqd = P.nq * d, dshift = 31 - __clz(d);
   const int nact = c.pos / P.split_len + 1;
+  if (nact > P.combine_group) {
+    combine_splits_grouped(c, l, o, scratch, tid, nth);
+    return;
+  }
   const unsigned long long* ob = layer_words(P, l) + P.act.att;  // o words [split][head][d], then (m, l)
   const int no = nact * nqd;              // o words of the active splits (a prefix of [split][head][d])
   if (tid >= 0) {
@@ -1367,7 +1628,7 @@ __device__ __noinline__ bool wait_prev_step(const unsigned long long* sync, unsi
 }
 
 __device__ __forceinline__ void produce(const KernelParams& P, const StepParams& S, Ctl* ctl, unsigned char* ring,
-                                        uint32_t c0, uint32_t c1, int lane) {
+                                        uint32_t c0, uint32_t c1, int lane, const CUtensorMap* kvmap, bool mma) {
   const uint64_t policy = evict_first_policy();
   const unsigned ns = (unsigned)P.num_stages;
   unsigned stage = 0, uses = 0;  // ring slot and how many times the ring has wrapped
@@ -1433,6 +1694,24 @@ __device__ __forceinline__ void produce(const KernelParams& P, const StepParams&
             const int b = min(a + P.split_len, pos);
             for (int jj = a; jj < b; jj += P.rows_per_stage) {
               const int n = min(P.rows_per_stage, b - jj);
+              if (mma) {
+                // tensor-core path: K then V as swizzled tiles of box rows (a whole stage, or one
+                // page's share of it); rows past b come along and are masked by the consumers
+                const int br = P.attn_box_rows, nbox = (n + br - 1) / br;
+                unsigned char* dst = acquire((unsigned)(2 * nbox * br * 128), (unsigned)n);
+                if (!dst) {
+                  q = 1;
+                  break;
+                }
+                for (int bx = 0; bx < nbox; ++bx) {
+                  const int p = jj + bx * br;
+                  const int yk = (int)(kv_off(P, ctl, layer, 0, kvh, p) >> 6), yv = (int)(kv_off(P, ctl, layer, 1, kvh, p) >> 6);
+                  tile_load(dst + bx * br * 128, kvmap, 0, yk, &ctl->full[stage], policy);
+                  tile_load(dst + kMmaRows * 128 + bx * br * 128, kvmap, 0, yv, &ctl->full[stage], policy);
+                }
+                advance();
+                continue;
+              }
               const unsigned nb = (unsigned)(n * P.d * 2);
               unsigned char* dst = acquire(2 * nb, (unsigned)n);
               if (!dst) {
@@ -1494,7 +1773,8 @@ __device__ __forceinline__ void stage_tasks(const Task* src, Task* dst, int n, i
 // kGreedy: greedy decoding (the argmax of each step's logits is the next step's token).  A separate
 // instantiation, so that the teacher-forced kernel carries none of its state in registers.
 template <bool kGreedy, bool kF8>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const __grid_constant__ StepParams S) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const __grid_constant__ StepParams S,
+                                                             const __grid_constant__ CUtensorMap kvmap) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
   if (threadIdx.x == 0) {
@@ -1532,15 +1812,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   __syncthreads();
   if (ctl->skip) return;
   unsigned char* ring = smem + P.off_ring;
+  // the swizzled tiles need 1024-byte aligned stages (the host aligns the ring's offset; the base
+  // of dynamic shared memory is checked here, and the CUDA-core path taken if it is not aligned)
+  const bool mma = P.attn_mma != 0 && (smem_addr(ring) & 1023u) == 0u;
   const int warp = threadIdx.x / 32;
   if (warp == 0) {
-    produce(ctl->params, S, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31);
+    produce(ctl->params, S, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31, &kvmap, mma);
     return;
   }
   Ctx c;
   c.P = &ctl->params;
   c.ctl = ctl;
   c.ring = ring;
+  c.mma = mma;
 
   c.ns = (unsigned)P.num_stages;
   c.stage = 0;

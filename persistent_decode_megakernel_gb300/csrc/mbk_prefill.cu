@@ -719,6 +719,19 @@ int pack_tokens(const PrefillBatch& b, const int32_t* tokens, int n, int cap, st
 
 }  // namespace
 
+bool make_kv_tile_map(CUtensorMap* map, const void* kv, uint64_t rows, uint32_t box_rows) {
+  const EncodeTiled enc = encoder();
+  if (enc == nullptr || ((uintptr_t)kv & 15u) != 0u || rows == 0 || rows > 0x7fffffffull || box_rows == 0 || box_rows > 256)
+    return false;
+  const cuuint64_t dim[2] = {64, rows};
+  const cuuint64_t stride[1] = {128};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dim, stride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 void prefill_free(PrefillState& s) {
   if (s.ws != nullptr) cudaFree(s.ws);
   s.ws = nullptr;

@@ -85,4 +85,10 @@ int prefill_run(const PrefillModel& m, PrefillState& st, const int32_t* tokens_h
 // Frees the workspace (the tensor maps are host memory).
 void prefill_free(PrefillState& st);
 
+// Tensor map of a KV cache (or page pool) of head_dim 64 for the decode kernel's tensor-core
+// attention: `rows` rows of 64 bf16 (128 bytes) from `kv` (16-byte aligned), tiles of 64 columns by
+// box_rows rows with the 128-byte swizzle; reads past the last row return zeros.  False if the
+// encoder is unavailable or refuses the arguments.
+bool make_kv_tile_map(CUtensorMap* map, const void* kv, uint64_t rows, uint32_t box_rows);
+
 }  // namespace mbk

@@ -234,13 +234,24 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   // attention: rotated queries (d + d/8 floats a head), current K/V (raw, then the bf16 row appended),
   // the partial output (o, m, l) of every (32-position block, query head) item of a split, and each
   // compute warp's 32 item weights
-  const int attn_items = (p.split_len + 31) / 32 * g;
+  // tensor-core attention: one partial per compute warp that holds a 16-position block, plus the
+  // current row's (in place of the 32-position items)
+  p.attn_mma = opt.attn_mma != 0 && s.d == 64 && g <= 8;
+  const int attn_parts = p.attn_mma ? std::max((p.split_len + 31) / 32, std::min(kComputeWarps, (p.split_len + 15) / 16) + 1)
+                                    : (p.split_len + 31) / 32;
+  const int attn_items = attn_parts * g;
   const int attn_floats = g * (s.d + s.d / 8) + 3 * s.d + attn_items * (s.d + 4) + kComputeWarps * 32;
-  p.sv_floats = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
-  // the O projection of a split context combines the splits from the o and (m, l) words of every
-  // active split, polled into the vector area after the combined output
-  if (p.nsplit > 1) p.sv_floats = std::max(p.sv_floats, qd + p.nsplit * (qd + 2 * s.nq));
-  p.sv_floats = (p.sv_floats + 31) / 32 * 32;
+  const int sv_base = std::max(std::max(std::max(s.H, s.I), qd), attn_floats);
+  // the O projection of a split context combines the splits from the (m, l) words of every active
+  // split and their o words, combine_group splits per poll, polled into the vector area after the
+  // combined output; every split in one poll where the shared memory allows (set with the layout)
+  auto sv_for = [&](int cg) {
+    int v = sv_base;
+    if (p.nsplit > 1) v = std::max(v, qd + p.nsplit * 2 * s.nq + cg * qd);
+    return (v + 31) / 32 * 32;
+  };
+  p.combine_group = p.nsplit;
+  p.sv_floats = sv_for(p.combine_group);
 
   // tasks
   std::vector<std::vector<Task>> cta_tasks(num_ctas);
@@ -403,16 +414,27 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   // shared memory layout: [control block][input vector][results][residuals][task records][ring]
   p.max_cta_tasks = 0;
   for (const auto& v : cta_tasks) p.max_cta_tasks = std::max(p.max_cta_tasks, (int)v.size());
-  p.off_sv = kCtlBytes;
-  p.off_res = p.off_sv + (uint32_t)p.sv_floats * 4;
-  p.off_resid = p.off_res + kResSlots * 4;
-  p.off_tasks = p.off_resid + kMaxTaskRows * 4;
-  p.off_ring = (p.off_tasks + (uint32_t)std::min(p.max_cta_tasks, kTaskWindow) * (uint32_t)sizeof(Task) + 127) / 128 * 128;
-  int avail = opt.smem_limit - (int)p.off_ring;
-  p.num_stages = std::min(kMaxRingStages, avail / kStageBytes);
-  if (p.num_stages < 2) return "not enough shared memory for the weight ring";
-  if (p.num_stages < (p.split_len + p.attn_rows_per_stage - 1) / p.attn_rows_per_stage + 1 || p.num_stages < kGemvBatch)
-    return "weight ring too small to hold one attention split or one GEMV batch";
+  const int need_stages = std::max(std::max(2, kGemvBatch), (p.split_len + p.attn_rows_per_stage - 1) / p.attn_rows_per_stage + 1);
+  for (;;) {
+    p.off_sv = kCtlBytes;
+    p.off_res = p.off_sv + (uint32_t)p.sv_floats * 4;
+    p.off_resid = p.off_res + kResSlots * 4;
+    p.off_tasks = p.off_resid + kMaxTaskRows * 4;
+    const uint32_t ring_align = p.attn_mma ? 1024u : 128u;  // swizzled tiles: 1024-byte aligned stages
+    p.off_ring = (p.off_tasks + (uint32_t)std::min(p.max_cta_tasks, kTaskWindow) * (uint32_t)sizeof(Task) + ring_align - 1) /
+                 ring_align * ring_align;
+    const int avail = opt.smem_limit - (int)p.off_ring;
+    p.num_stages = std::min(kMaxRingStages, std::max(0, avail) / kStageBytes);
+    if (p.num_stages >= need_stages) break;
+    // the ring must hold one attention split and one GEMV batch: poll the splits in smaller groups
+    if (p.nsplit > 1 && p.combine_group > 1) {
+      p.combine_group = (p.combine_group + 1) / 2;
+      p.sv_floats = sv_for(p.combine_group);
+      continue;
+    }
+    return p.num_stages < 2 ? "not enough shared memory for the weight ring"
+                            : "weight ring too small to hold one attention split or one GEMV batch";
+  }
   p.smem_bytes = (int)p.off_ring + p.num_stages * kStageBytes;
 
   // flatten (chunk indices become global); every task gets its word offsets and flags

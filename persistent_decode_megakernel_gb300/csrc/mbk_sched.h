@@ -22,6 +22,7 @@ struct PlanOptions {
   int max_tasks_per_op = 0;    // split each projection into at most this many tasks (0: one per CTA)
   int fuse_attention = -1;     // fold the O projection into the attention tasks: -1 where it applies, 0 never
   int smem_limit = 232448;     // dynamic shared memory available per CTA
+  int attn_mma = 1;            // attention on the tensor cores where the shape allows (0: never)
 };
 
 struct Plan {
@@ -33,8 +34,10 @@ struct Plan {
   ActLayout act{};
   uint64_t act_words = 0;            // words per step (one parity)
   bool fused_attn = false;           // attention tasks also apply Wo (TF_WO); no O-projection tasks
+  bool attn_mma = false;             // attention on the tensor cores (head_dim 64, g <= 8; ring 1024-aligned)
   int nsplit = 1;                    // context splits per KV head
   int split_len = 0;                 // positions per split
+  int combine_group = 1;             // splits whose o words one poll of the split combine brings
   int attn_rows_per_stage = 0;       // cached positions per ring stage
   int num_stages = 0;
   int smem_bytes = 0;

@@ -19,6 +19,7 @@
 
 #include "../../include/mbk.h"
 #include "mbk_args.h"
+#include "mbk_prefill.h"  // make_kv_tile_map
 #include "mbk_device.h"
 #include "mbk_sched.h"
 
@@ -47,6 +48,7 @@ struct DeviceState {
   std::string resident_key;  // config + pointers of the schedule now in the array
   Plan plan;
   KernelParams kp{};
+  CUtensorMap kvmap{};  // the cache as swizzled tiles (tensor-core attention)
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -111,6 +113,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     // build the schedule (host memory) and lay it out in the array
     PlanOptions opt;
     opt.smem_limit = D.smem_optin;
+    opt.attn_mma = env_int("MBK_ATTN_MMA", 1);
     Plan plan;
     if (!build_plan(s, wa, D.num_sms, opt, &plan).empty()) return MBK_ERR_UNSUPPORTED;
     // layout: tasks | task_off | chunks | chunk_off | layer table | rope | words | status
@@ -162,6 +165,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     kp.act = plan.act;
     kp.nsplit = plan.nsplit;
     kp.split_len = plan.split_len;
+    kp.combine_group = plan.combine_group;
     kp.rows_per_stage = plan.attn_rows_per_stage;
     kp.num_stages = plan.num_stages;
     kp.off_sv = plan.off_sv;
@@ -188,6 +192,9 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     kp.page_size = s.C;
     kp.page_shift = 0;
     kp.page_elems = 0;
+    kp.attn_box_rows = std::min(s.C, 64);
+    kp.attn_mma = plan.attn_mma && make_kv_tile_map(&D.kvmap, kv_cache, (uint64_t)s.L * 2 * s.nkv * s.C,
+                                                    (uint32_t)kp.attn_box_rows) ? 1 : 0;
     kp.wbytes = 2;  // bf16 weights as given
     kp.wscale_layer = 0;
     kp.wscale = nullptr;
@@ -216,7 +223,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
   sp.out_tokens = nullptr;
   sp.tokword = nullptr;
   KernelParams kp = D.kp;
-  void* args[] = {&kp, &sp};
+  void* args[] = {&kp, &sp, &D.kvmap};
   cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(false, false), dim3(D.plan.num_ctas), dim3(kThreads), args,
                                               (size_t)D.plan.smem_bytes, st);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;

@@ -66,7 +66,7 @@ class MbkPlanInfo(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("num_tasks", ctypes.c_int), ("num_chunks", ctypes.c_int),
                 ("stage_bytes", ctypes.c_int), ("num_stages", ctypes.c_int), ("attn_splits", ctypes.c_int),
                 ("weight_bytes", ctypes.c_int64), ("max_cta_bytes", ctypes.c_int64), ("act_words", ctypes.c_int64),
-                ("smem_bytes", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_int), ("combine_group", ctypes.c_int), ("attn_mma", ctypes.c_int)]
 
 
 class MbkSimInfo(ctypes.Structure):

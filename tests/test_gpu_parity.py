@@ -75,12 +75,26 @@ def test_tiny_with_random_gains():
     rep.check()
 
 
-def test_last_cache_rows_and_ragged_split():
+@pytest.mark.parametrize("mma", ["0", "1"])
+def test_last_cache_rows_and_ragged_split(mma, monkeypatch):
     """Decode up to the last cache row (pos = C-1) with a context that spans several splits and a
-    ragged final split."""
+    ragged final split; attention on the CUDA cores (0) and on the tensor cores (1)."""
+    monkeypatch.setenv("MBK_ATTN_MMA", mma)
     shape = workloads.scaled_down(workloads.SHAPES["smollm-135m-long"], n_layers=2, kv_capacity=1500, prefill=1494,
                                   pos0=1494, steps=6, vocab=8192)
     rep = run_parity(workloads.generate(shape, seed=5))
+    rep.check()
+
+
+def test_split_combine_in_groups():
+    """A context whose active splits do not fit one poll of the split combine (16,384 positions of
+    the 135M shape: 32 splits, 16 per poll): the outputs are combined over two polls."""
+    from persistent_decode_megakernel_gb300 import mbk
+    shape = workloads.scaled_down(workloads.SHAPES["smollm-135m-long"], n_layers=2, kv_capacity=16384, prefill=9000,
+                                  pos0=9000, steps=4, vocab=4096)
+    info = mbk.mbk_plan_check(mbk.config_from_shape(shape), torch.cuda.get_device_properties(0).multi_processor_count)
+    assert info.combine_group < shape.pos0 // (shape.kv_capacity // info.attn_splits) + 1
+    rep = run_parity(workloads.generate(shape, seed=13))
     rep.check()
 
 
@@ -113,10 +127,13 @@ def test_gqa_head_dim_128_with_the_o_projection_fused():
 
 
 @pytest.mark.parametrize("fuse", ["0", "1"])
-def test_o_projection_fused_and_separate(fuse, monkeypatch):
+@pytest.mark.parametrize("mma", ["0", "1"])
+def test_o_projection_fused_and_separate(fuse, mma, monkeypatch):
     """The O projection runs either inside the attention tasks (per-KV-head partial sums) or as tasks
-    of its own; both schedules must meet the parity bars on a GQA shape with one context split."""
+    of its own, with attention on the CUDA cores or the tensor cores; every schedule must meet the
+    parity bars on a GQA shape with one context split."""
     monkeypatch.setenv("MBK_FUSE_ATTENTION", fuse)
+    monkeypatch.setenv("MBK_ATTN_MMA", mma)
     shape = workloads.scaled_down(workloads.SHAPES["smollm-135m"], n_layers=4, vocab=8192, steps=12)
     rep = run_parity(workloads.generate(shape, seed=9))
     rep.check()

@@ -65,6 +65,34 @@ def test_plan_builds_and_checks(lib, name, num_sms):
         assert info.attn_splits == 1
 
 
+@pytest.mark.parametrize("shape,mma", [("tiny", 1), ("smollm-135m", 1), ("qwen2-0.5b", 1), ("smollm-1.7b", 1),
+                                       ("smollm-135m-long", 1), ("mqa16", 0), ("mha128", 0)])
+def test_plan_puts_attention_on_the_tensor_cores_where_the_shape_allows(lib, monkeypatch, shape, mma):
+    """Head dim 64 with at most 8 query heads per KV head: tensor-core attention, with the weight ring
+    at a 1024-byte aligned offset (the swizzled K/V tiles); other shapes, or MBK_ATTN_MMA=0: CUDA cores."""
+    extra = {"mqa16": workloads.DecoderShape("mqa16", 2, 1024, 2048, 16, 1, 64, 2048, 96, 1e-5, 1e4, False, steps=1),
+             "mha128": workloads.DecoderShape("mha128", 2, 512, 1024, 4, 4, 128, 2048, 64, 1e-5, 1e4, False, steps=1)}
+    s = extra.get(shape) or workloads.SHAPES[shape]
+    info = mbk.mbk_plan_check(mbk.config_from_shape(s), 152)
+    assert info.attn_mma == mma
+    if mma:
+        assert (info.smem_bytes - info.num_stages * info.stage_bytes) % 1024 == 0
+    monkeypatch.setenv("MBK_ATTN_MMA", "0")
+    assert mbk.mbk_plan_check(mbk.config_from_shape(s), 152).attn_mma == 0
+
+
+@pytest.mark.parametrize("capacity,groups", [(8192, 1), (16384, 2), (80000, 16)])
+def test_split_combine_groups_fit_the_shared_memory(lib, capacity, groups):
+    """Long caches: the split combine brings as many splits per poll as the shared memory holds next
+    to a weight ring deep enough for one attention split; the rest come in further polls."""
+    s = workloads.scaled_down(workloads.SHAPES["smollm-135m-long"], kv_capacity=capacity)
+    info = mbk.mbk_plan_check(mbk.config_from_shape(s), 152)
+    assert info.attn_splits == (capacity + 511) // 512
+    assert -(-info.attn_splits // info.combine_group) == groups
+    assert info.num_stages >= 512 // 64 + 1
+    assert info.smem_bytes <= 232448
+
+
 def test_plan_balances_bytes_across_ctas(lib):
     s = workloads.SHAPES["smollm-135m"]
     info = mbk.mbk_plan_check(mbk.config_from_shape(s), 152)
