@@ -705,6 +705,14 @@ __device__ __forceinline__ float res_row(const float* res, int i, int gpr) {
   return v;
 }
 
+// One rotate-half RoPE pair: (x0, x1) at (i, i + d/2) turned by the angle whose cosine and sine are
+// r.x and r.y.  Products and sums are rounded one at a time (no contraction), so every site that
+// rotates the same values gets the same bits -- the K row appended to the cache and the score this
+// step takes with it.
+__device__ __forceinline__ float2 rope_rot(float x0, float x1, float2 r) {
+  return make_float2(__fsub_rn(__fmul_rn(x0, r.x), __fmul_rn(x1, r.y)), __fadd_rn(__fmul_rn(x1, r.x), __fmul_rn(x0, r.y)));
+}
+
 // ------------------------------------------------------------------ attention on the tensor cores
 // Head dimension 64, at most 8 query heads per KV head.  The producer brings each stage's K rows
 // (64 of them, 128 bytes each) and then its V rows as 2-D TMA tiles with the 128-byte swizzle: the
@@ -759,25 +767,47 @@ __device__ __forceinline__ uint32_t swz128(int r, int ch) { return (uint32_t)r *
 // unnormalised o) per query head over its blocks and writes it as one partial; the current row
 // (owner split) is a partial of its own (m = its score, l = 1, o = its V row).  Partial p of head h
 // goes to pw + (p * g + h) * (d + 4) as o[d], m, l -- the item layout the merge reads.  Returns the
-// number of partials.  sq holds the rotated fp32 queries (attn_qpos layout, QS floats a head), cur
-// the current K and V rows as bf16, s_first the ring slot of the task's first stage.
+// number of partials.  sq holds the raw (not yet rotated) fp32 queries (attn_qpos layout, QS floats
+// a head), kv the raw current K and V rows (fp32), s_first the ring slot of the task's first stage.
 __device__ __forceinline__ int attn_items_mma(Ctx& c, const float* sq, int QS, int g, int nh, bool owner,
-                                              const uint16_t* cur, unsigned s_first, float scale, float* pw) {
+                                              const float* kv, unsigned s_first, float scale, float* pw) {
   constexpr int D = 64;
   const int gid = c.lane >> 2, tig = c.lane & 3, mi = c.lane >> 3, rr = c.lane & 7;
   const int nkb = (nh + 15) >> 4;
   const int nwp = min(kComputeWarps, nkb);
+  const float2* cs = c.ctl->rope;  // this step's cos/sin
   if (c.warp < nkb) {
-    // B = Q^T: b0 = Q[head gid][16 ks + 2 tig, +1], b1 = the same 8 columns on (zero for heads >= g)
-    uint32_t qh[4][2], ql[4][2];
+    // B = Q^T: b0 = Q[head gid][16 ks + 2 tig, +1], b1 = the same 8 columns on (zero for heads >= g).
+    // The lane holds both halves of each rotate-half pair it needs (columns i and i + 32 sit in
+    // k-steps ks and ks + 2), so it applies RoPE to the raw queries itself.
+    float qv[4][2][2];
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float2 x = make_float2(0.f, 0.f);
         if (gid < g) x = *reinterpret_cast<const float2*>(sq + gid * QS + attn_qpos(16 * ks + 8 * hf + 2 * tig));
-        split_pair(x.x, x.y, qh[ks][hf], ql[ks][hf]);
+        qv[ks][hf][0] = x.x;
+        qv[ks][hf][1] = x.y;
       }
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float2 y = rope_rot(qv[ks][hf][e], qv[ks + 2][hf][e], cs[16 * ks + 8 * hf + 2 * tig + e]);
+          qv[ks][hf][e] = y.x;
+          qv[ks + 2][hf][e] = y.y;
+        }
+      }
+    }
+    uint32_t qh[4][2], ql[4][2];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) split_pair(qv[ks][hf][0], qv[ks][hf][1], qh[ks][hf], ql[ks][hf]);
     }
     float ot[4][4];  // O^T tile mt: dims 16 mt + gid (+ 8) by heads 2 tig, 2 tig + 1
 #pragma unroll
@@ -866,12 +896,28 @@ __device__ __forceinline__ int attn_items_mma(Ctx& c, const float* sq, int QS, i
   if (owner) {  // the current row: head h on warp kComputeWarps - 1 - h (the warps with the fewest blocks)
     const int h = kComputeWarps - 1 - c.warp;
     if (h >= 0 && h < g) {
-      const float2 q = *reinterpret_cast<const float2*>(sq + h * QS + attn_qpos(2 * c.lane));
-      const uint32_t kw = *reinterpret_cast<const uint32_t*>(cur + 2 * c.lane);
-      const uint32_t vw = *reinterpret_cast<const uint32_t*>(cur + D + 2 * c.lane);
-      const float sdot = warp_sum(fmaf(q.x, bf16_lo(kw), q.y * bf16_hi(kw)));
+      // lane: elements 2 lane, 2 lane + 1 of the raw query and of the raw K and V rows (kv); the
+      // rotate-half partner of element i < 32 is i + 32, in lane (lane + 16) mod 32.  K is rotated
+      // and rounded exactly as the row appended to the cache.
+      const int e = 2 * c.lane;
+      const bool lo = c.lane < 16;
+      const float2 q = *reinterpret_cast<const float2*>(sq + h * QS + attn_qpos(e));
+      const float2 k = *reinterpret_cast<const float2*>(kv + e);
+      const float2 v = *reinterpret_cast<const float2*>(kv + D + e);
+      const float q0p = __shfl_xor_sync(0xffffffffu, q.x, 16), q1p = __shfl_xor_sync(0xffffffffu, q.y, 16);
+      const float k0p = __shfl_xor_sync(0xffffffffu, k.x, 16), k1p = __shfl_xor_sync(0xffffffffu, k.y, 16);
+      const float2 r0 = cs[e & 31], r1 = cs[(e + 1) & 31];
+      const float2 qa = lo ? rope_rot(q.x, q0p, r0) : rope_rot(q0p, q.x, r0);
+      const float2 qb = lo ? rope_rot(q.y, q1p, r1) : rope_rot(q1p, q.y, r1);
+      const float2 ka = lo ? rope_rot(k.x, k0p, r0) : rope_rot(k0p, k.x, r0);
+      const float2 kb = lo ? rope_rot(k.y, k1p, r1) : rope_rot(k1p, k.y, r1);
+      const float q0 = lo ? qa.x : qa.y, q1 = lo ? qb.x : qb.y;
+      const float k0 = __bfloat162float(__float2bfloat16_rn(lo ? ka.x : ka.y));
+      const float k1 = __bfloat162float(__float2bfloat16_rn(lo ? kb.x : kb.y));
+      const float sdot = warp_sum(fmaf(q0, k0, q1 * k1));
       float* pp = pw + (size_t)(nwp * g + h) * (D + 4);
-      *reinterpret_cast<float2*>(pp + 2 * c.lane) = make_float2(bf16_lo(vw), bf16_hi(vw));
+      *reinterpret_cast<float2*>(pp + e) =
+          make_float2(__bfloat162float(__float2bfloat16_rn(v.x)), __bfloat162float(__float2bfloat16_rn(v.y)));
       if (c.lane == 0) {
         pp[D] = sdot * scale;
         pp[D + 1] = 1.f;
@@ -945,23 +991,24 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   }
   compute_sync();
   trace_mark(c, 1);
-  // RoPE (rotate-half pairs (i, i + d/2)); the current K/V row is rounded to bf16 and appended
+  // RoPE (rotate-half pairs (i, i + d/2)) of the queries, in place (the tensor-core path rotates
+  // them in its fragments instead); the current K/V row is rounded to bf16 and appended
+  if (!c.mma) {
 #pragma unroll 1
-  for (int e = c.ctid; e < g * half; e += kCT) {
-    const int h = e >> hshift, i = e & (half - 1);
-    const float2 r = cs[i];
-    float* q = sq + h * QS;
-    const int i0 = attn_qpos(i), i1 = attn_qpos(i + half);
-    const float x0 = q[i0], x1 = q[i1];
-    q[i0] = x0 * r.x - x1 * r.y;
-    q[i1] = x1 * r.x + x0 * r.y;
+    for (int e = c.ctid; e < g * half; e += kCT) {
+      const int h = e >> hshift, i = e & (half - 1);
+      float* q = sq + h * QS;
+      const int i0 = attn_qpos(i), i1 = attn_qpos(i + half);
+      const float2 y = rope_rot(q[i0], q[i1], cs[i]);
+      q[i0] = y.x;
+      q[i1] = y.y;
+    }
   }
   if (owner && c.ctid >= kCT - half) {
     const int i = c.ctid - (kCT - half);
-    const float2 r = cs[i];
-    const float x0 = kc[i], x1 = kc[i + half];
-    const __nv_bfloat16 k0 = __float2bfloat16_rn(x0 * r.x - x1 * r.y);
-    const __nv_bfloat16 k1 = __float2bfloat16_rn(x1 * r.x + x0 * r.y);
+    const float2 y = rope_rot(kc[i], kc[i + half], cs[i]);
+    const __nv_bfloat16 k0 = __float2bfloat16_rn(y.x);
+    const __nv_bfloat16 k1 = __float2bfloat16_rn(y.y);
     const __nv_bfloat16 v0 = __float2bfloat16_rn(vc[i]);
     const __nv_bfloat16 v1 = __float2bfloat16_rn(vc[i + half]);
     cur[i] = __bfloat16_as_ushort(k0);
@@ -984,21 +1031,23 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   slot_after(c, 0, s_first, ph_unused);
 #pragma unroll 1
   for (int st = 0; st < nst; ++st) stage_wait(c, (unsigned)st);
-  if (c.mma && (nh & 15) != 0) {
-    // tensor-core path: V rows nh .. (end of the last 16-row block) hold whatever the tile copy read
-    // past the task's rows; zero them so that their zero weights cannot meet a NaN.  The fence orders
-    // these writes before the producer's next tile copy into the slot.
-    const int nz = (16 - (nh & 15)) * 8;  // 16-byte chunks
-    for (int i = c.ctid; i < nz; i += kCT) {
-      const int r = nh + (i >> 3);
-      unsigned slot = s_first + (unsigned)(r / kMmaRows);
+  if (!c.mma) {
+    compute_sync();  // the rotated queries and the current row
+  } else if ((nh & 15) != 0 && c.warp == ((nh - 1) >> 4) % kComputeWarps) {
+    // tensor-core path (no block barrier: each warp reads only the raw queries and its own blocks):
+    // V rows nh .. (end of the last 16-row block) hold whatever the tile copy read past the task's
+    // rows; the warp that takes that block zeroes them, so that their zero weights cannot meet a NaN.
+    // The fence orders these writes before the producer's next tile copy into the slot.
+    for (int i = c.lane; i < (16 - (nh & 15)) * 8; i += 32) {
+      const int row = nh + (i >> 3);
+      unsigned slot = s_first + (unsigned)(row / kMmaRows);
       slot = slot >= c.ns ? slot - c.ns : slot;
-      *reinterpret_cast<uint4*>(c.ring + (size_t)slot * kStageBytes + kMmaRows * 128 + (r & (kMmaRows - 1)) * 128 +
+      *reinterpret_cast<uint4*>(c.ring + (size_t)slot * kStageBytes + kMmaRows * 128 + (row & (kMmaRows - 1)) * 128 +
                                 (i & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
   }
-  compute_sync();
   trace_mark(c, 4);
   const int rshift = 31 - __clz(R);
   const unsigned ns = c.ns;
@@ -1014,7 +1063,7 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
   const float scale = P.attn_scale * 1.4426950408889634f;
   const int nchunk = d >> 3;  // 16-byte K chunks per row
   int nparts = nblk;          // partials per query head for the merge
-  if (c.mma) nparts = attn_items_mma(c, sq, QS, g, nh, owner, cur, s_first, scale, pw);
+  if (c.mma) nparts = attn_items_mma(c, sq, QS, g, nh, owner, kc, s_first, scale, pw);
 #pragma unroll 1
   for (int it = c.mma ? items : c.warp; it < items; it += kComputeWarps) {  // (CUDA-core items)
     const int blk = it / g, h = it - blk * g;
@@ -1138,42 +1187,54 @@ __device__ __forceinline__ void task_attn(Ctx& c, const Task& t, float* sv, floa
 
   const int istride = g * (d + 4);  // items of one head are g apart
   if (wo) {
-    // 3'. (fused) output rows of this KV head's columns of Wo.  Each lane owns the 8-element groups
-    // v = lane (+32) of o and merges them itself from the items (o = sum_b o_b 2^(m_b - M) /
-    // sum_b l_b 2^(m_b - M), M = max_b m_b): no merge pass and no barrier before the dot products.
+    // 3'. (fused) output rows of this KV head's columns of Wo.  The partials are merged once
+    // (o = sum_p o_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p), each thread of the first
+    // O/4 taking four elements, into the query area (free now); after the barrier every warp reads
+    // the merged o for its dot products.  (Merging in every warp instead saves the barrier but
+    // multiplies the shared-memory reads by the warp count.)
+    float* om = sq;
+#pragma unroll 1
+    for (int i = c.ctid; i < (O >> 2); i += kCT) {
+      const int e0 = i << 2, h = e0 >> dshift, tt = e0 & (d - 1);
+      const float* ph = pw + h * (d + 4);
+      float M = -INFINITY;
+#pragma unroll 4
+      for (int q = 0; q < nparts; ++q) M = fmaxf(M, ph[q * istride + d]);
+      float den = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int q = 0; q < nparts; ++q) {
+        const float* pq = ph + q * istride;
+        const float f = exp2f(pq[d] - M);
+        den = fmaf(pq[d + 1], f, den);
+        const float4 o4 = *reinterpret_cast<const float4*>(pq + tt);
+        acc.x = fmaf(o4.x, f, acc.x);
+        acc.y = fmaf(o4.y, f, acc.y);
+        acc.z = fmaf(o4.z, f, acc.z);
+        acc.w = fmaf(o4.w, f, acc.w);
+      }
+      const float inv = 1.f / den;
+      *reinterpret_cast<float4*>(om + e0) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    compute_sync();
     const int nvec = O >> 3;  // <= 64 for fused plans
     float ov[2][8];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int v = c.lane + 32 * k;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ov[k][j] = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
       if (v < nvec) {
-        const int e0 = v << 3, h = e0 >> dshift, tt = e0 & (d - 1);
-        const float* ph = pw + h * (d + 4);
-        float M = -INFINITY;
-        for (int q = 0; q < nparts; ++q) M = fmaxf(M, ph[q * istride + d]);
-        float den = 0.f;
-#pragma unroll 1
-        for (int q = 0; q < nparts; ++q) {
-          const float* pq = ph + q * istride;
-          const float f = exp2f(pq[d] - M);
-          den = fmaf(pq[d + 1], f, den);
-          const float4 o0 = *reinterpret_cast<const float4*>(pq + tt);
-          const float4 o1 = *reinterpret_cast<const float4*>(pq + tt + 4);
-          ov[k][0] = fmaf(o0.x, f, ov[k][0]);
-          ov[k][1] = fmaf(o0.y, f, ov[k][1]);
-          ov[k][2] = fmaf(o0.z, f, ov[k][2]);
-          ov[k][3] = fmaf(o0.w, f, ov[k][3]);
-          ov[k][4] = fmaf(o1.x, f, ov[k][4]);
-          ov[k][5] = fmaf(o1.y, f, ov[k][5]);
-          ov[k][6] = fmaf(o1.z, f, ov[k][6]);
-          ov[k][7] = fmaf(o1.w, f, ov[k][7]);
-        }
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ov[k][j] *= inv;
+        a = *reinterpret_cast<const float4*>(om + 8 * v);
+        b = *reinterpret_cast<const float4*>(om + 8 * v + 4);
       }
+      ov[k][0] = a.x;
+      ov[k][1] = a.y;
+      ov[k][2] = a.z;
+      ov[k][3] = a.w;
+      ov[k][4] = b.x;
+      ov[k][5] = b.y;
+      ov[k][6] = b.z;
+      ov[k][7] = b.w;
     }
     trace_mark(c, 6);
     const size_t row_bytes = (size_t)O * (F8 ? 1 : 2);

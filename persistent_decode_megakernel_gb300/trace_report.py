@@ -11,9 +11,9 @@ gate/up, down) medians over the middle layers and the traced repetitions:
   tail  -- the last task of the round ending after the median one (imbalance and stragglers);
   span  -- the round on the critical path: from the previous round's last task to this round's.
 
-Attention tasks also report their phases (rotation and K/V staging, the (block, head) items, the
-merge of the items, the fused O rows), and the median SM clock seen by the tasks (clock64 against
-globaltimer).  The trace switch adds a few globaltimer stores per task, so traced steps run a few
+Attention tasks also report their phases (inputs ready to the first K/V stage landed; rotation and
+K/V staging; the (block, head) items; the merge of the items; the fused O rows), and the median SM
+clock seen by the tasks (clock64 against globaltimer).  The trace switch adds a few globaltimer stores per task, so traced steps run a few
 percent slower than untraced ones.
 
   python -m persistent_decode_megakernel_gb300.trace_report [--config smollm-135m] [--pos 100] [--reps 6]
@@ -40,7 +40,8 @@ def trace_rounds(name: str, pos: int, reps: int = 6, device: int = 0) -> dict:
     plan = mbk.mbk_debug_plan(dec.handle)
     cta, types, layer = plan[:, 0], plan[:, 1], plan[:, 2]
     res = {k: {"hop": [], "exec": [], "tail": [], "span": []} for k in ROUNDS}
-    attn = {"rope_and_kv_staged": [], "items": [], "merge": [], "o_rows": [], "combine_and_out": []}
+    attn = {"first_stage_wait": [], "rope_and_kv_staged": [], "items": [], "merge": [], "o_rows": [],
+            "combine_and_out": []}
     clocks, spans = [], []
     mid = (types == 2) & (layer >= 2) & (layer < s.n_layers - 2)
     for _ in range(reps):
@@ -71,6 +72,8 @@ def trace_rounds(name: str, pos: int, reps: int = 6, device: int = 0) -> dict:
                 prev_end = np.nanmax(en)
         r = rel[mid]
         if len(r):
+            if np.isfinite(r[:, 3]).any():
+                attn["first_stage_wait"].append(np.nanmedian(r[:, 3] - r[:, 1]))
             attn["rope_and_kv_staged"].append(np.nanmedian(r[:, 4] - r[:, 1]))
             attn["items"].append(np.nanmedian(r[:, 5] - r[:, 4]))
             if np.isfinite(r[:, 6]).any():
