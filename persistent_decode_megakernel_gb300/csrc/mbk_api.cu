@@ -139,6 +139,8 @@ int mbk_plan_check(const mbk_config* cfg, int num_sms, mbk_plan_info* info) {
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
   opt.fuse_attention = env_int("MBK_FUSE_ATTENTION", -1);
   opt.attn_mma = env_int("MBK_ATTN_MMA", 1);
+  opt.attn_split = env_int("MBK_ATTN_SPLIT", 0);
+  opt.combine_tasks = env_int("MBK_COMBINE_TASKS", 0);
   std::string err = build_plan(s, w, num_sms, opt, &p);
   if (!err.empty()) return MBK_ERR_STATE;
   info->num_ctas = p.num_ctas;
@@ -283,6 +285,8 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   opt.max_tasks_per_op = env_int("MBK_MAX_TASKS_PER_OP", 0);
   opt.fuse_attention = env_int("MBK_FUSE_ATTENTION", -1);
   opt.attn_mma = env_int("MBK_ATTN_MMA", 1);
+  opt.attn_split = env_int("MBK_ATTN_SPLIT", 0);
+  opt.combine_tasks = env_int("MBK_COMBINE_TASKS", 0);
   std::string err = build_plan(s, wa, prop.multiProcessorCount, opt, &h->plan);
   if (!err.empty()) {
     free_all(h);

@@ -41,6 +41,8 @@ void add_chunks(std::vector<Chunk>& out, const Seg& sg) {
 // time.  Among the feasible splits, the largest one that keeps every lane on at least one vector
 // and no more warps than the task's largest kGemvBatch-chunk batch can use, within the
 // partial-result slots.
+constexpr int kCombineRows = 24;  // fewest output rows of a split-context O-projection task (by default)
+
 uint32_t pow2_floor(uint32_t v) {
   uint32_t p = 1;
   while (p * 2 <= v) p *= 2;
@@ -207,7 +209,8 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   // attention context splits: one split for short caches; otherwise splits of at most
   // kAttnSplitMax positions and at most kAttnSplitStages ring stages (a split holds all its stages)
   p.attn_rows_per_stage = kStageBytes / (2 * s.d * 2);
-  const int split_cap = std::min(kAttnSplitMax, kAttnSplitStages * p.attn_rows_per_stage);
+  if (opt.attn_split != 0 && (opt.attn_split < 64 || opt.attn_split % 64 != 0)) return "attention split not a multiple of 64";
+  const int split_cap = std::min(opt.attn_split > 0 ? opt.attn_split : kAttnSplitMax, kAttnSplitStages * p.attn_rows_per_stage);
   p.split_len = s.C <= split_cap ? s.C : split_cap;
   p.nsplit = (s.C + p.split_len - 1) / p.split_len;
   // the split combine keeps (m, l) of every query head and split in the results area
@@ -268,6 +271,11 @@ std::string build_plan(const PlanShape& s, const WeightAddrs& w, int num_ctas, c
   auto gemv_op = [&](TaskType type, int layer, int rows, int res_per_row, int row_bytes, auto segs_for) {
     int n = std::min(max_tasks, rows);
     if (type == T_OPROJ && n_busy < num_ctas) n = std::min(n, num_ctas - n_busy);  // one task per free CTA
+    // A split context's O-projection tasks each poll every active split's outputs before their rows;
+    // many such tasks flood L2 with polls and slow every exchange of the layer, so they get at least
+    // kCombineRows rows each (24 tasks at hidden 576 measured fastest, between 8 and 104)
+    if (type == T_OPROJ && p.nsplit > 1)
+      n = std::min(n, opt.combine_tasks > 0 ? opt.combine_tasks : std::max(1, rows / kCombineRows));
     // results per task must fit the result slots, and its chunks the per-task chunk bound
     const int rpc = kStageBytes / row_bytes;
     auto chunks_for = [&](int task_rows) { return res_per_row * ((task_rows + rpc - 1) / rpc) + 2; };

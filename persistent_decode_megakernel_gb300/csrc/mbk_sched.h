@@ -23,6 +23,9 @@ struct PlanOptions {
   int fuse_attention = -1;     // fold the O projection into the attention tasks: -1 where it applies, 0 never
   int smem_limit = 232448;     // dynamic shared memory available per CTA
   int attn_mma = 1;            // attention on the tensor cores where the shape allows (0: never)
+  int attn_split = 0;          // longest attention split in positions (0: kAttnSplitMax; else a multiple of 64)
+  int combine_tasks = 0;       // O-projection tasks of a split context (each polls every split's outputs);
+                               // 0: one per kCombineRows output rows
 };
 
 struct Plan {

@@ -105,6 +105,8 @@ extern "C" int mbk_plan_simulate(const mbk_config* cfg, int num_sms, int positio
   if (const char* e = std::getenv("MBK_MAX_TASKS_PER_OP")) opt.max_tasks_per_op = std::atoi(e);
   if (const char* e = std::getenv("MBK_FUSE_ATTENTION")) opt.fuse_attention = std::atoi(e);
   if (const char* e = std::getenv("MBK_ATTN_MMA")) opt.attn_mma = std::atoi(e);
+  if (const char* e = std::getenv("MBK_ATTN_SPLIT")) opt.attn_split = std::atoi(e);
+  if (const char* e = std::getenv("MBK_COMBINE_TASKS")) opt.combine_tasks = std::atoi(e);
   Plan p;
   if (!build_plan(s, fake_weight_addrs(s), num_sms, opt, &p).empty()) return MBK_ERR_STATE;
   // the same host-side fault injection as a handle: one task dropped from its CTA's list

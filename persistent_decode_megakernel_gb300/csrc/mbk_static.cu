@@ -114,6 +114,8 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     PlanOptions opt;
     opt.smem_limit = D.smem_optin;
     opt.attn_mma = env_int("MBK_ATTN_MMA", 1);
+    opt.attn_split = env_int("MBK_ATTN_SPLIT", 0);
+    opt.combine_tasks = env_int("MBK_COMBINE_TASKS", 0);
     Plan plan;
     if (!build_plan(s, wa, D.num_sms, opt, &plan).empty()) return MBK_ERR_UNSUPPORTED;
     // layout: tasks | task_off | chunks | chunk_off | layer table | rope | words | status

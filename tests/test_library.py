@@ -93,6 +93,28 @@ def test_split_combine_groups_fit_the_shared_memory(lib, capacity, groups):
     assert info.smem_bytes <= 232448
 
 
+def test_split_context_o_projection_gets_at_least_24_rows_per_task(lib, monkeypatch):
+    """A split context's O-projection tasks each poll every split's outputs; the plan gives each at
+    least 24 output rows (24 tasks per layer at hidden 576) unless MBK_COMBINE_TASKS says otherwise."""
+    s = workloads.SHAPES["smollm-135m-long"]
+    base = mbk.mbk_plan_check(mbk.config_from_shape(s), 152).num_tasks
+    monkeypatch.setenv("MBK_COMBINE_TASKS", "48")
+    assert mbk.mbk_plan_check(mbk.config_from_shape(s), 152).num_tasks == base + s.n_layers * (48 - 24)
+    monkeypatch.setenv("MBK_COMBINE_TASKS", "24")
+    assert mbk.mbk_plan_check(mbk.config_from_shape(s), 152).num_tasks == base
+
+
+@pytest.mark.parametrize("split,splits", [("256", 32), ("512", 16), ("100", None), ("32", None)])
+def test_attention_split_length_knob(lib, monkeypatch, split, splits):
+    monkeypatch.setenv("MBK_ATTN_SPLIT", split)
+    cfg = mbk.config_from_shape(workloads.SHAPES["smollm-135m-long"])
+    if splits is None:
+        with pytest.raises(mbk.MbkError):
+            mbk.mbk_plan_check(cfg, 152)
+    else:
+        assert mbk.mbk_plan_check(cfg, 152).attn_splits == splits
+
+
 def test_plan_balances_bytes_across_ctas(lib):
     s = workloads.SHAPES["smollm-135m"]
     info = mbk.mbk_plan_check(mbk.config_from_shape(s), 152)
