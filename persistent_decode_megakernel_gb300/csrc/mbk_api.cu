@@ -17,7 +17,7 @@
 #include "mbk_sched.h"
 
 namespace mbk {
-const void* decode_kernel_ptr(bool greedy, bool fp8);
+const void* decode_kernel_ptr(bool greedy, bool fp8, bool mma);
 cudaError_t launch_quantize_fp8(const uint16_t* w, int rows, int cols, uint8_t* q, float* s, cudaStream_t st);
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
 cudaError_t launch_kv_fill(const KernelParams& kp, int layer, const float* k_raw, const float* v_raw, int p0, int n,
@@ -311,8 +311,9 @@ int create_impl(const mbk_config* cfg, const mbk_weights* weights, void* kv_cach
   const Plan& p = h->plan;
   h->grid = p.num_ctas;
 
-  for (bool greedy : {false, true}) {  // the teacher-forced and the greedy instantiation
-    const void* kfn = decode_kernel_ptr(greedy, s.wb == 1);
+  for (int k = 0; k < 4; ++k) {  // teacher-forced and greedy, tensor-core and CUDA-core attention
+    const bool greedy = (k & 1) != 0, mma = (k & 2) != 0;
+    const void* kfn = decode_kernel_ptr(greedy, s.wb == 1, mma);
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess) {
       free_all(h);
       delete h;
@@ -462,7 +463,7 @@ int launch_steps(mbk_handle* h, int32_t token, const int32_t* d_tokens, int n, i
     h->inject_armed = false;
   }
   void* args[] = {&kp, &sp, &h->kvmap};
-  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(sp.greedy != 0, h->kp.wbytes == 1), dim3(h->grid),
+  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(sp.greedy != 0, h->kp.wbytes == 1, h->kp.attn_mma != 0), dim3(h->grid),
                                               dim3(kThreads), args,
                                               (size_t)h->plan.smem_bytes, (cudaStream_t)stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;

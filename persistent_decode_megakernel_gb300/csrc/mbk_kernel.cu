@@ -1833,13 +1833,23 @@ __device__ __forceinline__ void stage_tasks(const Task* src, Task* dst, int n, i
 
 // kGreedy: greedy decoding (the argmax of each step's logits is the next step's token).  A separate
 // instantiation, so that the teacher-forced kernel carries none of its state in registers.
-template <bool kGreedy, bool kF8>
+// kMma: attention on the tensor cores (K/V stages as swizzled tiles) or on the CUDA cores; separate
+// instantiations, so that each carries only the attention path it runs -- code that is never executed
+// still costs instruction-cache capacity in a kernel that walks its whole body every layer.
+template <bool kGreedy, bool kF8, bool kMma>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KernelParams P, const __grid_constant__ StepParams S,
                                                              const __grid_constant__ CUtensorMap kvmap) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
   if (threadIdx.x == 0) {
     ctl->skip = *(volatile unsigned*)P.status;  // sticky error from an earlier step: do nothing
+    // the swizzled tiles need 1024-byte aligned ring stages: the host aligns the ring's offset and
+    // dynamic shared memory starts on a 1 KB boundary; should it not, the step fails (status) rather
+    // than read misplaced rows
+    if (kMma && ctl->skip == 0u && (smem_addr(smem + P.off_ring) & 1023u) != 0u) {
+      record_failure(P.status, P.host_status, &ctl->abort, 0u, 0xA1160000u);
+      ctl->skip = 1u;
+    }
     ctl->abort = 0;
     ctl->prod_quit = 0;
     for (int s = 0; s < P.num_stages; ++s) {
@@ -1873,9 +1883,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   __syncthreads();
   if (ctl->skip) return;
   unsigned char* ring = smem + P.off_ring;
-  // the swizzled tiles need 1024-byte aligned stages (the host aligns the ring's offset; the base
-  // of dynamic shared memory is checked here, and the CUDA-core path taken if it is not aligned)
-  const bool mma = P.attn_mma != 0 && (smem_addr(ring) & 1023u) == 0u;
+  constexpr bool mma = kMma;
   const int warp = threadIdx.x / 32;
   if (warp == 0) {
     produce(ctl->params, S, ctl, ring, P.chunk_off[blockIdx.x], P.chunk_off[blockIdx.x + 1], threadIdx.x & 31, &kvmap, mma);
@@ -2002,12 +2010,19 @@ __global__ void kv_fill_kernel(uint16_t* kv, int layer, const float* k_raw, cons
 
 // Launch helpers used by the C ABI (mbk_api.cu).
 namespace mbk {
-const void* decode_kernel_ptr(bool greedy, bool fp8) {
+const void* decode_kernel_ptr(bool greedy, bool fp8, bool mma) {
+  if (mma) {
+    if (fp8)
+      return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, true, true>)
+                    : reinterpret_cast<const void*>(&decode_kernel<false, true, true>);
+    return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, false, true>)
+                  : reinterpret_cast<const void*>(&decode_kernel<false, false, true>);
+  }
   if (fp8)
-    return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, true>)
-                  : reinterpret_cast<const void*>(&decode_kernel<false, true>);
-  return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, false>)
-                : reinterpret_cast<const void*>(&decode_kernel<false, false>);
+    return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, true, false>)
+                  : reinterpret_cast<const void*>(&decode_kernel<false, true, false>);
+  return greedy ? reinterpret_cast<const void*>(&decode_kernel<true, false, false>)
+                : reinterpret_cast<const void*>(&decode_kernel<false, false, false>);
 }
 
 // FP8 copies of a bf16 matrix [rows][cols] (cols even): per row the scale amax / 448 (1 for an

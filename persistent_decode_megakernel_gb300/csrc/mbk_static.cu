@@ -24,7 +24,7 @@
 #include "mbk_sched.h"
 
 namespace mbk {
-const void* decode_kernel_ptr(bool greedy, bool fp8);
+const void* decode_kernel_ptr(bool greedy, bool fp8, bool mma);
 cudaError_t launch_rope_table(float2* out, int C, int d, double theta, cudaStream_t st);
 }  // namespace mbk
 
@@ -96,8 +96,10 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     cudaDeviceGetAttribute(&D.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (!coop) return MBK_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(decode_kernel_ptr(false, false), cudaFuncAttributeMaxDynamicSharedMemorySize, D.smem_optin) != cudaSuccess)
-      return MBK_ERR_CUDA;
+    for (bool mma : {false, true})
+      if (cudaFuncSetAttribute(decode_kernel_ptr(false, false, mma), cudaFuncAttributeMaxDynamicSharedMemorySize, D.smem_optin) !=
+          cudaSuccess)
+        return MBK_ERR_CUDA;
     D.base = static_cast<unsigned char*>(p);
     D.num_sms = prop.multiProcessorCount;
     D.ready = true;
@@ -226,7 +228,7 @@ extern "C" int mbk_decode_step_static(const mbk_config* cfg, const mbk_weights* 
   sp.tokword = nullptr;
   KernelParams kp = D.kp;
   void* args[] = {&kp, &sp, &D.kvmap};
-  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(false, false), dim3(D.plan.num_ctas), dim3(kThreads), args,
+  cudaError_t e = cudaLaunchCooperativeKernel(decode_kernel_ptr(false, false, D.kp.attn_mma != 0), dim3(D.plan.num_ctas), dim3(kThreads), args,
                                               (size_t)D.plan.smem_bytes, st);
   if (e == cudaErrorCooperativeLaunchTooLarge) return MBK_ERR_UNSUPPORTED;
   return e == cudaSuccess ? MBK_OK : MBK_ERR_CUDA;
