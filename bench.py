@@ -458,7 +458,7 @@ def measure_prefill(device: int, n: int = 4096):
             "attention_tflop": round(attn / 1e12, 3), "achieved_tflops": round(tf, 2),
             "peak_tflops": peak, "peak_kind": kind, "frac": round(tf / peak, 4),
             "note": "tensor cores run the projections twice (bf16 high/low input pair): overhead, not work; "
-                    "the causal attention runs on CUDA cores"}
+                    "the causal attention runs on the tensor cores as well (mma.sync, fp32 operands as bf16 pairs)"}
 
 
 def profiled_traffic(shape_name: str):

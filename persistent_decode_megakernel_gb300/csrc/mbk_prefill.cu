@@ -570,6 +570,212 @@ __global__ void __launch_bounds__(kAttnWarps * 32) prefill_attn_kernel(const Att
 }
 
 
+// ------------------------------------------------------------------ causal attention on the tensor cores
+// Head dim 64, at most 8 query heads per KV head.  One CTA: a tile of at most 32 (g <= 4) or 16 tokens of
+// one sequence and one KV head (mma_tile_tokens).  Its query rows are the (token, head) pairs, 16 per warp (row rho of the tile
+// is token rho / g, head rho % g), so the g heads of a group share every K/V block.  Keys come 64 at a
+// time, three buffers deep (one block barrier per block: a buffer refilled at block b was last read at
+// block b - 2), by cp.async into shared tiles of 128-byte rows with the 16-byte chunk c of row r
+// at chunk c ^ (r & 7) (the eight rows of a fragment load fall in eight bank groups); rows past the
+// tile's last position are zero-filled.  Per warp and block, on mma.sync m16n8k16 (bf16 operands, fp32
+// accumulation): S = Q K^T (B = K rows by ldmatrix) and O += P V (B = V rows by ldmatrix.trans), with S's
+// accumulator fragments reused as P's A fragments; the fp32 queries and probabilities enter as bf16
+// high/low pairs (x = hi + lo, relative error 2^-17 per operand; K and V are bf16 and enter exactly).
+// An online softmax per row (running max and sum, scores in base 2); a row stops mattering past its
+// token's position (masked to -inf).
+constexpr int kMmaKeys = 64;
+constexpr int kMmaBufs = 3;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ void hi_lo_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const float h0 = bf16f(to_bf16(x0)), h1 = bf16f(to_bf16(x1));
+  hi = pack_bf16x2(h0, h1);
+  lo = pack_bf16x2(x0 - h0, x1 - h1);
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// byte offset of 16-byte chunk c of row r in a [rows][128 B] swizzled tile
+__device__ __forceinline__ uint32_t swz_off(int r, int c) { return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4); }
+// 16-byte asynchronous copy global -> shared; zero-filled when !ok (src is then not read)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0) : "memory");
+}
+
+__global__ void __launch_bounds__(kMaxGroup / 2 * 32) prefill_attn_mma_kernel(const AttnArgs a) {
+  constexpr int D = 64;
+  __shared__ __align__(1024) unsigned char kvs[kMmaBufs][2][kMmaKeys * 128];  // [buffer][K, V][64 rows of 128 B]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int kvh = blockIdx.y, g = a.g;
+  // a tile's work grows with its position and the tiles are in increasing position order: the
+  // blocks take them from the last, so the longest start first and the short ones fill the tail
+  const int2 tile = a.tiles[gridDim.x - 1 - blockIdx.x];
+  const int t0 = tile.x, ntok = tile.y;
+  const int last = a.pos[t0 + ntok - 1];  // the tile's largest position (positions increase in a tile)
+  const int32_t* table = table_of(a.kv, a.seq[t0]);
+  // this lane's rows gid and gid + 8 of the warp; rows past the tile (ntok * g) run as position `last`
+  // with zero queries (finite, never written)
+  int rtok[2], rhead[2], rpos[2];
+  bool rok[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int rho = 16 * warp + gid + 8 * r;
+    rok[r] = rho < ntok * g;
+    rtok[r] = rok[r] ? rho / g : 0;
+    rhead[r] = rok[r] ? rho - rtok[r] * g : 0;
+    rpos[r] = rok[r] ? a.pos[t0 + rtok[r]] : last;
+  }
+  // A = Q: for k-step ks, a0 = (row gid, columns 16 ks + 2 tig, +1), a1 = (row gid + 8, same),
+  // a2 = (row gid, +8), a3 = (row gid + 8, +8); high and low parts
+  uint32_t qh[4][4], ql[4][4];
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = i & 1, col = 16 * ks + 2 * tig + ((i & 2) ? 8 : 0);
+      float2 x = make_float2(0.f, 0.f);
+      if (rok[r])
+        x = *reinterpret_cast<const float2*>(a.qkv + (size_t)(t0 + rtok[r]) * a.ld + (size_t)(kvh * g + rhead[r]) * D + col);
+      hi_lo_pair(x.x, x.y, qh[ks][i], ql[ks][i]);
+    }
+  }
+  float o[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  const int nblk = last / kMmaKeys + 1;
+  auto load = [&](int b) {  // key block b into buffer b % kMmaBufs: K rows, then V rows (16-byte pieces)
+    const int p0 = b * kMmaKeys;
+    const uint32_t base = saddr(&kvs[b % kMmaBufs][0][0]);
+    for (int e = threadIdx.x; e < 2 * kMmaKeys * 8; e += nthr) {
+      const int kv = e / (kMmaKeys * 8), r = (e >> 3) & (kMmaKeys - 1), c = e & 7, p = p0 + r;
+      const bool ok = p <= last;
+      const uint16_t* src = ok ? a.kv.kv + kv_index(a.kv, table, a.layer, kv, kvh, p) + c * 8 : a.kv.kv;
+      cp_async16(base + (uint32_t)kv * (kMmaKeys * 128) + swz_off(r, c), src, ok);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  load(0);
+  const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll 1
+  for (int b = 0; b < nblk; ++b) {
+    if (b + 1 < nblk) {
+      load(b + 1);  // its buffer was last read in block b - 2, before every warp passed block b - 1's barrier
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();  // block b has landed for every thread's copies
+    const int p0 = b * kMmaKeys;
+    const uint32_t kb = saddr(&kvs[b % kMmaBufs][0][0]), vb = saddr(&kvs[b % kMmaBufs][1][0]);
+    // S = Q K^T: n-tile n holds keys p0 + 8 n .. + 7; ldmatrix.x4 brings the B fragments of two n-tiles
+    float sc[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + swz_off(16 * np + ((mi >> 1) << 3) + rr, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+        mma_bf16_16816(sc[2 * np], qh[ks], b0, b1);
+        mma_bf16_16816(sc[2 * np], ql[ks], b0, b1);
+        mma_bf16_16816(sc[2 * np + 1], qh[ks], b2, b3);
+        mma_bf16_16816(sc[2 * np + 1], ql[ks], b2, b3);
+      }
+    }
+    // scale and mask: element k of n-tile n is (row gid + 8 (k >> 1), key p0 + 8 n + 2 tig + (k & 1))
+    float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int key = p0 + 8 * n + 2 * tig + (k & 1);
+        sc[n][k] = key <= rpos[k >> 1] ? sc[n][k] * a.scale_log2 : -INFINITY;
+      }
+      bm0 = fmaxf(bm0, fmaxf(sc[n][0], sc[n][1]));
+      bm1 = fmaxf(bm1, fmaxf(sc[n][2], sc[n][3]));
+    }
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 1));
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 2));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 1));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 2));
+    // key 0 <= every row's position, so the first block gives every row a finite max; a later block
+    // whose keys are all past a row's position leaves that row's max as it was
+    const float nm0 = fmaxf(m0, bm0), nm1 = fmaxf(m1, bm1);
+    const float al0 = exp2f(m0 - nm0), al1 = exp2f(m1 - nm1);
+    m0 = nm0;
+    m1 = nm1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      sc[n][0] = exp2f(sc[n][0] - m0);
+      sc[n][1] = exp2f(sc[n][1] - m0);
+      sc[n][2] = exp2f(sc[n][2] - m1);
+      sc[n][3] = exp2f(sc[n][3] - m1);
+      ps0 += sc[n][0] + sc[n][1];
+      ps1 += sc[n][2] + sc[n][3];
+      o[n][0] *= al0;
+      o[n][1] *= al0;
+      o[n][2] *= al1;
+      o[n][3] *= al1;
+    }
+    l0 = fmaf(l0, al0, ps0);
+    l1 = fmaf(l1, al1, ps1);
+    // O += P V: k-step kk covers keys 16 kk .. + 15 (n-tiles 2 kk, 2 kk + 1 of S as P's A fragment)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t ph[4], pl[4];
+      hi_lo_pair(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+      hi_lo_pair(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+      hi_lo_pair(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+      hi_lo_pair(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+      for (int dp = 0; dp < 4; ++dp) {  // dims 16 dp .. + 15: two n-tiles
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + swz_off(16 * kk + ((mi & 1) << 3) + rr, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], ph, b0, b1);
+        mma_bf16_16816(o[2 * dp], pl, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], ph, b2, b3);
+        mma_bf16_16816(o[2 * dp + 1], pl, b2, b3);
+      }
+    }
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const size_t qd = (size_t)a.nq * D;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (!rok[r]) continue;
+    const float inv = 1.f / (r ? l1 : l0);
+    const size_t base = (size_t)(t0 + rtok[r]) * qd + (size_t)(kvh * g + rhead[r]) * D + 2 * tig;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      split_store(o[n][2 * r] * inv, a.o_hi, a.o_lo, base + 8 * n);
+      split_store(o[n][2 * r + 1] * inv, a.o_hi, a.o_lo, base + 8 * n + 1);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ host side
 // cuTensorMapEncodeTiled, looked up through the runtime (no link against the driver library).
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -638,6 +844,12 @@ cudaError_t gemm(const PrefillModel& m, const CUtensorMap& a_hi, const CUtensorM
   return cudaGetLastError();
 }
 
+// The tensor-core attention takes head dim 64 with at most 8 query heads per KV head; its tiles hold
+// 32 tokens up to 4 query heads per KV head and 16 beyond, so tokens x g heads make at most 8 warps of
+// 16 rows.
+bool mma_attention(const PrefillModel& m) { return m.d == 64 && m.nq / m.nkv <= kMaxGroup / 2; }
+int mma_tile_tokens(const PrefillModel& m) { return m.nq / m.nkv <= 4 ? 32 : 16; }
+
 cudaError_t attention(const PrefillModel& m, const PrefillState& s, const KvGeom& geom, int layer, int ntiles,
                       cudaStream_t st) {
   AttnArgs a;
@@ -654,7 +866,10 @@ cudaError_t attention(const PrefillModel& m, const PrefillState& s, const KvGeom
   a.o_hi = s.a_hi;
   a.o_lo = s.a_lo;
   const dim3 grid((unsigned)ntiles, (unsigned)m.nkv);
-  if (m.d == 64)
+  if (mma_attention(m)) {
+    // (tile tokens * g) / 16 warps
+    prefill_attn_mma_kernel<<<grid, (unsigned)(mma_tile_tokens(m) * a.g / 16 * 32), 0, st>>>(a);
+  } else if (m.d == 64)
     prefill_attn_kernel<64><<<grid, kAttnWarps * 32, attn_smem<64>(a.g), st>>>(a);
   else
     prefill_attn_kernel<128><<<grid, kAttnWarps * 32, attn_smem<128>(a.g), st>>>(a);
@@ -691,8 +906,8 @@ bool ensure_workspace(const PrefillModel& m, PrefillState& s, int n) {
 
 // The int region of the workspace as one host image [tokens | pos | seq | rows | tiles] (cap entries
 // each, tiles two): the positions and sequence of every token, the last token of every sequence, and
-// the attention tiles (at most kAttnWarps consecutive tokens of one sequence).  Returns the tile count.
-int pack_tokens(const PrefillBatch& b, const int32_t* tokens, int n, int cap, std::vector<int32_t>& img) {
+// the attention tiles (at most tile_tokens consecutive tokens of one sequence).  Returns the tile count.
+int pack_tokens(const PrefillBatch& b, const int32_t* tokens, int n, int cap, int tile_tokens, std::vector<int32_t>& img) {
   img.assign((size_t)6 * cap, 0);
   int32_t* tok = img.data();
   int32_t* pos = tok + cap;
@@ -705,9 +920,9 @@ int pack_tokens(const PrefillBatch& b, const int32_t* tokens, int n, int cap, st
       tok[t] = tokens[t];
       pos[t] = b.starts[q] + i;
       seq[t] = q;
-      if (i % kAttnWarps == 0) {
+      if (i % tile_tokens == 0) {
         tiles[2 * nt] = t;
-        tiles[2 * nt + 1] = std::min(kAttnWarps, b.counts[q] - i);
+        tiles[2 * nt + 1] = std::min(tile_tokens, b.counts[q] - i);
         ++nt;
       }
     }
@@ -779,7 +994,7 @@ int prefill_run(const PrefillModel& m, PrefillState& s, const int32_t* tokens_ho
       !make_map(&al_q, s.a_lo, n, qd) || !make_map(&ah_I, s.a_hi, n, m.I) || !make_map(&al_I, s.a_lo, n, m.I))
     return MBK_ERR_UNSUPPORTED;
   std::vector<int32_t> img;
-  const int ntiles = pack_tokens(batch, tokens_host, n, s.cap, img);
+  const int ntiles = pack_tokens(batch, tokens_host, n, s.cap, mma_attention(m) ? mma_tile_tokens(m) : kAttnWarps, img);
   if (cudaMemcpyAsync(s.tokens, img.data(), sizeof(int32_t) * img.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MBK_ERR_CUDA;
   KvGeom geom{m.kv, m.page_table, 0, m.page_size, m.page_shift, m.nkv, m.d, m.page_elems};
