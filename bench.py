@@ -498,9 +498,14 @@ def main():
                     help="fp8: stream the library's FP8 (E4M3, per-row scale) copies of the weights")
     ap.add_argument("--steps-per-call", type=int, default=0,
                     help="teacher-forced steps per launch (default: the workload's positions; 1 = one launch per step)")
+    ap.add_argument("--prefill-only", type=int, default=0, metavar="N",
+                    help="diagnostics: time one N-token prefill (as config.prefill does) and print its line only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.prefill_only > 0:
+        print(json.dumps(measure_prefill(0, args.prefill_only)))
+        return
     if args.impl == "reference":
         run_reference(args, args.config)
     else:
