@@ -477,11 +477,16 @@ def profiled_traffic(shape_name: str):
 
 
 def _kernel_hash() -> str:
+    """Hash of the decode kernel's code: its sources with comments and whitespace removed, so that a
+    comment-only edit keeps the committed ncu counters."""
     import hashlib
     h = hashlib.sha256()
     for f in ("mbk_kernel.cu", "mbk_plan.h", "mbk_device.h", "mbk_sched.cpp"):
-        with open(os.path.join(_ROOT, "persistent_decode_megakernel_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(_ROOT, "persistent_decode_megakernel_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

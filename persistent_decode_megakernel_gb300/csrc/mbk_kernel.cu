@@ -4,18 +4,20 @@
 // and why small models want one": resident CTAs working through a task list and synchronising
 // through global memory).  Every CTA runs 12 warps:
 //   warp 0      streams the weights of its upcoming tasks into a ring of shared-memory stages with
-//               TMA bulk copies (cp.async.bulk + mbarrier transaction counts).  Weights do not depend
-//               on the token, so the stream runs ahead of the data dependencies by up to the ring's
-//               depth -- the "cross-phase prefetch of the next GEMM's weights while a CTA waits" the
-//               article lists as future work ("Checking the 5.5x").
+//               TMA bulk copies (cp.async.bulk + mbarrier transaction counts), and an attention
+//               task's cached K/V rows as 2-D TMA tiles with the 128-byte swizzle the tensor-core
+//               attention reads.  Weights do not depend on the token, so the stream runs ahead of the
+//               data dependencies by up to the ring's depth -- the "cross-phase prefetch of the next
+//               GEMM's weights while a CTA waits" the article lists as future work ("Checking the 5.5x").
 //   warps 1-11  execute the CTA's tasks in order.  Activations move between CTAs as 64-bit words
 //               {tag:32 | fp32 value:32}, each written once per step by exactly one thread; a reader
 //               polls the word until its tag equals this step's tag.  A value and its readiness
 //               travel in one single-copy-atomic store, so no fence, counter or grid barrier is
 //               needed (the pages' counting grid barrier is the thing this replaces).
 // The step is a long chain of small dependent tasks, so the kernel is built for latency: one code
-// path serves every projection type and one serves attention, keeping the instructions of a task
-// hot in the instruction cache; a projection row's output word is written by the warp that
+// path serves every projection type and one serves attention (its blocks on the tensor cores, or on
+// the CUDA cores in a separate instantiation), keeping the instructions of a task hot in the
+// instruction cache; a projection row's output word is written by the warp that
 // computed it the moment its dot product is done; token-independent loads (norm gains, biases,
 // descriptors) are issued before a task waits for its inputs and consumed after.
 // Every wait is bounded by a globaltimer budget; on expiry the CTA records timeout status and
