@@ -342,7 +342,16 @@ typedef struct {
  * covered exactly once, every task's inputs produced by an earlier task in every CTA's order,
  * every bulk copy 16-byte aligned and within its tensor) and fills *info.  Returns MBK_OK,
  * MBK_ERR_INVALID_ARG for a shape the kernel does not support, or MBK_ERR_STATE when a check
- * fails.  Weight addresses are taken from a fake base so no device memory is needed. */
+ * fails.  Weight addresses are taken from a fake base so no device memory is needed.
+ *
+ * Environment knobs read wherever a schedule is built (mbk_create, mbk_create_paged,
+ * mbk_decode_step_static, mbk_plan_check, mbk_plan_simulate), all for experiments, defaults best
+ * measured: MBK_MAX_TASKS_PER_OP (at most this many CTAs per projection), MBK_FUSE_ATTENTION (0: the
+ * O projection as tasks of its own), MBK_ATTN_MMA (0: attention on the CUDA cores instead of the
+ * tensor cores), MBK_ATTN_SPLIT (context split length, a multiple of 64; default 512) and
+ * MBK_COMBINE_TASKS (O-projection tasks of a split context; default one per 24 output rows).  At
+ * launch: MBK_WAIT_TIMEOUT_MS (bounded waits, default 1000) and MBK_POLL_BACKOFF_NS (sleep between
+ * polls, default 0). */
 int mbk_plan_check(const mbk_config *cfg, int num_sms, mbk_plan_info *info);
 
 /* Execution model of the schedule's exchange protocol (host only; no GPU needed).  Builds the plan as
@@ -353,8 +362,7 @@ int mbk_plan_check(const mbk_config *cfg, int num_sms, mbk_plan_info *info);
  * grows within a step, so if tasks remain when no task is ready the plan can deadlock on the GPU
  * whatever the timing (the kernel's bounded waits would then report MBK_ERR_TIMEOUT).  The depths
  * count exchange rounds: the longest chain of tasks each reading a word its predecessor wrote.  The
- * same environment knobs as a handle apply (MBK_MAX_TASKS_PER_OP, MBK_FUSE_ATTENTION and the
- * fault-injection knob MBK_DEBUG_DROP_TASK).  Returns MBK_OK when every task ran and no word was
+ * same environment knobs as mbk_plan_check apply, and the fault-injection knob MBK_DEBUG_DROP_TASK.  Returns MBK_OK when every task ran and no word was
  * written twice, MBK_ERR_STATE otherwise (details in *info), MBK_ERR_INVALID_ARG for a bad argument
  * or an unsupported shape. */
 typedef struct {
